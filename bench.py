@@ -1,0 +1,430 @@
+#!/usr/bin/env python
+"""Benchmark of split-KV decode attention on one GB300 (or N replicas).
+
+Workload timed by default: the unified-cache multi-sequence decode -- a
+shared fp16 cell-major cache of 262144 rows x 8 KV heads x 128 (1 GiB of K+V),
+8 sequences with one query token and 32 q heads each, every sequence reading
+its own 32768 rows through a sorted row list (the cache's rows are split among
+the sequences).  One step = one skv_attn_partial call: split planning, the
+gathered-row split-KV decode kernel and the log-sum-exp combine.
+
+Printed: one JSON line (rank 0) with the throughput in GB/s of algorithmic
+K/V bytes, the decode kernel's roofline fraction against the measured HBM
+copy bandwidth, an end-to-end number through the C ABI with the inputs copied
+from pinned host memory every step, the fp64 CPU oracle timed on a bounded
+sample on the host cores, and the SM clocks sampled during the timed region.
+``--impl reference`` times the CPU oracle as the reference arm instead.
+
+Extra measurements (window + host tail stream with q8_0/q4_0 rows, pinned
+host->device copy bandwidth, tiny decode latency) go under "extra".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode attn KV GB/s & % of HBM roofline; tail H2D GB/s; tokens·heads/s"
+WORKLOAD = "unified_cache_multiseq_decode"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-extras", action="store_true")
+    p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline sample")
+    return p.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p.get("bf16_tflops", 1900.0)), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (getattr(self, "out", "") or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sms.append(float(f[1]))
+                maxes.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes), "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+def profile_traffic(kernel_src: str, profile_name: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the kernel source as it is now (its sha256 prefix is recorded beside it)."""
+    path = os.path.join(ROOT, "profiles", profile_name)
+    try:
+        txt = open(path).read()
+        with open(kernel_src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        rec = {}
+        for line in txt.splitlines():
+            if ":" in line and line.strip().startswith(("- ", "* ")):
+                k, v = line.strip()[2:].split(":", 1)
+                rec[k.strip()] = v.strip().strip("`")
+        if rec.get("kernel_source_sha256") == sha and "dram_bytes_per_launch_full_size" in rec:
+            return float(rec["dram_bytes_per_launch_full_size"])
+    except Exception:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    from split_kv_flash_attn_gb300 import workloads as wl
+    oracle.build()
+    w = wl.unified_decode()
+    cores = oracle.max_threads()
+    bytes_per_seq = w.kv_rows.shape[1] * w.Hk * w.D * 2 * 2
+    times = []
+    for i in range(args.warmup + args.steps):
+        s = i % w.S
+        t0 = time.perf_counter()
+        oracle.attention(w.q[s:s + 1], D=w.D, H=w.H, Hk=w.Hk, scale=w.scale, k0=w.k, v0=w.v,
+                         n_rows0=w.k.shape[0], k_row_bytes0=w.k.shape[1], v_row_bytes0=w.v.shape[1],
+                         n_keys=w.n_keys, kv_rows=w.kv_rows[s:s + 1])
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    sec = statistics.mean(times)
+    value = bytes_per_seq / sec / 1e9
+    sample = f"one of the 8 sequences per step (32768 rows x 8 KV heads x 32 q heads, {bytes_per_seq} B)"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "S": 8, "H": 32, "Hk": 8, "D": 128, "n_cache": 262144,
+                   "rows_per_seq": 32768},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from split_kv_flash_attn_gb300 import build as skv_build
+    if not os.path.exists(skv_build.LIB):
+        skv_build.build()
+    import split_kv_flash_attn_gb300 as skv
+    from split_kv_flash_attn_gb300 import workloads as wl
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        t = torch.tensor([x], device="cuda", dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    hbm_peak, _, peak_kind = peaks()
+    w = wl.unified_decode()
+    h = skv.Handle(local)
+    q = torch.from_numpy(w.q).cuda()
+    K = torch.from_numpy(w.k).cuda()
+    V = torch.from_numpy(w.v).cuda()
+    rows = torch.from_numpy(w.kv_rows).cuda()
+    o = torch.empty((w.S, 1, w.H, w.D), dtype=torch.float32, device="cuda")
+    lse = torch.empty((w.S, 1, w.H), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    n_valid = int((w.kv_rows >= 0).sum())
+    algo_bytes = n_valid * w.Hk * w.D * 2 * 2              # K + V head segments actually gathered
+    tokens_heads = w.S * w.H
+
+    def step():
+        skv.attn_partial(h, q, K, V, Hk=w.Hk, kv_rows=rows, o=o, lse=lse, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    K_ = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K_)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K_)]
+    for a, b in kev:                        # materialise the events before handing them to the library
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        for i in range(K_):
+            ev[i][0].record(stream)
+            h.set_profile_events(kev[i][0], kev[i][1])
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    h.set_profile_events(None, None)
+    step_ms = sum(a.elapsed_time(b) for a, b in ev) / K_
+    kern_ms = sum(a.elapsed_time(b) for a, b in kev) / K_
+    step_ms = max_over_ranks(step_ms)
+    value = algo_bytes * world / (step_ms * 1e-3) / 1e9
+    achieved = algo_bytes / (kern_ms * 1e-3) / 1e9
+    _, n_splits = skv.plan_splits(w.kv_rows.shape[1], w.S * w.Hk, h.sm_count(), 2, 64, 2048)
+    launches_per_step = 1 + (1 if n_splits > 1 else 0)
+
+    # ---- end to end through the C ABI with host buffers ---------------------
+    e2e = None
+    try:
+        hq, hK, hV, hrows = (torch.from_numpy(x).pin_memory() for x in (w.q, w.k, w.v, w.kv_rows))
+        ho = torch.empty(o.shape, dtype=torch.float32).pin_memory()
+        hl = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+        dq, dK, dV, drows = (torch.empty_like(x, device="cuda") for x in (hq, hK, hV, hrows))
+
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            dK.copy_(hK, non_blocking=True)
+            dV.copy_(hV, non_blocking=True)
+            drows.copy_(hrows, non_blocking=True)
+            skv.attn_partial(h, dq, dK, dV, Hk=w.Hk, kv_rows=drows, o=o, lse=lse, stream=stream)
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_e2e = max(3, K_ // 2)
+        barrier()
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e)
+        h2d = sum(x.numel() * x.element_size() for x in (hq, hK, hV, hrows))
+        d2h = ho.numel() * 4 + hl.numel() * 4
+        e2e = {"value": algo_bytes * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        del hK, hV, dK, dV
+    except Exception as exc:  # noqa: BLE001 -- report, do not lose the main line
+        e2e = {"value": None, "unit": "GB/s", "error": repr(exc)[:200]}
+
+    # ---- CPU oracle baseline on a bounded sample (rank 0) --------------------
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        try:
+            import oracle
+            oracle.build()
+            t0 = time.perf_counter()
+            oracle.attention(w.q[0:1], D=w.D, H=w.H, Hk=w.Hk, scale=w.scale, k0=w.k, v0=w.v,
+                             n_rows0=w.k.shape[0], k_row_bytes0=w.k.shape[1], v_row_bytes0=w.v.shape[1],
+                             n_keys=w.n_keys, kv_rows=w.kv_rows[0:1])
+            sec = time.perf_counter() - t0
+            sb = int((w.kv_rows[0] >= 0).sum()) * w.Hk * w.D * 4
+            cpu = {"value": sb / sec / 1e9, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
+                   "sample": f"sequence 0 of 8 (32 q heads x 32768 gathered rows, {sb} B), {sec:.2f} s"}
+        except Exception as exc:  # noqa: BLE001
+            cpu = {"value": None, "unit": "GB/s", "cores": None, "kind": "oracle", "sample": repr(exc)[:200]}
+
+    extra = {}
+    if not args.no_extras and rank == 0:
+        extra = run_extras(torch, skv, wl, h, hbm_peak)
+
+    traffic = profile_traffic(os.path.join(ROOT, "split_kv_flash_attn_gb300", "csrc", "decode_kernel.cuh"),
+                              "splitkv_decode_unified_cache.md")
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K_, "warmup": args.warmup,
+        "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "S": w.S, "nq": 1, "H": w.H, "Hk": w.Hk, "D": w.D,
+                   "n_cache": w.k.shape[0], "rows_per_seq": 32768, "kv_dtype": "f16", "accumulate": "f32",
+                   "l2": "inputs larger than L2: 1 GiB of K/V gathered per step vs 126 MB L2",
+                   "parallelism": f"replicas x{world}"},
+        "tokens_heads_per_s": tokens_heads * world / (step_ms * 1e-3),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": traffic,
+                     "kernel": "splitkv_decode_kernel<128,f16,f16>", "kernel_ms": kern_ms,
+                     "peak_kind": f"{peak_kind} (hbm_gbs, STREAM-style copy)"},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K_,
+        "clocks": clk.summary(),
+        "extra": extra,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def run_extras(torch, skv, wl, h, hbm_peak):
+    """Window + host-tail decode with q8_0 K / q4_0 V (1,048,576 rows), the
+    pinned host->device copy bandwidth at the tail's tile size, and the tiny
+    decode's latency."""
+    out = {}
+    stream = torch.cuda.current_stream()
+    try:
+        w = wl.long_context_decode()
+        q = torch.from_numpy(w.q).cuda()
+        kw_, vw_ = torch.from_numpy(w.k).cuda(), torch.from_numpy(w.v).cuda()
+        kt, vt = torch.from_numpy(w.k_tail).pin_memory(), torch.from_numpy(w.v_tail).pin_memory()
+        o = torch.empty((1, 1, w.H, w.D), dtype=torch.float32, device="cuda")
+        lse = torch.empty((1, 1, w.H), dtype=torch.float32, device="cuda")
+        # window alone: the decode kernel over 131072 quantised rows in HBM
+        b, a = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b.record(stream)
+        a.record(stream)
+        for _ in range(3):
+            skv.attn_partial(h, q, kw_, vw_, Hk=w.Hk, k_type=w.k_type, v_type=w.v_type, o=o, lse=lse)
+        torch.cuda.synchronize()
+        h.set_profile_events(b, a)
+        ks = []
+        for _ in range(10):
+            skv.attn_partial(h, q, kw_, vw_, Hk=w.Hk, k_type=w.k_type, v_type=w.v_type, o=o, lse=lse)
+            torch.cuda.synchronize()
+            ks.append(b.elapsed_time(a))
+        h.set_profile_events(None, None)
+        win_bytes = w.k.nbytes + w.v.nbytes
+        win_ms = statistics.median(ks)
+        out["long_context_window"] = {"rows": w.k.shape[0], "bytes": win_bytes, "kernel_ms": win_ms,
+                                      "GBps": win_bytes / win_ms / 1e6, "frac_hbm": win_bytes / win_ms / 1e6 / hbm_peak}
+        # whole call: window + 28 streamed tail tiles + combine
+        for _ in range(2):
+            skv.attn_window_tail(h, q, kw_, vw_, kt, vt, Hk=w.Hk, tile_rows=w.tile_rows, k_type=w.k_type,
+                                 v_type=w.v_type, o=o, lse=lse)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        n = 5
+        for _ in range(n):
+            skv.attn_window_tail(h, q, kw_, vw_, kt, vt, Hk=w.Hk, tile_rows=w.tile_rows, k_type=w.k_type,
+                                 v_type=w.v_type, o=o, lse=lse)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        call_ms = e0.elapsed_time(e1) / n
+        tail_bytes = w.k_tail.nbytes + w.v_tail.nbytes
+        # pinned H2D microbenchmark with the same transfer sizes (one K and one V tile copy)
+        tk = w.tile_rows * w.k.shape[1]
+        tv = w.tile_rows * w.v.shape[1]
+        dst = torch.empty(tk + tv, dtype=torch.uint8, device="cuda")
+        src = torch.from_numpy(np.ascontiguousarray(w.k_tail[:w.tile_rows]).reshape(-1)).pin_memory()
+        srcv = torch.from_numpy(np.ascontiguousarray(w.v_tail[:w.tile_rows]).reshape(-1)).pin_memory()
+        for _ in range(3):
+            dst[:tk].copy_(src, non_blocking=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        reps = 20
+        for _ in range(reps):
+            dst[:tk].copy_(src, non_blocking=True)
+            dst[tk:].copy_(srcv, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        h2d_gbs = reps * (tk + tv) / (e0.elapsed_time(e1) * 1e-3) / 1e9
+        tail_gbs = tail_bytes / (call_ms * 1e-3) / 1e9
+        out["long_context_window_tail"] = {
+            "n_kv": w.extra["n_kv"], "wc": w.extra["wc"], "tile_rows": w.tile_rows, "tail_bytes": tail_bytes,
+            "call_ms": call_ms, "tail_stream_GBps": tail_gbs, "pinned_h2d_GBps": h2d_gbs,
+            "frac_of_pinned_h2d": tail_gbs / h2d_gbs, "tokens_heads_per_s": w.H / (call_ms * 1e-3)}
+        del kw_, vw_, kt, vt, dst, src, srcv
+    except Exception as exc:  # noqa: BLE001
+        out["long_context_error"] = repr(exc)[:300]
+    try:
+        w = wl.tiny_decode()
+        q = torch.from_numpy(w.q).cuda()
+        kw_, vw_ = torch.from_numpy(w.k).cuda(), torch.from_numpy(w.v).cuda()
+        kt, vt = torch.from_numpy(w.k_tail).pin_memory(), torch.from_numpy(w.v_tail).pin_memory()
+        for _ in range(5):
+            skv.attn_window_tail(h, q, kw_, vw_, kt, vt, Hk=w.Hk, tile_rows=w.tile_rows)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        n = 50
+        for _ in range(n):
+            skv.attn_window_tail(h, q, kw_, vw_, kt, vt, Hk=w.Hk, tile_rows=w.tile_rows)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) / n * 1e3
+        out["tiny_decode_window_tail"] = {"us_per_call": us, "tokens_heads_per_s": w.H / (us * 1e-6)}
+    except Exception as exc:  # noqa: BLE001
+        out["tiny_error"] = repr(exc)[:300]
+    return out
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,212 @@
+/*
+ * splitkv.h -- C ABI of libsplitkv.so: split-KV flash attention over a
+ * partitioned KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * The method.  Attention over a long key list is computed per key partition,
+ * each partition giving a normalised partial output O_t and its log-sum-exp
+ * lse_t; partials merge exactly by
+ *     M = max_t lse_t,  O = sum_t e^{lse_t - M} O_t / sum_t e^{lse_t - M},
+ *     lse = M + ln sum_t e^{lse_t - M}
+ * ("Rolling KV -- position-windowed KV residency", opencoti patch 0070,
+ * fattn.cu key-axis tiling and streaming_combine_kernel).  Partitions are a
+ * device-resident position window [0, wc) plus a pinned-host tail [wc, n_kv)
+ * (same page, two-region forward), or a per-sequence row list into a shared
+ * cache with -1 padding ("llama + CUDA: flash_attn_ext_rows (fix unified kv
+ * for multi-seq)", the op's doc comment), or pages of a device block cache
+ * over a pinned host copy ("Strata compare", KV streaming).
+ *
+ * Conventions shared by every entry point.
+ *  - Every function returns an int status (SKV_OK = 0) and never exits or
+ *    aborts.  skv_last_error(h) gives a message for the last failure on h.
+ *  - Pointers named *_host are host memory; every other data pointer is
+ *    device memory (cudaMalloc / torch CUDA tensors).  The caller owns all
+ *    tensors; the handle owns only its streams, events, workspace, ring and
+ *    block-cache state.
+ *  - Calls are asynchronous and ordered on the caller's `stream` (a
+ *    cudaStream_t passed as void*; NULL is the legacy default stream).
+ *    Errors found on the host return at once; nothing waits on the GPU
+ *    unless a function says so.
+ *  - Calls that share one handle must be ordered with respect to each other
+ *    (one stream, or caller-side events): they share the handle's workspace
+ *    and ring.
+ *  - Scratch (workspace, ring) grows on demand and never shrinks.  Growth
+ *    calls cudaMalloc, which is refused with SKV_ECAPTURE while `stream` is
+ *    capturing a CUDA graph; call skv_reserve() beforehand.
+ *
+ * Layouts.
+ *  - q:   fp16 [S][nq][H][D] (row-major).
+ *  - A cache row holds all Hk KV heads of one position, head after head
+ *    ("cell-major"); head k's data starts at byte k * seg, where seg = 2*D
+ *    (f16), 34*D/32 (q8_0) or 18*D/32 (q4_0); consecutive rows are
+ *    k_row_bytes / v_row_bytes apart.
+ *  - q8_0 block (34 B): fp16 scale d, 32 int8 codes q; value = d*q.
+ *    q4_0 block (18 B): fp16 scale d, 16 bytes; byte j holds u_j in its low
+ *    nibble and u_{j+16} in its high nibble; value = d*(u-8).  (The pages name
+ *    these 32-value block types but do not print their bytes; this is the
+ *    usual ggml layout.)
+ *  - GQA: q head h uses KV head h / (H/Hk).
+ *  - Outputs: o fp32 [S][nq][H][D] (normalised), lse fp32 [S][nq][H] in
+ *    natural log.  A row that sees no key gets o = 0 and lse = -inf.
+ *  - Optional additive mask: fp16 [S][nq][mask_ld], column = logical key
+ *    index.  Optional causal positions q_pos int32 [S][nq]: logical key j is
+ *    visible to token t iff key_pos0 + j <= q_pos[s][t].
+ */
+#ifndef SPLITKV_H
+#define SPLITKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------- */
+#define SKV_OK 0
+#define SKV_EINVAL 1         /* bad argument (null pointer, size, shape)       */
+#define SKV_EUNSUPPORTED 2   /* shape/type/alignment this build does not cover */
+#define SKV_ENOTPINNED 3     /* a *_host pointer is not page-locked host memory */
+#define SKV_ENOMEM 4         /* device or pinned allocation failed             */
+#define SKV_ECAPTURE 5       /* scratch must grow while the stream captures    */
+#define SKV_ECUDA 6          /* a CUDA runtime call failed                     */
+#define SKV_ETIMEOUT 7       /* a device-side wait gave up (bounded spin)      */
+#define SKV_EDEVICE 8        /* the device status word reports a violation     */
+
+/* ---- element types of cache rows -------------------------------------- */
+#define SKV_F16 0
+#define SKV_Q8_0 1
+#define SKV_Q4_0 2
+
+typedef struct skv_handle skv_handle;
+
+typedef struct skv_shape {
+    int32_t S;           /* sequences                                       */
+    int32_t nq;          /* query tokens per sequence                       */
+    int32_t H;           /* query heads                                     */
+    int32_t Hk;          /* KV heads; H % Hk == 0                           */
+    int32_t D;           /* head dim (Dk = Dv): 64 or 128                    */
+    float scale;         /* score scale, usually 1/sqrt(D)                  */
+    int32_t k_type;      /* SKV_F16 / SKV_Q8_0 / SKV_Q4_0                    */
+    int32_t v_type;
+    int64_t k_row_bytes; /* byte stride between consecutive cache rows      */
+    int64_t v_row_bytes;
+} skv_shape;
+
+/* ---- handle ---------------------------------------------------------- */
+
+/* Create a handle on `device` (makes it current): a copy stream, the
+ * double-buffer events and an error buffer.  No scratch is allocated yet. */
+int skv_create(int device, skv_handle **out);
+
+/* Free the handle's scratch, events and stream.  Synchronises the device. */
+int skv_destroy(skv_handle *h);
+
+/* Message of the last failure on h (never NULL; "" after success). */
+const char *skv_last_error(const skv_handle *h);
+
+/* Static text for a status code. */
+const char *skv_status_string(int status);
+
+/* Grow the workspace (partial outputs) to at least workspace_bytes and the
+ * tail ring to n_slots (<= 4) slots of ring_bytes_per_slot each.  Call
+ * outside graph capture.  Synchronous with respect to earlier work on h. */
+int skv_reserve(skv_handle *h, size_t workspace_bytes, size_t ring_bytes_per_slot, int32_t n_slots);
+
+/* Current scratch sizes (bytes), for inspection. */
+int skv_scratch_info(const skv_handle *h, size_t *workspace_bytes, size_t *ring_bytes_per_slot,
+                     int32_t *n_slots);
+
+/* Number of SMs of the handle's device. */
+int skv_sm_count(const skv_handle *h, int32_t *out);
+
+/* Profiling hook.  When `before`/`after` (cudaEvent_t passed as void*) are
+ * non-NULL, every later launch of the attention kernel (the split-KV decode
+ * kernel) is bracketed by cudaEventRecord(before) / cudaEventRecord(after) on
+ * the stream it is launched on, so a caller can time that kernel alone.
+ * With several attention launches in one call, the events end up around the
+ * last one.  Pass NULLs to switch the hook off. */
+int skv_set_profile_events(skv_handle *h, void *before, void *after);
+
+/* ---- host-side planning (pure host logic; no GPU needed) --------------- */
+
+/* Split a key range of n_keys keys, shared by n_units independent
+ * (sequence, KV head, column group) units, into n_splits pieces of split_len
+ * keys (a multiple of `tile`, at most max_split keys when max_split > 0) so
+ * that units * n_splits CTAs fill whole waves of sm_count * ctas_per_sm.
+ * The last piece may be shorter.  The tile-count policy of the Rolling KV
+ * patch (coarse key tiles to cut launch overhead, tiles aligned to the
+ * kernel's key stride) chose tiles per launch; here one launch covers every
+ * split and the policy chooses split sizes instead. */
+int skv_plan_splits(int64_t n_keys, int64_t n_units, int32_t sm_count, int32_t ctas_per_sm,
+                    int32_t tile, int64_t max_split, int64_t *split_len, int32_t *n_splits);
+
+/* ---- attention ------------------------------------------------------- */
+
+/* Attention of every (s, t, h) row over logical keys [kv_begin, kv_end) of a
+ * cache (key_offset semantics below), written as one normalised result:
+ *   kv_rows == NULL : logical key j reads cache row j.
+ *   kv_rows != NULL : logical key j of sequence s reads cache row
+ *                     kv_rows[s*kv_rows_ld + j] (kv_rows_per_head == 0) or
+ *                     kv_rows[(s*Hk + k)*kv_rows_ld + j] (== 1); a negative
+ *                     entry is padding: nothing is read and the key is absent
+ *                     (flash_attn_ext_rows semantics).  Key tiles whose rows
+ *                     are all padding issue no memory reads.
+ * Mask column and causal position of logical key j: column j, position
+ * key_pos0 + j.  k, v are device pointers to row 0 of the cache.
+ * Internally the range is split across CTAs (skv_plan_splits) and the
+ * partials are merged by the log-sum-exp combine; o/lse receive the merged
+ * result.  Errors: SKV_EINVAL (shape), SKV_EUNSUPPORTED (D not 64/128, a
+ * type pairing or alignment the kernels do not cover), SKV_ECAPTURE. */
+int skv_attn_partial(skv_handle *h, const skv_shape *shape,
+                     const void *q, const void *k, const void *v,
+                     const void *mask, int64_t mask_ld,
+                     const int32_t *q_pos, int64_t key_pos0,
+                     const int32_t *kv_rows, int64_t kv_rows_ld, int32_t kv_rows_per_head,
+                     int64_t kv_begin, int64_t kv_end,
+                     float *o, float *lse, void *stream);
+
+/* Log-sum-exp combine (formula at the top of this file) of n_parts partial
+ * results: o_parts fp32 [n_parts][rows][D], lse_parts fp32 [n_parts][rows]
+ * -> o [rows][D], lse [rows].  A part with lse = -inf contributes nothing
+ * (its o is never read); every part -inf gives o = 0, lse = -inf.
+ * n_parts = 0 is allowed (fills o = 0, lse = -inf). */
+int skv_attn_combine(skv_handle *h, int32_t n_parts, const float *o_parts, const float *lse_parts,
+                     int64_t rows, int32_t D, float *o, float *lse, void *stream);
+
+/* Window + host-tail attention (Rolling KV patch two-region forward, with
+ * the bulk raw-byte lift and persistent scratch ring of opencoti patch 0102).
+ * Logical keys [0, n_win) are window rows k_win/v_win (device); logical keys
+ * [n_win, n_win + n_tail) are rows of k_tail_host/v_tail_host, which must be
+ * page-locked host memory (SKV_ENOTPINNED otherwise).  The tail is cut into
+ * tiles of tile_rows rows (<= 0: 32768); each tile's raw bytes (any of the
+ * three types) are copied in one cudaMemcpyAsync per K/V into a ring slot on
+ * the handle's copy stream, while the window and earlier tiles compute on
+ * `stream`; copy_done/compute_done events order slot reuse.  All partials
+ * merge in one combine into o/lse.  Ring slots hold tile_rows rows and grow
+ * only outside capture. */
+int skv_attn_window_tail(skv_handle *h, const skv_shape *shape, const void *q,
+                         const void *k_win, const void *v_win, int64_t n_win,
+                         const void *k_tail_host, const void *v_tail_host, int64_t n_tail,
+                         int64_t tile_rows,
+                         const void *mask, int64_t mask_ld, const int32_t *q_pos,
+                         float *o, float *lse, void *stream);
+
+/* ---- quantised rows and gathers (bit-exact test hooks) ------------------ */
+
+/* Decode n_values (multiple of 32) values of q8_0 / q4_0 blocks into fp32.
+ * The product of an fp16 scale and a code of at most 8 bits is exact in
+ * fp32, so the output is the exact value d*q (resp. d*(u-8)). */
+int skv_kv_dequant_q8_0(skv_handle *h, const void *blocks, int64_t n_values, float *out, void *stream);
+int skv_kv_dequant_q4_0(skv_handle *h, const void *blocks, int64_t n_values, float *out, void *stream);
+
+/* dst[i] = src[rows[i]] for i < n, row_bytes bytes per row; rows[i] < 0
+ * writes a zero row and reads nothing (the gather through a row list of the
+ * flash_attn_ext_rows thread, padding clamped to nothing). */
+int skv_gather_rows(skv_handle *h, const void *src, int64_t row_bytes, const int32_t *rows, int64_t n,
+                    void *dst, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPLITKV_H */

@@ -1,0 +1,212 @@
+"""Split-KV flash attention over a partitioned KV cache, for GB300 (sm_103a).
+
+A thin Python layer over libsplitkv.so (C ABI: include/splitkv.h).  The
+functions below carry the C names without the ``skv_`` prefix and only
+marshal arguments (torch tensors -> device pointers, streams); all compute
+runs in the library's CUDA kernels.  PyTorch provides device memory and
+streams.
+
+    h = Handle(0)
+    o, lse = attn_partial(h, q, k, v, Hk=8, kv_rows=rows)        # unified cache
+    o, lse = attn_window_tail(h, q, k_win, v_win, k_tail, v_tail, Hk=8, ...)
+    o, lse = attn_combine(h, o_parts, lse_parts)
+    x = kv_dequant_q8_0(h, blocks, n_values)
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+from . import _lib
+from ._lib import F16, Q4_0, Q8_0, SkvShape
+
+__all__ = ["Handle", "SplitKVError", "F16", "Q8_0", "Q4_0", "attn_partial", "attn_combine", "attn_window_tail",
+           "kv_dequant_q8_0", "kv_dequant_q4_0", "gather_rows", "plan_splits", "segment_bytes"]
+
+
+class SplitKVError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{_lib.STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+def segment_bytes(type_: int, D: int) -> int:
+    return {F16: 2 * D, Q8_0: 34 * (D // 32), Q4_0: 18 * (D // 32)}[type_]
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    torch = _torch()
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+class Handle:
+    """Owns the library handle: copy stream, events, workspace, tail ring."""
+
+    def __init__(self, device: int = 0):
+        self._h = ctypes.c_void_p()
+        rc = _lib.lib().skv_create(int(device), ctypes.byref(self._h))
+        if rc != 0:
+            raise SplitKVError(rc, "skv_create failed")
+        self.device = device
+
+    @property
+    def ptr(self):
+        return self._h
+
+    def check(self, rc: int):
+        if rc != 0:
+            msg = _lib.lib().skv_last_error(self._h).decode(errors="replace")
+            raise SplitKVError(rc, msg)
+
+    def reserve(self, workspace_bytes: int = 0, ring_bytes_per_slot: int = 0, n_slots: int = 0):
+        self.check(_lib.lib().skv_reserve(self._h, workspace_bytes, ring_bytes_per_slot, n_slots))
+
+    def scratch_info(self):
+        ws, ring, n = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_int32()
+        self.check(_lib.lib().skv_scratch_info(self._h, ctypes.byref(ws), ctypes.byref(ring), ctypes.byref(n)))
+        return ws.value, ring.value, n.value
+
+    def sm_count(self) -> int:
+        n = ctypes.c_int32()
+        self.check(_lib.lib().skv_sm_count(self._h, ctypes.byref(n)))
+        return n.value
+
+    def set_profile_events(self, before=None, after=None):
+        """Bracket later attention-kernel launches with these torch.cuda.Events."""
+        b = ctypes.c_void_p(before.cuda_event) if before is not None else None
+        a = ctypes.c_void_p(after.cuda_event) if after is not None else None
+        self.check(_lib.lib().skv_set_profile_events(self._h, b, a))
+
+    def close(self):
+        if self._h:
+            _lib.lib().skv_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def plan_splits(n_keys, n_units, sm_count, ctas_per_sm, tile=64, max_split=0):
+    """Host-side split planner (no GPU needed): returns (split_len, n_splits)."""
+    sl, ns = ctypes.c_int64(), ctypes.c_int32()
+    rc = _lib.lib().skv_plan_splits(int(n_keys), int(n_units), int(sm_count), int(ctas_per_sm), int(tile),
+                                    int(max_split), ctypes.byref(sl), ctypes.byref(ns))
+    if rc != 0:
+        raise SplitKVError(rc, "skv_plan_splits rejected its arguments")
+    return sl.value, ns.value
+
+
+def _shape(q, Hk, k_type, v_type, k_row_bytes, v_row_bytes, scale):
+    S, nq, H, D = (int(x) for x in q.shape)
+    if k_row_bytes is None:
+        k_row_bytes = Hk * segment_bytes(k_type, D)
+    if v_row_bytes is None:
+        v_row_bytes = Hk * segment_bytes(v_type, D)
+    sc = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    return SkvShape(S, nq, H, int(Hk), D, sc, int(k_type), int(v_type), int(k_row_bytes), int(v_row_bytes))
+
+
+def _outputs(q, o, lse):
+    torch = _torch()
+    S, nq, H, D = q.shape
+    if o is None:
+        o = torch.empty((S, nq, H, D), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((S, nq, H), dtype=torch.float32, device=q.device)
+    return o, lse
+
+
+def attn_partial(h: Handle, q, k, v, *, Hk, k_type=F16, v_type=F16, k_row_bytes=None, v_row_bytes=None,
+                 scale=None, kv_begin=0, kv_end=None, kv_rows=None, kv_rows_per_head=False,
+                 mask=None, q_pos=None, key_pos0=0, o=None, lse=None, stream=None):
+    """skv_attn_partial: attention over logical keys [kv_begin, kv_end)."""
+    sh = _shape(q, Hk, k_type, v_type, k_row_bytes, v_row_bytes, scale)
+    if kv_end is None:
+        kv_end = int(kv_rows.shape[-1]) if kv_rows is not None else int(k.shape[0])
+    rows_ld = int(kv_rows.shape[-1]) if kv_rows is not None else 0
+    mask_ld = int(mask.shape[-1]) if mask is not None else 0
+    o, lse = _outputs(q, o, lse)
+    h.check(_lib.lib().skv_attn_partial(h.ptr, ctypes.byref(sh), _ptr(q), _ptr(k), _ptr(v), _ptr(mask), mask_ld,
+                                        _ptr(q_pos), int(key_pos0), _ptr(kv_rows), rows_ld,
+                                        int(bool(kv_rows_per_head)), int(kv_begin), int(kv_end), _ptr(o),
+                                        _ptr(lse), _stream(stream)))
+    return o, lse
+
+
+def attn_combine(h: Handle, o_parts, lse_parts, *, o=None, lse=None, stream=None):
+    """skv_attn_combine: o_parts [P, rows, D] fp32, lse_parts [P, rows] -> (o [rows, D], lse [rows])."""
+    torch = _torch()
+    P, rows, D = (int(x) for x in o_parts.shape)
+    if o is None:
+        o = torch.empty((rows, D), dtype=torch.float32, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty((rows,), dtype=torch.float32, device=o_parts.device)
+    h.check(_lib.lib().skv_attn_combine(h.ptr, P, _ptr(o_parts), _ptr(lse_parts), rows, D, _ptr(o), _ptr(lse),
+                                        _stream(stream)))
+    return o, lse
+
+
+def attn_window_tail(h: Handle, q, k_win, v_win, k_tail_host, v_tail_host, *, Hk, n_win=None, n_tail=None,
+                     tile_rows=32768, k_type=F16, v_type=F16, k_row_bytes=None, v_row_bytes=None, scale=None,
+                     mask=None, q_pos=None, o=None, lse=None, stream=None):
+    """skv_attn_window_tail: window rows on the device, tail rows in pinned host memory."""
+    sh = _shape(q, Hk, k_type, v_type, k_row_bytes, v_row_bytes, scale)
+    if n_win is None:
+        n_win = int(k_win.shape[0]) if k_win is not None else 0
+    if n_tail is None:
+        n_tail = int(k_tail_host.shape[0]) if k_tail_host is not None else 0
+    mask_ld = int(mask.shape[-1]) if mask is not None else 0
+    o, lse = _outputs(q, o, lse)
+    h.check(_lib.lib().skv_attn_window_tail(h.ptr, ctypes.byref(sh), _ptr(q), _ptr(k_win), _ptr(v_win), int(n_win),
+                                            _ptr(k_tail_host), _ptr(v_tail_host), int(n_tail), int(tile_rows),
+                                            _ptr(mask), mask_ld, _ptr(q_pos), _ptr(o), _ptr(lse), _stream(stream)))
+    return o, lse
+
+
+def _dequant(fn, h, blocks, n_values, out, stream):
+    torch = _torch()
+    if out is None:
+        out = torch.empty((n_values,), dtype=torch.float32, device=blocks.device)
+    h.check(fn(h.ptr, _ptr(blocks), int(n_values), _ptr(out), _stream(stream)))
+    return out
+
+
+def kv_dequant_q8_0(h: Handle, blocks, n_values, *, out=None, stream=None):
+    return _dequant(_lib.lib().skv_kv_dequant_q8_0, h, blocks, n_values, out, stream)
+
+
+def kv_dequant_q4_0(h: Handle, blocks, n_values, *, out=None, stream=None):
+    return _dequant(_lib.lib().skv_kv_dequant_q4_0, h, blocks, n_values, out, stream)
+
+
+def gather_rows(h: Handle, src, rows, *, row_bytes=None, out=None, stream=None):
+    """dst[i] = src[rows[i]]; negative rows give zero rows."""
+    torch = _torch()
+    n = int(rows.numel())
+    if row_bytes is None:
+        row_bytes = src[0].numel() * src.element_size()
+    if out is None:
+        out = torch.empty((n, row_bytes), dtype=torch.uint8, device=src.device)
+    h.check(_lib.lib().skv_gather_rows(h.ptr, _ptr(src), int(row_bytes), _ptr(rows), n, _ptr(out),
+                                       _stream(stream)))
+    return out

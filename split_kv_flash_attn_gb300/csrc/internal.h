@@ -1,0 +1,100 @@
+// internal.h -- handle layout and kernel launchers shared by the library's
+// translation units (not part of the public ABI).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+
+#include "../../include/splitkv.h"
+
+#define SKV_MAX_SLOTS 4
+
+struct skv_handle {
+    int device = 0;
+    int sm_count = 0;
+    int max_smem_optin = 0;
+    cudaStream_t copy_stream = nullptr;
+    cudaEvent_t entry = nullptr;                       // orders the copy stream after the caller's work
+    cudaEvent_t copy_done[SKV_MAX_SLOTS] = {};
+    cudaEvent_t compute_done[SKV_MAX_SLOTS] = {};
+    void *workspace = nullptr;                         // partial outputs (grow-only)
+    size_t ws_cap = 0;
+    void *ring[SKV_MAX_SLOTS] = {};                    // tail-tile slots: [K bytes | V bytes]
+    size_t ring_cap = 0;                               // bytes per slot
+    int n_ring = 0;
+    cudaEvent_t prof_before = nullptr;                 // optional timing hook around attention kernels
+    cudaEvent_t prof_after = nullptr;
+    char err[512] = {0};
+};
+
+namespace skv {
+
+// Record a formatted error on the handle and return `code`.
+int fail(skv_handle *h, int code, const char *fmt, ...);
+// Map a CUDA error to SKV_ECUDA with its text (SKV_OK if e == cudaSuccess).
+int cuda_fail(skv_handle *h, cudaError_t e, const char *what);
+// True when `stream` is capturing a graph.
+bool capturing(cudaStream_t stream);
+// Grow-only scratch.  Return SKV_ECAPTURE when growth is needed in capture.
+int ensure_workspace(skv_handle *h, size_t bytes, cudaStream_t stream);
+int ensure_ring(skv_handle *h, size_t bytes_per_slot, int n_slots, cudaStream_t stream);
+
+int64_t segment_bytes(int type, int D);
+
+// How key indices of one launch map to cache rows.
+enum RowMode { ROWS_DENSE = 0, ROWS_LIST = 1, ROWS_PAGED = 2 };
+
+struct DecodeArgs {
+    const __half *q;            // [S][nq][H][D]
+    const uint8_t *k;           // cache base
+    const uint8_t *v;
+    int64_t k_row_bytes;        // dense / list: byte stride between rows
+    int64_t v_row_bytes;
+    int row_mode;
+    int64_t row0;               // dense: cache row of local key 0
+    const int32_t *rows;        // list: row ids; paged: page ids
+    int64_t rows_ld;            // entries per list
+    int rows_per_head;          // list/paged: lists are [S][Hk][rows_ld]
+    int64_t rows_off;           // list: entry of local key 0 inside each list
+    int page_rows;              // paged: rows per page (power of two)
+    const __half *mask;         // [S][nq][mask_ld] or null; column = logical key index
+    int64_t mask_ld;
+    const int32_t *q_pos;       // [S][nq] or null
+    int64_t key_pos0;           // causal position of logical key 0
+    int64_t logical0;           // logical index of local key 0
+    int64_t n_local;            // local keys of this launch
+    int S, nq, H, Hk, G;
+    float scale_log2;           // scale * log2(e)
+    int n_cg;                   // column groups (8 query columns each) per (s, k)
+    int n_splits;
+    int64_t split_len;
+    float *o_part;              // [part][R][D]
+    float *lse_part;            // [part][R]
+    int part0;                  // part index of split 0 of this launch
+    int64_t R;                  // S*nq*H
+};
+
+// Launch the split-KV decode kernel (one CTA per (split, unit)).
+int launch_decode(skv_handle *h, const DecodeArgs &a, int k_type, int v_type, int D, cudaStream_t st);
+int launch_decode_f16(skv_handle *h, const DecodeArgs &a, int D, cudaStream_t st);
+int launch_decode_quant(skv_handle *h, const DecodeArgs &a, int k_type, int v_type, int D, cudaStream_t st);
+// CTAs of the decode kernel resident per SM for this type/D pairing (0 if unsupported).
+int decode_ctas_per_sm(skv_handle *h, int k_type, int v_type, int D);
+int decode_ctas_f16(skv_handle *h, int D);
+int decode_ctas_quant(skv_handle *h, int k_type, int v_type, int D);
+// Keys per pipeline stage of the decode kernel, and the most keys one CTA may
+// take in list/paged mode.
+constexpr int kDecodeTile = 64;
+constexpr int kMaxListSplit = 2048;
+
+int launch_combine(int n_parts, const float *o_parts, const float *lse_parts, int64_t rows, int D, float *o,
+                   float *lse, cudaStream_t st);
+
+int launch_dequant(int type, const void *blocks, int64_t n_values, float *out, cudaStream_t st);
+int launch_gather(const void *src, int64_t row_bytes, const int32_t *rows, int64_t n, void *dst,
+                  cudaStream_t st);
+
+}  // namespace skv

@@ -1,0 +1,109 @@
+"""Host-only checks of the C ABI (no GPU): the library builds and loads, it
+exports every function include/splitkv.h declares, and the pure-host split
+planner keeps its contract."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from split_kv_flash_attn_gb300 import build as b
+    b.build()
+    from split_kv_flash_attn_gb300 import _lib
+    return _lib.load()
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(skv_\w+)\s*\(", txt, re.M))
+    return names
+
+
+def test_header_declares_entry_points():
+    names = _declared()
+    for must in ("skv_attn_partial", "skv_attn_combine", "skv_attn_window_tail",
+                 "skv_kv_dequant_q8_0", "skv_kv_dequant_q4_0"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in sorted(_declared()) if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_lists_every_export():
+    from split_kv_flash_attn_gb300 import _lib
+    assert set(_lib.EXPORTS) == _declared()
+
+
+def test_status_strings(lib):
+    assert lib.skv_status_string(0) == b"ok"
+    assert b"page-locked" in lib.skv_status_string(3)
+    assert lib.skv_status_string(99) == b"unknown status"
+
+
+def test_null_handle_rejected(lib):
+    assert lib.skv_attn_combine(None, 1, None, None, 1, 64, None, None, None) == 1
+    assert lib.skv_destroy(None) == 0
+
+
+def _plan(n_keys, units, sms=152, ctas=2, tile=64, max_split=0):
+    from split_kv_flash_attn_gb300 import plan_splits
+    return plan_splits(n_keys, units, sms, ctas, tile, max_split)
+
+
+@pytest.mark.parametrize("n_keys,units,max_split", [
+    (32768, 64, 2048), (131072, 8, 0), (32768, 8, 0), (256, 1, 0), (1, 1, 0), (65, 3, 0),
+    (1000003, 7, 2048), (4096, 1000, 2048), (512 * 64, 16, 2048), (64, 152 * 2, 0)])
+def test_planner_covers_range(n_keys, units, max_split):
+    sl, ns = _plan(n_keys, units, max_split=max_split)
+    assert sl % 64 == 0 and sl > 0
+    assert ns * sl >= n_keys and (ns - 1) * sl < n_keys     # covers, no empty split
+    if max_split:
+        assert sl <= max_split
+
+
+def test_planner_fills_waves_for_unified_cache():
+    # 64 (sequence, KV head) units of 32768 gathered keys on 152 SMs x 2 CTAs:
+    # 19 splits of 1728 keys make exactly four waves of 304 CTAs.
+    sl, ns = _plan(32768, 64, max_split=2048)
+    assert (sl, ns) == (1728, 19)
+    assert (64 * ns) % 304 == 0
+
+
+def test_planner_window_one_wave():
+    sl, ns = _plan(131072, 8)
+    assert 8 * ns == 304 or (8 * ns) % 304 == 0
+
+
+def test_planner_empty_and_bad_args():
+    from split_kv_flash_attn_gb300 import SplitKVError, plan_splits
+    assert plan_splits(0, 4, 152, 2)[1] == 0
+    with pytest.raises(SplitKVError):
+        plan_splits(10, 0, 152, 2)
+    with pytest.raises(SplitKVError):
+        plan_splits(10, 1, 152, 2, tile=64, max_split=32)
+
+
+def test_product_path_fails_loudly_without_library(tmp_path):
+    from split_kv_flash_attn_gb300 import _lib
+    with pytest.raises(ImportError):
+        _lib.load(str(tmp_path / "missing.so"))
+
+
+def test_product_package_never_imports_oracle():
+    pkg = os.path.join(ROOT, "split_kv_flash_attn_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                txt = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in txt and "from oracle" not in txt, f
+                assert "splitkv_oracle" not in txt, f

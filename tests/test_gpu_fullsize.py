@@ -1,0 +1,66 @@
+"""Parity at the benchmark's full sizes, in the launch configuration that
+bench.py times.
+
+* Unified-cache decode (262144-row shared cache, 8 sequences x 32768 rows,
+  32 q heads, 8 KV heads, D = 128): every output row against the oracle.
+* Long-context window + host tail (1,048,576 rows, q8_0 K / q4_0 V, window
+  131072, 28 tail tiles of 32768 rows): the full call on the GPU; the oracle
+  recomputes the rows of sampled KV heads (first and last), which it can do
+  one head group at a time.
+"""
+import numpy as np
+import pytest
+
+from split_kv_flash_attn_gb300 import workloads as wl
+from tests.gpu_util import check_attention, dev, pinned, vmax_of
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def skv():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import split_kv_flash_attn_gb300 as m
+    return m
+
+
+def test_unified_cache_full_size(skv, oracle_mod):
+    w = wl.unified_decode()
+    h = skv.Handle(0)
+    o, l = skv.attn_partial(h, dev(w.q), dev(w.k), dev(w.v), Hk=w.Hk, kv_rows=dev(w.kv_rows))
+    want_o, want_l = oracle_mod.attention(w.q, D=w.D, H=w.H, Hk=w.Hk, scale=w.scale, k0=w.k, v0=w.v,
+                                          n_rows0=w.k.shape[0], k_row_bytes0=w.k.shape[1],
+                                          v_row_bytes0=w.v.shape[1], n_keys=w.n_keys, kv_rows=w.kv_rows)
+    vmax = float(np.abs(w.v.view(np.float16)).max())
+    check_attention(o, l, want_o, want_l, vmax, "unified full")
+    h.close()
+
+
+def _head_slice(rows, kh, seg):
+    return np.ascontiguousarray(rows[:, kh * seg:(kh + 1) * seg])
+
+
+def test_long_context_full_size_sampled_heads(skv, oracle_mod):
+    w = wl.long_context_decode()
+    h = skv.Handle(0)
+    o, l = skv.attn_window_tail(h, dev(w.q), dev(w.k), dev(w.v), pinned(w.k_tail), pinned(w.v_tail), Hk=w.Hk,
+                                tile_rows=w.tile_rows, k_type=w.k_type, v_type=w.v_type)
+    o = o.cpu()
+    l = l.cpu()
+    G = w.H // w.Hk
+    sk, sv = wl.segment_bytes(w.k_type, w.D), wl.segment_bytes(w.v_type, w.D)
+    for kh in (0, w.Hk - 1):
+        kwin, vwin = _head_slice(w.k, kh, sk), _head_slice(w.v, kh, sv)
+        ktail, vtail = _head_slice(w.k_tail, kh, sk), _head_slice(w.v_tail, kh, sv)
+        qh = np.ascontiguousarray(w.q[:, :, kh * G:(kh + 1) * G])
+        want_o, want_l = oracle_mod.attention(qh, D=w.D, H=G, Hk=1, scale=w.scale, k_type=w.k_type,
+                                              v_type=w.v_type, k0=kwin, v0=vwin, n_rows0=kwin.shape[0],
+                                              k_row_bytes0=sk, v_row_bytes0=sv, k1=ktail, v1=vtail,
+                                              n_rows1=ktail.shape[0], k_row_bytes1=sk, v_row_bytes1=sv,
+                                              n_keys=w.n_keys)
+        vmax = max(vmax_of(oracle_mod, w.v_type, vwin, w.D), vmax_of(oracle_mod, w.v_type, vtail, w.D))
+        check_attention(o[:, :, kh * G:(kh + 1) * G], l[:, :, kh * G:(kh + 1) * G], want_o, want_l, vmax,
+                        f"long context head {kh}")
+    h.close()
