@@ -116,6 +116,12 @@ int skv_reserve(skv_handle *h, size_t workspace_bytes, size_t ring_bytes_per_slo
 int skv_scratch_info(const skv_handle *h, size_t *workspace_bytes, size_t *ring_bytes_per_slot,
                      int32_t *n_slots);
 
+/* Wait for all work on the device, then read and clear the handle's device
+ * status word.  SKV_ETIMEOUT: a bounded device-side wait (tensor-core
+ * pipeline barriers) gave up; the affected outputs are not valid.  The word
+ * (bit 0 = timeout) is stored in *dev_code when dev_code is not NULL. */
+int skv_status(skv_handle *h, int32_t *dev_code);
+
 /* Number of SMs of the handle's device. */
 int skv_sm_count(const skv_handle *h, int32_t *out);
 

@@ -88,6 +88,12 @@ class Handle:
         self.check(_lib.lib().skv_sm_count(self._h, ctypes.byref(n)))
         return n.value
 
+    def status(self) -> int:
+        """Synchronise and read/clear the device status word (raises on a timeout)."""
+        code = ctypes.c_int32()
+        self.check(_lib.lib().skv_status(self._h, ctypes.byref(code)))
+        return code.value
+
     def set_profile_events(self, before=None, after=None):
         """Bracket later attention-kernel launches with these torch.cuda.Events."""
         b = ctypes.c_void_p(before.cuda_event) if before is not None else None

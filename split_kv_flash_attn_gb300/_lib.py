@@ -20,7 +20,7 @@ F16, Q8_0, Q4_0 = 0, 1, 2
 # Every entry point that include/splitkv.h declares.
 EXPORTS = [
     "skv_create", "skv_destroy", "skv_last_error", "skv_status_string", "skv_reserve", "skv_scratch_info",
-    "skv_sm_count", "skv_set_profile_events", "skv_plan_splits", "skv_attn_partial", "skv_attn_combine", "skv_attn_window_tail",
+    "skv_sm_count", "skv_status", "skv_set_profile_events", "skv_plan_splits", "skv_attn_partial", "skv_attn_combine", "skv_attn_window_tail",
     "skv_kv_dequant_q8_0", "skv_kv_dequant_q4_0", "skv_gather_rows",
 ]
 
@@ -43,6 +43,7 @@ def _declare(lib):
         "skv_scratch_info": ([P, ctypes.POINTER(SZ), ctypes.POINTER(SZ), ctypes.POINTER(I32)], ctypes.c_int),
         "skv_sm_count": ([P, ctypes.POINTER(I32)], ctypes.c_int),
         "skv_set_profile_events": ([P, P, P], ctypes.c_int),
+        "skv_status": ([P, ctypes.POINTER(I32)], ctypes.c_int),
         "skv_plan_splits": ([I64, I64, I32, I32, I32, I64, ctypes.POINTER(I64), ctypes.POINTER(I32)], ctypes.c_int),
         "skv_attn_partial": ([P, SH, P, P, P, P, I64, P, I64, P, I64, I32, I64, I64, P, P, P], ctypes.c_int),
         "skv_attn_combine": ([P, I32, P, P, I64, I32, P, P, P], ctypes.c_int),

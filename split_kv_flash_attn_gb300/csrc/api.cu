@@ -218,6 +218,11 @@ int skv_create(int device, skv_handle **out)
         e = cudaEventCreateWithFlags(&h->copy_done[s], cudaEventDisableTiming);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->compute_done[s], cudaEventDisableTiming);
     }
+    if (e == cudaSuccess) e = cudaMalloc(&h->counters, sizeof(int) * kMaxUnits);
+    if (e == cudaSuccess) e = cudaMemset(h->counters, 0, sizeof(int) * kMaxUnits);
+    if (e == cudaSuccess) e = cudaMalloc(&h->status, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(h->status, 0, sizeof(int));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         cudaGetLastError();
         skv_destroy(h);
@@ -233,6 +238,8 @@ int skv_destroy(skv_handle *h)
     if (!h) return SKV_OK;
     if (h->copy_stream) cudaStreamSynchronize(h->copy_stream);
     cudaFree(h->workspace);
+    cudaFree(h->counters);
+    cudaFree(h->status);
     for (int s = 0; s < SKV_MAX_SLOTS; ++s) cudaFree(h->ring[s]);
     for (int s = 0; s < SKV_MAX_SLOTS; ++s) {
         if (h->copy_done[s]) cudaEventDestroy(h->copy_done[s]);
@@ -269,6 +276,21 @@ int skv_sm_count(const skv_handle *h, int32_t *out)
 {
     if (!h || !out) return SKV_EINVAL;
     *out = h->sm_count;
+    return SKV_OK;
+}
+
+int skv_status(skv_handle *h, int32_t *dev_code)
+{
+    if (!h) return SKV_EINVAL;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(h, e, "cudaDeviceSynchronize");
+    int word = 0;
+    e = cudaMemcpy(&word, h->status, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemset(h->status, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(h, e, "reading the status word");
+    if (dev_code) *dev_code = word;
+    if (word & 1) return fail(h, SKV_ETIMEOUT, "a device-side wait gave up (status word 0x%x)", word);
+    if (word) return fail(h, SKV_EDEVICE, "device status word 0x%x", word);
     return SKV_OK;
 }
 
@@ -355,6 +377,39 @@ int skv_attn_partial(skv_handle *h, const skv_shape *shape, const void *q, const
         rc = launch_combine(0, nullptr, nullptr, R, D, o, lse, st);
         return rc == SKV_OK ? rc : cuda_fail(h, cudaGetLastError(), "fill launch");
     }
+    if (!kv_rows && prefill_eligible(shape, mask)) {
+        // Many query rows per KV head over a dense range: the tensor-core path.
+        const int64_t units_p = static_cast<int64_t>(shape->S) * prefill_units(shape);
+        int64_t split_len = 0;
+        int32_t n_splits = 0;
+        if ((rc = skv_plan_splits(n_local, units_p, h->sm_count, 1, kPrefillTile, 0, &split_len, &n_splits)))
+            return fail(h, rc, "split planning failed");
+        if (units_p > kMaxUnits) return fail(h, SKV_EUNSUPPORTED, "too many query tiles");
+        PrefillLaunch L;
+        memset(&L, 0, sizeof(L));
+        L.shape = shape;
+        L.q = q;
+        L.k = k;
+        L.v = v;
+        L.n_rows = kv_end;
+        L.row0 = kv_begin;
+        L.n_local = n_local;
+        L.logical0 = kv_begin;
+        L.q_pos = q_pos;
+        L.key_pos0 = key_pos0;
+        L.n_splits = n_splits;
+        L.split_len = split_len;
+        L.o_out = o;
+        L.lse_out = lse;
+        if (n_splits > 1) {
+            const size_t o_bytes = round_up(static_cast<size_t>(n_splits) * R * D * sizeof(float), 256);
+            if ((rc = ensure_workspace(h, o_bytes + static_cast<size_t>(n_splits) * R * sizeof(float), st)))
+                return rc;
+            L.o_split = static_cast<float *>(h->workspace);
+            L.lse_split = reinterpret_cast<float *>(static_cast<uint8_t *>(h->workspace) + o_bytes);
+        }
+        return launch_prefill(h, L, st);
+    }
     const int ctas = decode_ctas_per_sm(h, shape->k_type, shape->v_type, D);
     if (ctas <= 0) return fail(h, SKV_EUNSUPPORTED, "no decode kernel for this type pairing / head dim");
     const int64_t units = static_cast<int64_t>(shape->S) * shape->Hk * n_cg;
@@ -363,6 +418,9 @@ int skv_attn_partial(skv_handle *h, const skv_shape *shape, const void *q, const
     rc = skv_plan_splits(n_local, units, h->sm_count, ctas, kDecodeTile, kv_rows ? kMaxListSplit : 0, &split_len,
                          &n_splits);
     if (rc) return fail(h, rc, "split planning failed");
+
+    if (n_splits > kMaxSplits) return fail(h, SKV_EUNSUPPORTED, "%d splits exceed %d", n_splits, kMaxSplits);
+    if (units > kMaxUnits) return fail(h, SKV_EUNSUPPORTED, "%lld units exceed %d", (long long)units, kMaxUnits);
 
     DecodeArgs a = base_args(shape, G, n_cg, q, mask, mask_ld, q_pos, key_pos0);
     a.k = static_cast<const uint8_t *>(k);
@@ -382,20 +440,17 @@ int skv_attn_partial(skv_handle *h, const skv_shape *shape, const void *q, const
     a.n_local = n_local;
     a.n_splits = n_splits;
     a.split_len = split_len;
-    if (n_splits == 1) {
-        a.o_part = o;
-        a.lse_part = lse;
-        a.part0 = 0;
-        return launch_decode(h, a, shape->k_type, shape->v_type, D, st);
+    a.counters = h->counters;
+    a.o_out = o;
+    a.lse_out = lse;
+    if (n_splits > 1) {
+        const size_t o_bytes = round_up(static_cast<size_t>(n_splits) * R * D * sizeof(float), 256);
+        const size_t need = o_bytes + static_cast<size_t>(n_splits) * R * sizeof(float);
+        if ((rc = ensure_workspace(h, need, st))) return rc;
+        a.o_split = static_cast<float *>(h->workspace);
+        a.lse_split = reinterpret_cast<float *>(static_cast<uint8_t *>(h->workspace) + o_bytes);
     }
-    const size_t need = static_cast<size_t>(n_splits) * R * (D + 1) * sizeof(float);
-    if ((rc = ensure_workspace(h, need, st))) return rc;
-    a.o_part = static_cast<float *>(h->workspace);
-    a.lse_part = a.o_part + static_cast<size_t>(n_splits) * R * D;
-    a.part0 = 0;
-    if ((rc = launch_decode(h, a, shape->k_type, shape->v_type, D, st))) return rc;
-    rc = launch_combine(n_splits, a.o_part, a.lse_part, R, D, o, lse, st);
-    return rc == SKV_OK ? rc : cuda_fail(h, cudaGetLastError(), "combine launch");
+    return launch_decode(h, a, shape->k_type, shape->v_type, D, st);
 }
 
 int skv_attn_window_tail(skv_handle *h, const skv_shape *shape, const void *q, const void *k_win, const void *v_win,
@@ -435,35 +490,51 @@ int skv_attn_window_tail(skv_handle *h, const skv_shape *shape, const void *q, c
         }
         tile_rows = std::min(tile_rows, n_tail);
     }
-    const int ctas = decode_ctas_per_sm(h, shape->k_type, shape->v_type, D);
+    // Many query rows per KV head: the tensor-core prefill kernel; else the
+    // split-KV decode kernel.
+    const bool use_tc = prefill_eligible(shape, mask);
+    const int ctas = use_tc ? 1 : decode_ctas_per_sm(h, shape->k_type, shape->v_type, D);
     if (ctas <= 0) return fail(h, SKV_EUNSUPPORTED, "no decode kernel for this type pairing / head dim");
-    const int64_t units = static_cast<int64_t>(shape->S) * shape->Hk * n_cg;
+    const int64_t units = use_tc ? static_cast<int64_t>(shape->S) * prefill_units(shape)
+                                 : static_cast<int64_t>(shape->S) * shape->Hk * n_cg;
+    const int tile = use_tc ? kPrefillTile : kDecodeTile;
 
     int64_t w_len = 0, t_len = 0;
     int32_t w_splits = 0, t_splits = 0;
-    if ((rc = skv_plan_splits(n_win, units, h->sm_count, ctas, kDecodeTile, 0, &w_len, &w_splits)))
+    if ((rc = skv_plan_splits(n_win, units, h->sm_count, ctas, tile, 0, &w_len, &w_splits)))
         return fail(h, rc, "split planning failed");
     const int64_t n_tt = n_tail > 0 ? (n_tail + tile_rows - 1) / tile_rows : 0;
-    if (n_tt > 0 && (rc = skv_plan_splits(tile_rows, units, h->sm_count, ctas, kDecodeTile, 0, &t_len, &t_splits)))
+    if (n_tt > 0 && (rc = skv_plan_splits(tile_rows, units, h->sm_count, ctas, tile, 0, &t_len, &t_splits)))
         return fail(h, rc, "split planning failed");
-    const int64_t n_parts = w_splits + n_tt * t_splits;
-    if (n_parts > 0x7fffffff) return fail(h, SKV_EUNSUPPORTED, "too many partials");
+    // One merged part per launch (window, then each tail tile); each launch's
+    // splits merge inside the decode kernel.
+    const int64_t n_parts = (n_win > 0 ? 1 : 0) + n_tt;
+    const int max_splits = std::max(w_splits, t_splits);
+    if (max_splits > kMaxSplits) return fail(h, SKV_EUNSUPPORTED, "%d splits exceed %d", max_splits, kMaxSplits);
+    if (units > kMaxUnits) return fail(h, SKV_EUNSUPPORTED, "%lld units exceed %d", (long long)units, kMaxUnits);
 
-    // Scratch: partials, and the tail ring (K tile then V tile per slot).
-    const size_t need_ws = static_cast<size_t>(n_parts) * R * (D + 1) * sizeof(float);
-    if ((rc = ensure_workspace(h, need_ws, st))) return rc;
+    // Workspace: [split partials: O, lse][merged parts: O, lse].
+    const size_t so = round_up(static_cast<size_t>(max_splits) * R * D * sizeof(float), 256);
+    const size_t sl = round_up(static_cast<size_t>(max_splits) * R * sizeof(float), 256);
+    const size_t po = round_up(static_cast<size_t>(n_parts) * R * D * sizeof(float), 256);
+    const size_t pl = static_cast<size_t>(n_parts) * R * sizeof(float);
+    if ((rc = ensure_workspace(h, so + sl + po + pl, st))) return rc;
+    uint8_t *ws = static_cast<uint8_t *>(h->workspace);
+    float *o_parts = reinterpret_cast<float *>(ws + so + sl);
+    float *lse_parts = reinterpret_cast<float *>(ws + so + sl + po);
+
+    // The tail ring: K tile then V tile per slot.
     const size_t k_tile_bytes = static_cast<size_t>(tile_rows) * shape->k_row_bytes;
-    const size_t v_off = (k_tile_bytes + 255) / 256 * 256;
+    const size_t v_off = round_up(k_tile_bytes, 256);
     const size_t slot_bytes = v_off + static_cast<size_t>(tile_rows) * shape->v_row_bytes;
     const int n_slots = static_cast<int>(std::min<int64_t>(2, n_tt));
     if (n_tt > 0 && (rc = ensure_ring(h, slot_bytes, n_slots, st))) return rc;
 
-    float *o_parts = static_cast<float *>(h->workspace);
-    float *lse_parts = o_parts + static_cast<size_t>(n_parts) * R * D;
     DecodeArgs a = base_args(shape, G, n_cg, q, mask, mask_ld, q_pos, 0);
     a.row_mode = ROWS_DENSE;
-    a.o_part = o_parts;
-    a.lse_part = lse_parts;
+    a.o_split = reinterpret_cast<float *>(ws);
+    a.lse_split = reinterpret_cast<float *>(ws + so);
+    a.counters = h->counters;
 
     const uint8_t *kh_ = static_cast<const uint8_t *>(k_tail_host);
     const uint8_t *vh_ = static_cast<const uint8_t *>(v_tail_host);
@@ -493,6 +564,30 @@ int skv_attn_window_tail(skv_handle *h, const skv_shape *shape, const void *q, c
         for (int64_t t = 0; t < std::min<int64_t>(n_slots, n_tt); ++t)
             if ((rc = lift(t))) return rc;
     }
+    // One launch over a dense region (window or ring slot) of n_rows rows.
+    auto run = [&](int64_t n_rows) -> int {
+        if (!use_tc) return launch_decode(h, a, shape->k_type, shape->v_type, D, st);
+        PrefillLaunch L;
+        memset(&L, 0, sizeof(L));
+        L.shape = shape;
+        L.q = q;
+        L.k = a.k;
+        L.v = a.v;
+        L.n_rows = n_rows;
+        L.row0 = a.row0;
+        L.n_local = a.n_local;
+        L.logical0 = a.logical0;
+        L.q_pos = q_pos;
+        L.key_pos0 = 0;
+        L.n_splits = a.n_splits;
+        L.split_len = a.split_len;
+        L.o_split = a.o_split;
+        L.lse_split = a.lse_split;
+        L.o_out = a.o_out;
+        L.lse_out = a.lse_out;
+        return launch_prefill(h, L, st);
+    };
+    int64_t part = 0;
     if (n_win > 0) {
         a.k = static_cast<const uint8_t *>(k_win);
         a.v = static_cast<const uint8_t *>(v_win);
@@ -501,10 +596,12 @@ int skv_attn_window_tail(skv_handle *h, const skv_shape *shape, const void *q, c
         a.n_local = n_win;
         a.n_splits = w_splits;
         a.split_len = w_len;
-        a.part0 = 0;
-        if ((rc = launch_decode(h, a, shape->k_type, shape->v_type, D, st))) return rc;
+        a.o_out = o_parts;
+        a.lse_out = lse_parts;
+        if ((rc = run(n_win))) return rc;
+        ++part;
     }
-    for (int64_t t = 0; t < n_tt; ++t) {
+    for (int64_t t = 0; t < n_tt; ++t, ++part) {
         const int slot = static_cast<int>(t % n_slots);
         e = cudaStreamWaitEvent(st, h->copy_done[slot], 0);
         if (e != cudaSuccess) return cuda_fail(h, e, "wait copy_done");
@@ -516,8 +613,9 @@ int skv_attn_window_tail(skv_handle *h, const skv_shape *shape, const void *q, c
         a.n_local = rows_of(t);
         a.n_splits = t_splits;
         a.split_len = t_len;
-        a.part0 = static_cast<int>(w_splits + t * t_splits);
-        if ((rc = launch_decode(h, a, shape->k_type, shape->v_type, D, st))) return rc;
+        a.o_out = o_parts + static_cast<size_t>(part) * R * D;
+        a.lse_out = lse_parts + static_cast<size_t>(part) * R;
+        if ((rc = run(rows_of(t)))) return rc;
         e = cudaEventRecord(h->compute_done[slot], st);
         if (e != cudaSuccess) return cuda_fail(h, e, "record compute_done");
         if (t + n_slots < n_tt) {

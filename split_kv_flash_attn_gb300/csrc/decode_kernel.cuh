@@ -60,6 +60,7 @@ struct DecodeCfg {
     static constexpr int smem = scale_off + kWarps * (scale_k + scale_v);
     static constexpr int merge_bytes = kWarps * 8 * (D + 2) * 4;
     static_assert(merge_bytes <= STAGES * stage_bytes, "merge buffer must fit in the stage ring");
+    static_assert(8 * 256 * 4 <= STAGES * stage_bytes, "split-merge weights must fit in the stage ring");
 };
 
 // Byte offset of 16-byte chunk `ch` of row `r` in a swizzled fp16 tile whose
@@ -70,36 +71,74 @@ __device__ __forceinline__ uint32_t swz(int r, int ch)
     return static_cast<uint32_t>(r * (2 * D) + ((ch ^ (r & 7)) << 4));
 }
 
+// Two codes -> one half2, exactly.  The byte c (0..255) placed under the
+// exponent byte 0x64 reads as the fp16 value 1024 + c (the spacing of fp16
+// numbers in [1024, 2048) is 1), so one byte permute and one half2 subtract
+// turn two codes into two fp16 values without a conversion instruction.
+__device__ __forceinline__ uint32_t bytes_to_half2(uint32_t two_bytes, uint32_t bias_h2)
+{
+    const uint32_t h = __byte_perm(two_bytes, 0x64646464u, 0x4140);   // [b0, 0x64, b1, 0x64]
+    __half2 r = __hsub2(*reinterpret_cast<const __half2 *>(&h), *reinterpret_cast<const __half2 *>(&bias_h2));
+    return *reinterpret_cast<uint32_t *>(&r);
+}
+__device__ __forceinline__ uint32_t ld_u16(const uint8_t *p) { return *reinterpret_cast<const uint16_t *>(p); }
+
 // Convert 16 keys of q8_0 / q4_0 head segments (raw stage rows) into an fp16
 // code tile (swizzled, 16 x D) and per-(key, block) fp32 scales.
+//  q8_0: int8 q  -> byte q ^ 0x80 = q + 128, minus 1152 (= 1024 + 128) gives q.
+//  q4_0: nibble u -> byte u, minus 1032 (= 1024 + 8) gives u - 8.
 template <int T, int D>
 __device__ __forceinline__ void convert_codes(const uint8_t *raw, __half *code, float *scale, int lane)
 {
     constexpr int SEG = Seg<T, D>::bytes;
-    constexpr int BLK = T == SKV_Q8_0 ? 34 : 18;
-    constexpr int C8 = D / 8;   // 8-value chunks per key
+    constexpr int NB = D / 32;
+    uint8_t *cb = reinterpret_cast<uint8_t *>(code);
+    if constexpr (T == SKV_Q8_0) {
+        constexpr uint32_t kBias = 0x64806480u;   // half2(1152, 1152)
+        constexpr int ITEMS = 16 * NB * 4;        // (key, block, 8-value part)
 #pragma unroll 2
-    for (int idx = lane; idx < 16 * C8; idx += 32) {
-        const int kk = idx / C8;
-        const int c8 = idx % C8;
-        const int b = c8 >> 2;
-        const int part = c8 & 3;
-        const uint8_t *blk = raw + kk * SEG + b * BLK;
-        __align__(16) __half v[8];
-        if constexpr (T == SKV_Q8_0) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = __int2half_rn(static_cast<int8_t>(blk[2 + part * 8 + e]));
-        } else {
-            const int byte0 = (part & 1) * 8;
-            const int shift = (part >> 1) * 4;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = __int2half_rn(((blk[2 + byte0 + e] >> shift) & 0xF) - 8);
+        for (int idx = lane; idx < ITEMS; idx += 32) {
+            const int kk = idx / (NB * 4);
+            const int rem = idx % (NB * 4);
+            const int b = rem >> 2;
+            const int part = rem & 3;
+            const uint8_t *blk = raw + kk * SEG + b * 34;
+            const uint8_t *src = blk + 2 + part * 8;
+            uint4 out;
+            out.x = bytes_to_half2(ld_u16(src) ^ 0x8080u, kBias);
+            out.y = bytes_to_half2(ld_u16(src + 2) ^ 0x8080u, kBias);
+            out.z = bytes_to_half2(ld_u16(src + 4) ^ 0x8080u, kBias);
+            out.w = bytes_to_half2(ld_u16(src + 6) ^ 0x8080u, kBias);
+            *reinterpret_cast<uint4 *>(cb + swz<D>(kk, b * 4 + part)) = out;
+            if (part == 0) scale[kk * NB + b] = __half2float(*reinterpret_cast<const __half *>(blk));
         }
-        *reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(code) + swz<D>(kk, c8)) =
-            *reinterpret_cast<const uint4 *>(v);
-        if (part == 0) {
-            const __half d = *reinterpret_cast<const __half *>(blk);
-            scale[kk * (D / 32) + b] = __half2float(d);
+    } else {
+        constexpr uint32_t kBias = 0x64086408u;   // half2(1032, 1032)
+        constexpr int ITEMS = 16 * NB * 2;        // (key, block, 8-byte half of the codes)
+#pragma unroll 2
+        for (int idx = lane; idx < ITEMS; idx += 32) {
+            const int kk = idx / (NB * 2);
+            const int rem = idx % (NB * 2);
+            const int b = rem >> 1;
+            const int hb = rem & 1;
+            const uint8_t *blk = raw + kk * SEG + b * 18;
+            const uint8_t *src = blk + 2 + hb * 8;
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) w[i] = ld_u16(src + 2 * i);
+            uint4 lo, hi;
+            lo.x = bytes_to_half2(w[0] & 0x0F0Fu, kBias);
+            lo.y = bytes_to_half2(w[1] & 0x0F0Fu, kBias);
+            lo.z = bytes_to_half2(w[2] & 0x0F0Fu, kBias);
+            lo.w = bytes_to_half2(w[3] & 0x0F0Fu, kBias);
+            hi.x = bytes_to_half2((w[0] >> 4) & 0x0F0Fu, kBias);
+            hi.y = bytes_to_half2((w[1] >> 4) & 0x0F0Fu, kBias);
+            hi.z = bytes_to_half2((w[2] >> 4) & 0x0F0Fu, kBias);
+            hi.w = bytes_to_half2((w[3] >> 4) & 0x0F0Fu, kBias);
+            // byte j holds value j (low nibble) and value j + 16 (high nibble)
+            *reinterpret_cast<uint4 *>(cb + swz<D>(kk, b * 4 + hb)) = lo;
+            *reinterpret_cast<uint4 *>(cb + swz<D>(kk, b * 4 + 2 + hb)) = hi;
+            if (hb == 0) scale[kk * NB + b] = __half2float(*reinterpret_cast<const __half *>(blk));
         }
     }
 }
@@ -126,12 +165,14 @@ __global__ void __launch_bounds__(128) splitkv_decode_kernel(const DecodeArgs a)
     const int lane = tid & 31;
 
     // ---- unit and split -------------------------------------------------
-    const int split = blockIdx.x;
-    const int unit = blockIdx.y;
-    const int cg = unit % a.n_cg;
-    const int sk = unit / a.n_cg;
-    const int kh = sk % a.Hk;
-    const int s = sk / a.Hk;
+    // Grid: x = (KV head, column group) fastest, y = split, z = sequence, so
+    // CTAs that run side by side read the other heads' segments of the same
+    // cache rows.
+    const int cg = blockIdx.x % a.n_cg;
+    const int kh = blockIdx.x / a.n_cg;
+    const int split = blockIdx.y;
+    const int s = blockIdx.z;
+    const int unit = (s * a.Hk + kh) * a.n_cg + cg;
     const int64_t j_lo = static_cast<int64_t>(split) * a.split_len;
     const int64_t j_hi = min(a.n_local, j_lo + a.split_len);
     const int64_t list = a.rows_per_head ? (static_cast<int64_t>(s) * a.Hk + kh) : s;
@@ -139,14 +180,19 @@ __global__ void __launch_bounds__(128) splitkv_decode_kernel(const DecodeArgs a)
     const int64_t page_lo = j_lo >> lg_pr;
 
     // ---- row indices of this split (list / paged modes) -----------------
+    // Asynchronous 4-byte copies: every index request is in flight at once,
+    // so the split starts after one memory round trip, not one per index.
     if (a.row_mode == ROWS_LIST) {
-        const int32_t *src = a.rows + list * a.rows_ld + a.rows_off;
-        for (int64_t i = tid; i < j_hi - j_lo; i += C::kThreads) idx_s[i] = __ldg(src + j_lo + i);
+        const int32_t *src = a.rows + list * a.rows_ld + a.rows_off + j_lo;
+        const int n = static_cast<int>(j_hi - j_lo);
+        for (int i = tid; i < n; i += C::kThreads) cp_async4(smem_addr(idx_s + i), src + i, 4);
     } else if (a.row_mode == ROWS_PAGED) {
-        const int32_t *src = a.rows + list * a.rows_ld;
-        const int64_t n_pages = j_hi > j_lo ? ((j_hi - 1) >> lg_pr) - page_lo + 1 : 0;
-        for (int64_t i = tid; i < n_pages; i += C::kThreads) idx_s[i] = __ldg(src + page_lo + i);
+        const int32_t *src = a.rows + list * a.rows_ld + page_lo;
+        const int n = j_hi > j_lo ? static_cast<int>(((j_hi - 1) >> lg_pr) - page_lo + 1) : 0;
+        for (int i = tid; i < n; i += C::kThreads) cp_async4(smem_addr(idx_s + i), src + i, 4);
     }
+    cp_async_commit();
+    cp_async_wait<0>();
     __syncthreads();
 
     // Byte pointer of key j's head segment (nullptr: absent key).
@@ -416,42 +462,121 @@ __global__ void __launch_bounds__(128) splitkv_decode_kernel(const DecodeArgs a)
         }
     }
     __syncthreads();
-    {
-        const int col = tid >> 4;
-        const int sub = tid & 15;
-        const int c = cg * 8 + col;
-        const int t = c / a.G;
-        const int g = c % a.G;
-        if (t < a.nq) {
-            float M = -INFINITY;
+    // This CTA's result per column: written straight to the output when the
+    // launch has one split, else to the split scratch for the merge below.
+    const int col = tid >> 4;
+    const int sub = tid & 15;
+    const int ccol = cg * 8 + col;
+    const int t_c = ccol / a.G;
+    const int64_t r_c = (static_cast<int64_t>(s) * a.nq + (t_c < a.nq ? t_c : 0)) * a.H + kh * a.G + ccol % a.G;
+    const bool col_valid = t_c < a.nq;
+    const bool direct = a.n_splits == 1;
+    if (col_valid) {
+        float M = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < C::kWarps; ++w) M = fmaxf(M, mg_m[w * 8 + col]);
-            const int64_t r = (static_cast<int64_t>(s) * a.nq + t) * a.H + kh * a.G + g;
-            const int64_t part = a.part0 + split;
-            float *op = a.o_part + (part * a.R + r) * D;
-            if (M == -INFINITY) {
-                for (int d = sub; d < D; d += 16) op[d] = 0.f;
-                if (sub == 0) a.lse_part[part * a.R + r] = -INFINITY;
-            } else {
-                float sc[C::kWarps];
-                float L = 0.f;
+        for (int w = 0; w < C::kWarps; ++w) M = fmaxf(M, mg_m[w * 8 + col]);
+        float *op = direct ? a.o_out + r_c * D : a.o_split + (static_cast<int64_t>(split) * a.R + r_c) * D;
+        float *lp = direct ? a.lse_out + r_c : a.lse_split + static_cast<int64_t>(split) * a.R + r_c;
+        if (M == -INFINITY) {
+            for (int d = sub; d < D; d += 16) op[d] = 0.f;
+            if (sub == 0) *lp = -INFINITY;
+        } else {
+            float sc[C::kWarps];
+            float L = 0.f;
 #pragma unroll
-                for (int w = 0; w < C::kWarps; ++w) {
-                    const float mw = mg_m[w * 8 + col];
-                    sc[w] = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
-                    L += sc[w] * mg_l[w * 8 + col];
+            for (int w = 0; w < C::kWarps; ++w) {
+                const float mw = mg_m[w * 8 + col];
+                sc[w] = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
+                L += sc[w] * mg_l[w * 8 + col];
+            }
+            const float inv = 1.f / L;
+            for (int d = sub; d < D; d += 16) {
+                float acc = 0.f;
+#pragma unroll
+                for (int w = 0; w < C::kWarps; ++w) acc += sc[w] * mg_o[(w * 8 + col) * D + d];
+                op[d] = acc * inv;
+            }
+            if (sub == 0) *lp = (M + __log2f(L)) * 0.6931471805599453f;
+        }
+    }
+    if (direct) return;
+
+    // ---- last CTA of the unit merges all splits (log-sum-exp combine) ------
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const int prev = atomicAdd(a.counters + unit, 1);
+        s_last = prev == a.n_splits - 1;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    constexpr int CH = 256;                          // splits per weight chunk
+    float *wsm = reinterpret_cast<float *>(smem) + col * CH;
+    float M = -INFINITY;
+    if (col_valid)
+        for (int sp = sub; sp < a.n_splits; sp += 16)
+            M = fmaxf(M, __ldcg(a.lse_split + static_cast<int64_t>(sp) * a.R + r_c));
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float acc[D / 16];
+#pragma unroll
+    for (int e = 0; e < D / 16; ++e) acc[e] = 0.f;
+    float W = 0.f;
+    const unsigned gmask = 0xFFFFu << (lane & 16);   // the 16 lanes of this column
+    if (col_valid && M != -INFINITY) {
+        for (int base = 0; base < a.n_splits; base += CH) {
+            const int n = min(CH, a.n_splits - base);
+            __syncwarp(gmask);
+            for (int i = sub; i < n; i += 16) {
+                const float l = __ldcg(a.lse_split + static_cast<int64_t>(base + i) * a.R + r_c);
+                const float w = l == -INFINITY ? 0.f : fast_exp2((l - M) * 1.4426950408889634f);
+                wsm[i] = w;
+                W += w;
+            }
+            __syncwarp(gmask);
+            // Every split wrote finite values (0 for an empty split), so a zero
+            // weight needs no branch; 4 splits' loads are issued together.
+            const float *op0 = a.o_split + (static_cast<int64_t>(base) * a.R + r_c) * D + sub;
+            const int64_t pstride = a.R * D;
+            int i = 0;
+            for (; i + 4 <= n; i += 4) {
+                float x[4][D / 16];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int e = 0; e < D / 16; ++e) x[u][e] = __ldcg(op0 + (i + u) * pstride + 16 * e);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float w = wsm[i + u];
+#pragma unroll
+                    for (int e = 0; e < D / 16; ++e) acc[e] = fmaf(w, x[u][e], acc[e]);
                 }
-                const float inv = 1.f / L;
-                for (int d = sub; d < D; d += 16) {
-                    float acc = 0.f;
+            }
+            for (; i < n; ++i) {
+                const float w = wsm[i];
 #pragma unroll
-                    for (int w = 0; w < C::kWarps; ++w) acc += sc[w] * mg_o[(w * 8 + col) * D + d];
-                    op[d] = acc * inv;
-                }
-                if (sub == 0) a.lse_part[part * a.R + r] = (M + __log2f(L)) * 0.6931471805599453f;
+                for (int e = 0; e < D / 16; ++e) acc[e] = fmaf(w, __ldcg(op0 + i * pstride + 16 * e), acc[e]);
             }
         }
     }
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
+    if (col_valid) {
+        float *op = a.o_out + r_c * D;
+        if (M == -INFINITY) {
+#pragma unroll
+            for (int e = 0; e < D / 16; ++e) op[sub + 16 * e] = 0.f;
+            if (sub == 0) a.lse_out[r_c] = -INFINITY;
+        } else {
+            const float inv = 1.f / W;
+#pragma unroll
+            for (int e = 0; e < D / 16; ++e) op[sub + 16 * e] = acc[e] * inv;
+            if (sub == 0) a.lse_out[r_c] = M + __logf(W);
+        }
+    }
+    if (tid == 0) a.counters[unit] = 0;              // ready for the next launch
 }
 
 template <int D, int KT, int VT>
@@ -465,9 +590,10 @@ int launch_decode_t(skv_handle *h, const DecodeArgs &a, cudaStream_t st)
         if (e != cudaSuccess) return cuda_fail(h, e, "cudaFuncSetAttribute(decode)");
         attr_done = true;
     }
-    const int units = a.S * a.Hk * a.n_cg;
-    if (units > 65535) return fail(h, SKV_EUNSUPPORTED, "too many (sequence, KV head, column group) units: %d", units);
-    dim3 grid(static_cast<unsigned>(a.n_splits), static_cast<unsigned>(units));
+    if (a.Hk * a.n_cg > 65535 || a.n_splits > 65535 || a.S > 65535)
+        return fail(h, SKV_EUNSUPPORTED, "grid too large: Hk*n_cg=%d splits=%d S=%d", a.Hk * a.n_cg, a.n_splits, a.S);
+    if (a.n_splits > kMaxSplits) return fail(h, SKV_EUNSUPPORTED, "%d splits exceed %d", a.n_splits, kMaxSplits);
+    dim3 grid(static_cast<unsigned>(a.Hk * a.n_cg), static_cast<unsigned>(a.n_splits), static_cast<unsigned>(a.S));
     splitkv_decode_kernel<D, KT, VT><<<grid, C::kThreads, C::smem, st>>>(a);
     return cuda_fail(h, cudaGetLastError(), "decode kernel launch");
 }

@@ -20,11 +20,13 @@ struct skv_handle {
     cudaEvent_t entry = nullptr;                       // orders the copy stream after the caller's work
     cudaEvent_t copy_done[SKV_MAX_SLOTS] = {};
     cudaEvent_t compute_done[SKV_MAX_SLOTS] = {};
+    int *counters = nullptr;                           // per-unit arrival counters of the fused split merge
     void *workspace = nullptr;                         // partial outputs (grow-only)
     size_t ws_cap = 0;
     void *ring[SKV_MAX_SLOTS] = {};                    // tail-tile slots: [K bytes | V bytes]
     size_t ring_cap = 0;                               // bytes per slot
     int n_ring = 0;
+    int *status = nullptr;                             // device status word (bit 0: a bounded wait gave up)
     cudaEvent_t prof_before = nullptr;                 // optional timing hook around attention kernels
     cudaEvent_t prof_after = nullptr;
     char err[512] = {0};
@@ -71,11 +73,19 @@ struct DecodeArgs {
     int n_cg;                   // column groups (8 query columns each) per (s, k)
     int n_splits;
     int64_t split_len;
-    float *o_part;              // [part][R][D]
-    float *lse_part;            // [part][R]
-    int part0;                  // part index of split 0 of this launch
+    float *o_split;             // per-split partials [split][R][D] (unused when n_splits == 1)
+    float *lse_split;           // [split][R]
+    int *counters;              // [S*Hk*n_cg] arrival counters, zero between launches
+    float *o_out;               // merged result of this launch [R][D]
+    float *lse_out;             // [R]
     int64_t R;                  // S*nq*H
 };
+
+// Splits of one launch merged by the last-arriving CTA of each unit are
+// capped so that the merge's weights fit its shared-memory chunking.
+constexpr int kMaxSplits = 4096;
+// Units (sequence x KV head x column group) per launch: one counter each.
+constexpr int kMaxUnits = 65536;
 
 // Launch the split-KV decode kernel (one CTA per (split, unit)).
 int launch_decode(skv_handle *h, const DecodeArgs &a, int k_type, int v_type, int D, cudaStream_t st);
@@ -92,6 +102,30 @@ constexpr int kMaxListSplit = 2048;
 
 int launch_combine(int n_parts, const float *o_parts, const float *lse_parts, int64_t rows, int D, float *o,
                    float *lse, cudaStream_t st);
+
+// One launch of the tensor-core prefill kernel over a dense fp16 region.
+struct PrefillLaunch {
+    const skv_shape *shape;
+    const void *q;
+    const void *k;              // region base (row 0 of the tensor map)
+    const void *v;
+    int64_t n_rows;             // rows of the region (tensor-map extent)
+    int64_t row0;               // region row of local key 0
+    int64_t n_local;
+    int64_t logical0;
+    const int32_t *q_pos;
+    int64_t key_pos0;
+    int n_splits;
+    int64_t split_len;
+    float *o_split;
+    float *lse_split;
+    float *o_out;
+    float *lse_out;
+};
+bool prefill_eligible(const skv_shape *sh, const void *mask);
+int prefill_units(const skv_shape *sh);    // (KV head, 128-row query tile) pairs per sequence
+int launch_prefill(skv_handle *h, const PrefillLaunch &L, cudaStream_t st);
+constexpr int kPrefillTile = 128;
 
 int launch_dequant(int type, const void *blocks, int64_t n_values, float *out, cudaStream_t st);
 int launch_gather(const void *src, int64_t row_bytes, const int32_t *rows, int64_t n, void *dst,

@@ -25,8 +25,8 @@ def check_attention(o_gpu, lse_gpu, o_ref, lse_ref, vmax, what=""):
     assert np.all(o[empty] == 0.0), f"{what}: empty rows must give O = 0"
     assert np.all(np.isfinite(o)), f"{what}: non-finite O"
     if (~empty).any():
-        do = np.abs(o - o_ref)[~empty].max()
-        dl = np.abs(lse - lse_ref)[~empty].max()
+        do = np.abs(o[~empty] - o_ref[~empty]).max()
+        dl = np.abs(lse[~empty] - lse_ref[~empty]).max()
         assert do <= TOL_O_REL * vmax, f"{what}: max|dO| = {do:.3e} > {TOL_O_REL} * {vmax:.3f}"
         assert dl <= TOL_LSE, f"{what}: max|dlse| = {dl:.3e}"
         return do / vmax, dl
