@@ -211,6 +211,71 @@ int skv_kv_dequant_q4_0(skv_handle *h, const void *blocks, int64_t n_values, flo
 int skv_gather_rows(skv_handle *h, const void *src, int64_t row_bytes, const int32_t *rows, int64_t n,
                     void *dst, void *stream);
 
+/* ---- paged attention and the device block cache --------------------------
+ *
+ * A page is page_rows consecutive rows of ONE KV head, fp16, D values per
+ * row (page_rows * D * 2 bytes); a page pool is an array of such pages.
+ */
+
+/* Attention through page lists: logical key j of sequence s, KV head k reads
+ * row j % page_rows of pool page page_ids[(s*Hk + k)*pages_per_list +
+ * j / page_rows]; a negative page id is padding (its keys are absent).
+ * shape->k_type/v_type must be SKV_F16; the row strides are ignored.
+ * page_rows must be a power of two <= 2048. */
+int skv_attn_paged(skv_handle *h, const skv_shape *shape, const void *q, const void *k_pages, const void *v_pages,
+                   int32_t page_rows, const int32_t *page_ids, int32_t pages_per_list, float *o, float *lse,
+                   void *stream);
+
+/* Device block cache over a pinned host copy ("Strata compare", KV
+ * streaming: a VRAM block cache with CLOCK eviction over a pinned host copy,
+ * resolved on the device).  The host copy is paged [n_blocks][Hk][block_rows]
+ * [D] fp16 in page-locked, device-mapped memory (SKV_ENOTPINNED otherwise);
+ * page (block b, KV head k) = host page b*Hk + k.  The cache holds n_slots
+ * resident pages plus an overflow area of max_lookups pages: misses beyond the
+ * free capacity are read from the host for that call only. */
+typedef struct skv_bcache skv_bcache;
+
+typedef struct skv_bcache_counters {
+    uint64_t calls;        /* resolves so far                                 */
+    uint64_t lookups;      /* (sequence, KV head, block) lookups              */
+    uint64_t hits;         /* lookups that found the page resident            */
+    uint64_t misses;       /* distinct missed pages (placed + overflow)       */
+    uint64_t overflow;     /* missed pages that found no slot                 */
+    int64_t last_misses;   /* of the last resolve                             */
+    int64_t last_overflow;
+} skv_bcache_counters;
+
+int skv_bcache_create(skv_handle *h, int64_t n_blocks, int32_t block_rows, int32_t Hk, int32_t D, int32_t n_slots,
+                      int64_t max_lookups, const void *host_k, const void *host_v, skv_bcache **out);
+int skv_bcache_destroy(skv_bcache *c);
+
+/* Evict everything (page table -1, slots free, counters 0); stream-ordered. */
+int skv_bcache_reset(skv_bcache *c, void *stream);
+
+/* Make the pages named by sel (int32 block ids [S][Hk][n_sel], device) readable
+ * in the pool: hits keep their slot; misses take a slot by a CLOCK sweep that
+ * never evicts a page of this call, or an overflow page; then every missed page
+ * is copied from the host copy.  page_ids [S][Hk][n_sel] (device; NULL = the
+ * cache's own buffer) receives the pool page of each lookup (-1 for a block id
+ * out of range).  Runs entirely on `stream`, no host synchronisation. */
+int skv_bcache_resolve(skv_bcache *c, const int32_t *sel, int32_t S, int32_t n_sel, int32_t *page_ids, void *stream);
+
+/* Resolve, then attention through the pool (skv_attn_paged with page_rows =
+ * block_rows) for q of shape [S][nq][H][D]. */
+int skv_bcache_attn(skv_bcache *c, const skv_shape *shape, const void *q, const int32_t *sel, int32_t n_sel,
+                    float *o, float *lse, void *stream);
+
+/* Cumulative counters (synchronises the device). */
+int skv_bcache_stats(skv_bcache *c, skv_bcache_counters *out);
+
+/* Count violations of the residency invariants (page table and slot map are
+ * inverse maps; no page left claimed); synchronises the device. */
+int skv_bcache_check(skv_bcache *c, int32_t *violations);
+
+/* Device pointers of the page pool and of the last resolve's page ids. */
+int skv_bcache_pool(const skv_bcache *c, const void **k_pages, const void **v_pages, int64_t *n_pool_pages,
+                    const int32_t **last_page_ids);
+
 #ifdef __cplusplus
 }
 #endif

@@ -21,7 +21,8 @@ from . import _lib
 from ._lib import F16, Q4_0, Q8_0, SkvShape
 
 __all__ = ["Handle", "SplitKVError", "F16", "Q8_0", "Q4_0", "attn_partial", "attn_combine", "attn_window_tail",
-           "kv_dequant_q8_0", "kv_dequant_q4_0", "gather_rows", "plan_splits", "segment_bytes"]
+           "attn_paged", "BlockCache", "kv_dequant_q8_0", "kv_dequant_q4_0", "gather_rows", "plan_splits",
+           "segment_bytes"]
 
 
 class SplitKVError(RuntimeError):
@@ -187,6 +188,72 @@ def attn_window_tail(h: Handle, q, k_win, v_win, k_tail_host, v_tail_host, *, Hk
                                             _ptr(k_tail_host), _ptr(v_tail_host), int(n_tail), int(tile_rows),
                                             _ptr(mask), mask_ld, _ptr(q_pos), _ptr(o), _ptr(lse), _stream(stream)))
     return o, lse
+
+
+def attn_paged(h: Handle, q, k_pages, v_pages, page_ids, *, Hk, page_rows, scale=None, o=None, lse=None,
+               stream=None):
+    """skv_attn_paged: page_ids int32 [S, Hk, pages_per_list] into pools of
+    page_rows x D fp16 pages (one KV head per page)."""
+    sh = _shape(q, Hk, F16, F16, None, None, scale)
+    o, lse = _outputs(q, o, lse)
+    h.check(_lib.lib().skv_attn_paged(h.ptr, ctypes.byref(sh), _ptr(q), _ptr(k_pages), _ptr(v_pages),
+                                      int(page_rows), _ptr(page_ids), int(page_ids.shape[-1]), _ptr(o), _ptr(lse),
+                                      _stream(stream)))
+    return o, lse
+
+
+class BlockCache:
+    """Device block cache over a pinned paged host copy [n_blocks][Hk][block_rows][D] fp16."""
+
+    def __init__(self, h: Handle, host_k, host_v, *, n_blocks, block_rows, Hk, D, n_slots, max_lookups):
+        self.h = h
+        self.Hk, self.D, self.block_rows = int(Hk), int(D), int(block_rows)
+        self._c = ctypes.c_void_p()
+        h.check(_lib.lib().skv_bcache_create(h.ptr, int(n_blocks), int(block_rows), int(Hk), int(D), int(n_slots),
+                                             int(max_lookups), _ptr(host_k), _ptr(host_v), ctypes.byref(self._c)))
+        self._keep = (host_k, host_v)
+
+    def reset(self, stream=None):
+        self.h.check(_lib.lib().skv_bcache_reset(self._c, _stream(stream)))
+
+    def resolve(self, sel, page_ids=None, stream=None):
+        S, _, n_sel = (int(x) for x in sel.shape)
+        self.h.check(_lib.lib().skv_bcache_resolve(self._c, _ptr(sel), S, n_sel, _ptr(page_ids), _stream(stream)))
+        return page_ids
+
+    def attn(self, q, sel, *, scale=None, o=None, lse=None, stream=None):
+        sh = _shape(q, self.Hk, F16, F16, None, None, scale)
+        o, lse = _outputs(q, o, lse)
+        self.h.check(_lib.lib().skv_bcache_attn(self._c, ctypes.byref(sh), _ptr(q), _ptr(sel), int(sel.shape[-1]),
+                                                _ptr(o), _ptr(lse), _stream(stream)))
+        return o, lse
+
+    def stats(self):
+        c = _lib.SkvBcacheCounters()
+        self.h.check(_lib.lib().skv_bcache_stats(self._c, ctypes.byref(c)))
+        return {k: getattr(c, k) for k, _ in c._fields_}
+
+    def check(self) -> int:
+        v = ctypes.c_int32()
+        self.h.check(_lib.lib().skv_bcache_check(self._c, ctypes.byref(v)))
+        return v.value
+
+    def pool(self):
+        k, v, n, ids = ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_int64(), ctypes.c_void_p()
+        self.h.check(_lib.lib().skv_bcache_pool(self._c, ctypes.byref(k), ctypes.byref(v), ctypes.byref(n),
+                                                ctypes.byref(ids)))
+        return k.value, v.value, n.value, ids.value
+
+    def close(self):
+        if self._c:
+            _lib.lib().skv_bcache_destroy(self._c)
+            self._c = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def _dequant(fn, h, blocks, n_values, out, stream):

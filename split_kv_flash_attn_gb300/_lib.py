@@ -22,7 +22,15 @@ EXPORTS = [
     "skv_create", "skv_destroy", "skv_last_error", "skv_status_string", "skv_reserve", "skv_scratch_info",
     "skv_sm_count", "skv_status", "skv_set_profile_events", "skv_plan_splits", "skv_attn_partial", "skv_attn_combine", "skv_attn_window_tail",
     "skv_kv_dequant_q8_0", "skv_kv_dequant_q4_0", "skv_gather_rows",
+    "skv_attn_paged", "skv_bcache_create", "skv_bcache_destroy", "skv_bcache_reset", "skv_bcache_resolve",
+    "skv_bcache_attn", "skv_bcache_stats", "skv_bcache_check", "skv_bcache_pool",
 ]
+
+
+class SkvBcacheCounters(ctypes.Structure):
+    _fields_ = [("calls", ctypes.c_uint64), ("lookups", ctypes.c_uint64), ("hits", ctypes.c_uint64),
+                ("misses", ctypes.c_uint64), ("overflow", ctypes.c_uint64), ("last_misses", ctypes.c_int64),
+                ("last_overflow", ctypes.c_int64)]
 
 
 class SkvShape(ctypes.Structure):
@@ -51,6 +59,16 @@ def _declare(lib):
         "skv_kv_dequant_q8_0": ([P, P, I64, P, P], ctypes.c_int),
         "skv_kv_dequant_q4_0": ([P, P, I64, P, P], ctypes.c_int),
         "skv_gather_rows": ([P, P, I64, P, I64, P, P], ctypes.c_int),
+        "skv_attn_paged": ([P, SH, P, P, P, I32, P, I32, P, P, P], ctypes.c_int),
+        "skv_bcache_create": ([P, I64, I32, I32, I32, I32, I64, P, P, ctypes.POINTER(P)], ctypes.c_int),
+        "skv_bcache_destroy": ([P], ctypes.c_int),
+        "skv_bcache_reset": ([P, P], ctypes.c_int),
+        "skv_bcache_resolve": ([P, P, I32, I32, P, P], ctypes.c_int),
+        "skv_bcache_attn": ([P, SH, P, P, I32, P, P, P], ctypes.c_int),
+        "skv_bcache_stats": ([P, ctypes.POINTER(SkvBcacheCounters)], ctypes.c_int),
+        "skv_bcache_check": ([P, ctypes.POINTER(I32)], ctypes.c_int),
+        "skv_bcache_pool": ([P, ctypes.POINTER(P), ctypes.POINTER(P), ctypes.POINTER(I64), ctypes.POINTER(P)],
+                            ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)

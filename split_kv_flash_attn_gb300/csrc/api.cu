@@ -664,3 +664,70 @@ int skv_gather_rows(skv_handle *h, const void *src, int64_t row_bytes, const int
 }
 
 }  // extern "C"
+
+extern "C" {
+
+int skv_attn_paged(skv_handle *h, const skv_shape *shape, const void *q, const void *k_pages, const void *v_pages,
+                   int32_t page_rows, const int32_t *page_ids, int32_t pages_per_list, float *o, float *lse,
+                   void *stream)
+{
+    if (!h) return SKV_EINVAL;
+    h->err[0] = 0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (!shape) return fail(h, SKV_EINVAL, "shape is NULL");
+    if (shape->k_type != SKV_F16 || shape->v_type != SKV_F16)
+        return fail(h, SKV_EUNSUPPORTED, "paged attention reads fp16 pages");
+    skv_shape sh = *shape;
+    sh.k_row_bytes = sh.v_row_bytes = static_cast<int64_t>(sh.Hk) * 2 * sh.D;   // not used by the paged rows
+    int G = 0, n_cg = 0;
+    int rc = check_shape(h, &sh, &G, &n_cg);
+    if (rc) return rc;
+    if (!q || !o || !lse || !k_pages || !v_pages || !page_ids || pages_per_list < 0)
+        return fail(h, SKV_EINVAL, "NULL pointer or negative page count");
+    if (page_rows <= 0 || (page_rows & (page_rows - 1)) || page_rows > kMaxListSplit)
+        return fail(h, SKV_EINVAL, "page_rows must be a power of two <= %d", kMaxListSplit);
+    if ((reinterpret_cast<uintptr_t>(k_pages) | reinterpret_cast<uintptr_t>(v_pages)) & 15)
+        return fail(h, SKV_EUNSUPPORTED, "page pools must be 16-byte aligned");
+    const int D = sh.D;
+    const int64_t R = static_cast<int64_t>(sh.S) * sh.nq * sh.H;
+    const int64_t n_local = static_cast<int64_t>(pages_per_list) * page_rows;
+    if (n_local == 0) {
+        rc = launch_combine(0, nullptr, nullptr, R, D, o, lse, st);
+        return rc == SKV_OK ? rc : cuda_fail(h, cudaGetLastError(), "fill launch");
+    }
+    const int ctas = decode_ctas_per_sm(h, SKV_F16, SKV_F16, D);
+    const int64_t units = static_cast<int64_t>(sh.S) * sh.Hk * n_cg;
+    if (units > kMaxUnits) return fail(h, SKV_EUNSUPPORTED, "too many units");
+    int64_t split_len = 0;
+    int32_t n_splits = 0;
+    // splits end on page boundaries so that each CTA's page list is whole
+    const int64_t max_split = std::max<int64_t>(page_rows, (kMaxListSplit / page_rows) * page_rows);
+    rc = skv_plan_splits(n_local, units, h->sm_count, ctas, std::max(kDecodeTile, page_rows), max_split, &split_len,
+                         &n_splits);
+    if (rc) return fail(h, rc, "split planning failed");
+    if (n_splits > kMaxSplits) return fail(h, SKV_EUNSUPPORTED, "%d splits exceed %d", n_splits, kMaxSplits);
+    DecodeArgs a = base_args(&sh, G, n_cg, q, nullptr, 0, nullptr, 0);
+    a.k = static_cast<const uint8_t *>(k_pages);
+    a.v = static_cast<const uint8_t *>(v_pages);
+    a.row_mode = ROWS_PAGED;
+    a.rows = page_ids;
+    a.rows_ld = pages_per_list;
+    a.rows_per_head = 1;
+    a.page_rows = page_rows;
+    a.logical0 = 0;
+    a.n_local = n_local;
+    a.n_splits = n_splits;
+    a.split_len = split_len;
+    a.counters = h->counters;
+    a.o_out = o;
+    a.lse_out = lse;
+    if (n_splits > 1) {
+        const size_t o_bytes = round_up(static_cast<size_t>(n_splits) * R * D * sizeof(float), 256);
+        if ((rc = ensure_workspace(h, o_bytes + static_cast<size_t>(n_splits) * R * sizeof(float), st))) return rc;
+        a.o_split = static_cast<float *>(h->workspace);
+        a.lse_split = reinterpret_cast<float *>(static_cast<uint8_t *>(h->workspace) + o_bytes);
+    }
+    return launch_decode(h, a, SKV_F16, SKV_F16, D, st);
+}
+
+}  // extern "C"

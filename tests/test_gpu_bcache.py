@@ -1,0 +1,135 @@
+"""Block cache (selection-driven residency over a pinned paged host copy).
+
+Parity is against the oracle over the selected rows, and bitwise against the
+same paged attention with the whole cache resident on the device (identity
+page table), the check the Strata KV-streaming parity test makes.  After every
+resolve the page table and the slot map must be inverse maps with no claimed
+page left, and the counters must add up."""
+import math
+
+import numpy as np
+import pytest
+
+from split_kv_flash_attn_gb300 import workloads as wl
+from tests.gpu_util import check_attention, dev, pinned
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def skv():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import split_kv_flash_attn_gb300 as m
+    return m
+
+
+@pytest.fixture(scope="module")
+def h(skv):
+    return skv.Handle(0)
+
+
+def _resident(skv, h, w, q_d, sel, k_full, v_full):
+    """Paged attention with every page resident: page id = block * Hk + head."""
+    ids = (sel * w.Hk + np.arange(w.Hk, dtype=np.int32)[None, :, None]).astype(np.int32)
+    return skv.attn_paged(h, q_d, k_full, v_full, dev(ids), Hk=w.Hk, page_rows=w.extra["block_rows"])
+
+
+def _oracle(oracle_mod, w, sel):
+    br = w.extra["block_rows"]
+    rows = (sel[..., None] * br + np.arange(br, dtype=np.int32)).reshape(sel.shape[0], sel.shape[1], -1)
+    return oracle_mod.attention(w.q, D=w.D, H=w.H, Hk=w.Hk, scale=w.scale, k0=w.k, v0=w.v,
+                                n_rows0=w.extra["n_kv"], layout=oracle_mod.PAGED, page_rows=br,
+                                n_keys=rows.shape[-1], kv_rows=rows.astype(np.int32), rows_per_head=True)
+
+
+@pytest.mark.parametrize("n_slots", [128, 1024])
+def test_block_cache_cold_warm_drift(skv, h, oracle_mod, n_slots):
+    import torch
+    w = wl.block_sparse_decode(n_kv=64 * 512, S=4, H=32, Hk=4, D=128, n_sel=64, cache_pages=n_slots)
+    sel = w.extra["sel"]
+    n_blocks = w.extra["n_blocks"]
+    hk, hv = pinned(w.k), pinned(w.v)
+    c = skv.BlockCache(h, hk, hv, n_blocks=n_blocks, block_rows=64, Hk=w.Hk, D=w.D, n_slots=n_slots,
+                       max_lookups=w.S * w.Hk * sel.shape[-1])
+    q_d = dev(w.q)
+    k_full, v_full = dev(w.k), dev(w.v)
+    vmax = float(np.abs(w.v.view(np.float16)).max())
+    lookups = w.S * w.Hk * sel.shape[-1]
+    distinct = len({(int(b), k) for s in range(w.S) for k in range(w.Hk) for b in sel[s, k]})
+
+    o0, l0 = c.attn(q_d, dev(sel))                            # cold
+    want_o, want_l = _oracle(oracle_mod, w, sel)
+    check_attention(o0, l0, want_o, want_l, vmax, "cold")
+    r_o, r_l = _resident(skv, h, w, q_d, sel, k_full, v_full)
+    assert torch.equal(o0, r_o) and torch.equal(l0, r_l), "cold call differs from the all-resident run"
+    assert c.check() == 0
+    st = c.stats()
+    assert st["calls"] == 1 and st["lookups"] == lookups and st["hits"] == 0
+    assert st["misses"] == distinct and st["overflow"] == max(0, distinct - n_slots)
+
+    o1, l1 = c.attn(q_d, dev(sel))                            # warm, same selection
+    assert torch.equal(o1, o0) and torch.equal(l1, l0)
+    assert c.check() == 0
+    st1 = c.stats()
+    new_hits = st1["hits"] - st["hits"]
+    new_miss = st1["misses"] - st["misses"]
+    if n_slots >= distinct:
+        assert new_miss == 0 and new_hits == lookups      # everything stayed resident
+    else:
+        assert 0 < new_miss < distinct and new_hits > 0
+    assert st1["calls"] == 2 and st1["lookups"] == 2 * lookups
+
+    rng = np.random.default_rng(55)
+    cur = sel
+    for step in range(3):                                     # drift: 10% of the blocks redrawn per step
+        cur = wl.redraw_selection(cur, n_blocks, 0.1, rng)
+        o2, l2 = c.attn(q_d, dev(cur))
+        r_o, r_l = _resident(skv, h, w, q_d, cur, k_full, v_full)
+        assert torch.equal(o2, r_o) and torch.equal(l2, r_l), f"drift step {step}"
+        assert c.check() == 0
+    want_o, want_l = _oracle(oracle_mod, w, cur)
+    check_attention(o2, l2, want_o, want_l, vmax, "drift")
+
+    c.reset()
+    o3, l3 = c.attn(q_d, dev(sel))                            # after a reset: cold again
+    assert torch.equal(o3, o0) and torch.equal(l3, l0)
+    st3 = c.stats()
+    assert st3["calls"] == 1 and st3["hits"] == 0
+    c.close()
+
+
+def test_paged_attention_padding_pages(skv, h, oracle_mod):
+    import torch
+    rng = np.random.default_rng(7)
+    Hk, D, br, n_pages, S, H = 2, 128, 64, 40, 3, 8
+    pool_k = rng.standard_normal((n_pages, br, D)).astype(np.float16)
+    pool_v = rng.standard_normal((n_pages, br, D)).astype(np.float16)
+    ids = rng.integers(0, n_pages, size=(S, Hk, 12)).astype(np.int32)
+    ids[0, 0, 5:] = -1
+    ids[1, :, :] = -1
+    q = rng.standard_normal((S, 1, H, D)).astype(np.float16)
+    o, l = skv.attn_paged(h, dev(q), dev(pool_k), dev(pool_v), dev(ids), Hk=Hk, page_rows=br)
+    # oracle: the pool as a paged cache with Hk = 1 (one head per page); rows per (s, k)
+    rows = np.where(ids[..., None] >= 0, ids[..., None] * br + np.arange(br), -1).reshape(S, Hk, -1)
+    want_o = np.zeros((S, 1, H, D))
+    want_l = np.zeros((S, 1, H))
+    G = H // Hk
+    for k in range(Hk):
+        qk = np.ascontiguousarray(q[:, :, k * G:(k + 1) * G])
+        oo, ll = oracle_mod.attention(qk, D=D, H=G, Hk=1, scale=1 / math.sqrt(D), k0=pool_k, v0=pool_v,
+                                      n_rows0=n_pages * br, k_row_bytes0=2 * D, v_row_bytes0=2 * D,
+                                      n_keys=rows.shape[-1], kv_rows=np.ascontiguousarray(rows[:, k]).astype(np.int32))
+        want_o[:, :, k * G:(k + 1) * G] = oo
+        want_l[:, :, k * G:(k + 1) * G] = ll
+    check_attention(o, l, want_o, want_l, float(np.abs(pool_v).max()), "paged")
+    assert torch.all(torch.isneginf(l[1]))
+
+
+def test_block_cache_rejects_pageable_host_copy(skv, h):
+    import torch
+    k = torch.zeros((4, 2, 64, 128), dtype=torch.float16)
+    with pytest.raises(skv.SplitKVError) as e:
+        skv.BlockCache(h, k, k, n_blocks=4, block_rows=64, Hk=2, D=128, n_slots=2, max_lookups=8)
+    assert e.value.status == 3
