@@ -405,6 +405,14 @@ def run_extras(torch, skv, wl, h, hbm_peak):
     except Exception as exc:  # noqa: BLE001
         out["long_context_error"] = repr(exc)[:300]
     try:
+        out["prefill_chunk"] = bench_prefill(torch, skv, wl, h)
+    except Exception as exc:  # noqa: BLE001
+        out["prefill_error"] = repr(exc)[:300]
+    try:
+        out["block_sparse"] = bench_block_sparse(torch, skv, wl, h, hbm_peak)
+    except Exception as exc:  # noqa: BLE001
+        out["block_sparse_error"] = repr(exc)[:300]
+    try:
         w = wl.tiny_decode()
         q = torch.from_numpy(w.q).cuda()
         kw_, vw_ = torch.from_numpy(w.k).cuda(), torch.from_numpy(w.v).cuda()
@@ -424,6 +432,123 @@ def run_extras(torch, skv, wl, h, hbm_peak):
     except Exception as exc:  # noqa: BLE001
         out["tiny_error"] = repr(exc)[:300]
     return out
+
+
+def _time_calls(torch, fn, n, warm=2):
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(n):
+        fn()
+    e1.record(s)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n
+
+
+def bench_prefill(torch, skv, wl, h):
+    """Prefill chunk: 512 causal tokens x 32 heads over 65536 keys (32768 in
+    HBM + a 32768-row pinned tail in 8192-row tiles).  The tensor-core kernel
+    alone is timed on the window (every key visible to every token)."""
+    _, bf16_peak, kind = peaks()
+    w = wl.prefill_chunk()
+    q = torch.from_numpy(w.q).cuda()
+    kw_, vw_ = torch.from_numpy(w.k).cuda(), torch.from_numpy(w.v).cuda()
+    kt, vt = torch.from_numpy(w.k_tail).pin_memory(), torch.from_numpy(w.v_tail).pin_memory()
+    qp = torch.from_numpy(w.q_pos).cuda()
+    o = torch.empty((1, w.nq, w.H, w.D), dtype=torch.float32, device="cuda")
+    lse = torch.empty((1, w.nq, w.H), dtype=torch.float32, device="cuda")
+    rows_q = w.nq * w.H
+    n_win = w.k.shape[0]
+    win_flop = 4.0 * w.D * rows_q * n_win
+    b, a = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s = torch.cuda.current_stream()
+    b.record(s)
+    a.record(s)
+    for _ in range(2):
+        skv.attn_partial(h, q, kw_, vw_, Hk=w.Hk, q_pos=qp, o=o, lse=lse)
+    torch.cuda.synchronize()
+    h.set_profile_events(b, a)
+    ks = []
+    for _ in range(5):
+        skv.attn_partial(h, q, kw_, vw_, Hk=w.Hk, q_pos=qp, o=o, lse=lse)
+        torch.cuda.synchronize()
+        ks.append(b.elapsed_time(a))
+    h.set_profile_events(None, None)
+    k_ms = statistics.median(ks)
+    # causal pairs of the whole chunk: token i at 65024+i sees keys 0..65024+i
+    pos = w.q_pos.reshape(-1).astype(np.int64)
+    total_flop = 4.0 * w.D * w.H * float((pos + 1).sum())
+    call_ms = _time_calls(torch, lambda: skv.attn_window_tail(h, q, kw_, vw_, kt, vt, Hk=w.Hk,
+                                                               tile_rows=w.tile_rows, q_pos=qp, o=o, lse=lse), 5)
+    tail_bytes = w.k_tail.nbytes + w.v_tail.nbytes
+    h.status()
+    return {"kernel_ms_window": k_ms, "kernel_TFLOPs_window": win_flop / k_ms / 1e9,
+            "frac_of_bf16_peak": win_flop / k_ms / 1e9 / bf16_peak, "peak_TFLOPs": bf16_peak,
+            "peak_kind": f"{kind} bf16 dense (fp16 runs at the same tensor rate)",
+            "call_ms_window_tail": call_ms, "call_TFLOPs": total_flop / call_ms / 1e9, "flop": total_flop,
+            "tail_bytes": tail_bytes, "tail_GBps_if_copy_bound": tail_bytes / call_ms / 1e6}
+
+
+def bench_block_sparse(torch, skv, wl, h, hbm_peak):
+    """Block-sparse decode through the block cache: 4 sequences x 4 KV heads x
+    512 selected 64-row blocks (268,435,456 B of K+V per call) from a pinned
+    paged host cache of 262144 rows, 2048 resident pages.  Cold (after a
+    reset), warm (same selection) and drift (10% of blocks redrawn per call)."""
+    w = wl.block_sparse_decode()
+    sel = w.extra["sel"]
+    hk, hv = torch.from_numpy(w.k).pin_memory(), torch.from_numpy(w.v).pin_memory()
+    c = skv.BlockCache(h, hk, hv, n_blocks=w.extra["n_blocks"], block_rows=64, Hk=w.Hk, D=w.D,
+                       n_slots=w.extra["cache_pages"], max_lookups=w.S * w.Hk * sel.shape[-1])
+    q = torch.from_numpy(w.q).cuda()
+    o = torch.empty((w.S, 1, w.H, w.D), dtype=torch.float32, device="cuda")
+    lse = torch.empty((w.S, 1, w.H), dtype=torch.float32, device="cuda")
+    sel_d = torch.from_numpy(sel).cuda()
+    call_bytes = sel.size * 64 * w.D * 2 * 2
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # cold
+    c.attn(q, sel_d, o=o, lse=lse)
+    torch.cuda.synchronize()
+    c.reset()
+    e0.record(s)
+    c.attn(q, sel_d, o=o, lse=lse)
+    e1.record(s)
+    torch.cuda.synchronize()
+    cold_ms = e0.elapsed_time(e1)
+    st0 = c.stats()
+    warm_ms = _time_calls(torch, lambda: c.attn(q, sel_d, o=o, lse=lse), 8, warm=1)
+    st1 = c.stats()
+    rng = np.random.default_rng(5)
+    sels = [sel]
+    for _ in range(8):
+        sels.append(wl.redraw_selection(sels[-1], w.extra["n_blocks"], 0.1, rng))
+    sels_d = [torch.from_numpy(x).cuda() for x in sels[1:]]
+    torch.cuda.synchronize()
+    e0.record(s)
+    for sd in sels_d:
+        c.attn(q, sd, o=o, lse=lse)
+    e1.record(s)
+    torch.cuda.synchronize()
+    drift_ms = e0.elapsed_time(e1) / len(sels_d)
+    st2 = c.stats()
+    violations = c.check()
+    page_bytes = 64 * w.D * 2 * 2
+
+    def hit_rate(a, b):
+        look = b["lookups"] - a["lookups"]
+        return (b["hits"] - a["hits"]) / max(1, look)
+    warm_calls = st1["calls"] - st0["calls"]
+    miss_pages_warm = (st1["misses"] - st0["misses"]) / max(1, warm_calls)
+    c.close()
+    return {"call_bytes": call_bytes, "cold_ms": cold_ms, "warm_ms": warm_ms, "drift_ms": drift_ms,
+            "cold_misses": st0["last_misses"], "warm_hit_rate": hit_rate(st0, st1),
+            "warm_miss_pages_per_call": miss_pages_warm,
+            "warm_miss_GBps": miss_pages_warm * page_bytes / warm_ms / 1e6,
+            "drift_hit_rate": hit_rate(st1, st2), "effective_GBps_warm": call_bytes / warm_ms / 1e6,
+            "tokens_heads_per_s_warm": w.S * w.H / (warm_ms * 1e-3), "invariant_violations": violations}
 
 
 if __name__ == "__main__":

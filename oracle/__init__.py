@@ -56,7 +56,10 @@ def _load():
     with _lock:
         if _lib is not None:
             return _lib
-        lib = ctypes.CDLL(build())
+        # SPLITKV_ORACLE_LIB points the tests at another build of this oracle
+        # (the mutation tests load deliberately broken copies this way).
+        override = os.environ.get("SPLITKV_ORACLE_LIB")
+        lib = ctypes.CDLL(override if override else build())
         P, I, L, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
         lib.orc_half_to_double.argtypes = [ctypes.c_uint16]
         lib.orc_half_to_double.restype = D
