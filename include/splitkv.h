@@ -171,6 +171,32 @@ int skv_attn_partial(skv_handle *h, const skv_shape *shape,
                      int64_t kv_begin, int64_t kv_end,
                      float *o, float *lse, void *stream);
 
+/* skv_attn_partial for callers that cannot allocate device memory.  The pages
+ * have no counterpart of this entry point; it exists for code that must not
+ * call cudaMalloc: an engine that reserves all device memory up front and
+ * serves every buffer from its own pool, a latency-critical path that cannot
+ * afford the device-wide synchronisation cudaMalloc/cudaFree may cause, or a
+ * caller without a library handle (skv_create itself allocates).
+ *
+ * Same arguments and results as skv_attn_partial, without the handle; it
+ * always runs the split-KV decode kernel (never the tensor-core prefill
+ * kernel).  It allocates nothing: its scratch (split partials and the
+ * in-kernel merge's arrival counters) is one 16 MiB array in device global
+ * memory that every GPU loading this library holds until the process exits.
+ * The first call on a device, made with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress); make that first call before
+ * any stream capture.  Returns SKV_ENOMEM when the call needs more than the
+ * array holds (more than 4096 sequence x KV-head x 8-column units, or split
+ * partials beyond 16 MiB - 16 KiB) and SKV_EINVAL / SKV_EUNSUPPORTED for the
+ * same argument errors as skv_attn_partial (there is no handle to carry a
+ * message).  All calls share the one array: calls that overlap on the GPU
+ * (different streams, or different host threads) race and must be ordered by
+ * the caller.  The arrival counters are cleared on `stream` at every call. */
+int skv_attn_partial_static(const skv_shape *shape, const void *q, const void *k, const void *v,
+                            const void *mask, int64_t mask_ld, const int32_t *q_pos, int64_t key_pos0,
+                            const int32_t *kv_rows, int64_t kv_rows_ld, int32_t kv_rows_per_head,
+                            int64_t kv_begin, int64_t kv_end, float *o, float *lse, void *stream);
+
 /* Log-sum-exp combine (formula at the top of this file) of n_parts partial
  * results: o_parts fp32 [n_parts][rows][D], lse_parts fp32 [n_parts][rows]
  * -> o [rows][D], lse [rows].  A part with lse = -inf contributes nothing

@@ -24,6 +24,7 @@ EXPORTS = [
     "skv_kv_dequant_q8_0", "skv_kv_dequant_q4_0", "skv_gather_rows",
     "skv_attn_paged", "skv_bcache_create", "skv_bcache_destroy", "skv_bcache_reset", "skv_bcache_resolve",
     "skv_bcache_attn", "skv_bcache_stats", "skv_bcache_check", "skv_bcache_pool",
+    "skv_attn_partial_static",
 ]
 
 
@@ -60,6 +61,7 @@ def _declare(lib):
         "skv_kv_dequant_q4_0": ([P, P, I64, P, P], ctypes.c_int),
         "skv_gather_rows": ([P, P, I64, P, I64, P, P], ctypes.c_int),
         "skv_attn_paged": ([P, SH, P, P, P, I32, P, I32, P, P, P], ctypes.c_int),
+        "skv_attn_partial_static": ([SH, P, P, P, P, I64, P, I64, P, I64, I32, I64, I64, P, P, P], ctypes.c_int),
         "skv_bcache_create": ([P, I64, I32, I32, I32, I32, I64, P, P, ctypes.POINTER(P)], ctypes.c_int),
         "skv_bcache_destroy": ([P], ctypes.c_int),
         "skv_bcache_reset": ([P, P], ctypes.c_int),
