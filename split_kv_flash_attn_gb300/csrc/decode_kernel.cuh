@@ -44,7 +44,13 @@ struct DecodeCfg {
     static constexpr int kTile = kDecodeTile;
     static constexpr int kWarps = 4;
     static constexpr int kThreads = 128;
-    static constexpr int STAGES = (KT == SKV_F16 && VT == SKV_F16) ? 3 : 4;
+#ifndef SKV_DECODE_STAGES_F16
+#define SKV_DECODE_STAGES_F16 3
+#endif
+#ifndef SKV_DECODE_STAGES_QUANT
+#define SKV_DECODE_STAGES_QUANT 2   // 3 CTAs per SM: the code conversion needs the warps more than depth
+#endif
+    static constexpr int STAGES = (KT == SKV_F16 && VT == SKV_F16) ? SKV_DECODE_STAGES_F16 : SKV_DECODE_STAGES_QUANT;
     static constexpr int SEGK = Seg<KT, D>::bytes;
     static constexpr int SEGV = Seg<VT, D>::bytes;
     static constexpr int stage_k = ((kTile * SEGK + 127) / 128) * 128;
@@ -195,49 +201,75 @@ __global__ void __launch_bounds__(128) splitkv_decode_kernel(const DecodeArgs a)
     cp_async_wait<0>();
     __syncthreads();
 
-    // Byte pointer of key j's head segment (nullptr: absent key).
-    auto seg_ptr = [&](const uint8_t *base, int64_t row_bytes, int seg, int64_t j) -> const uint8_t * {
-        if (j >= j_hi) return nullptr;
-        if (a.row_mode == ROWS_DENSE) return base + (a.row0 + j) * row_bytes + static_cast<int64_t>(kh) * seg;
-        if (a.row_mode == ROWS_LIST) {
-            const int32_t r = idx_s[j - j_lo];
-            return r < 0 ? nullptr : base + static_cast<int64_t>(r) * row_bytes + static_cast<int64_t>(kh) * seg;
-        }
+    // Cache row (dense / list mode) or pool row (paged mode) of key j, or -1
+    // when the key is absent (past the split, or a padding entry).
+    auto key_row = [&](int64_t j) -> int64_t {
+        if (j >= j_hi) return -1;
+        if (a.row_mode == ROWS_DENSE) return a.row0 + j;
+        if (a.row_mode == ROWS_LIST) return idx_s[j - j_lo];
         const int32_t pg = idx_s[(j >> lg_pr) - page_lo];
-        if (pg < 0) return nullptr;
-        return base + ((static_cast<int64_t>(pg) << lg_pr) + (j & (a.page_rows - 1))) * seg;
+        return pg < 0 ? -1 : (static_cast<int64_t>(pg) << lg_pr) + (j & (a.page_rows - 1));
     };
+    // A row holds all Hk heads, except in paged mode where a page holds one.
+    const bool paged = a.row_mode == ROWS_PAGED;
+    const int64_t head_k = paged ? 0 : static_cast<int64_t>(kh) * SEGK;
+    const int64_t head_v = paged ? 0 : static_cast<int64_t>(kh) * SEGV;
+    const int64_t stride_k = paged ? SEGK : a.k_row_bytes;
+    const int64_t stride_v = paged ? SEGV : a.v_row_bytes;
 
     auto load_tile = [&](int t, int st) {
         uint8_t *sk_ = smem + st * C::stage_bytes;
         uint8_t *sv_ = sk_ + C::stage_k;
         const int64_t jt = j_lo + static_cast<int64_t>(t) * kTile;
-        {
-            constexpr int CPR = SEGK / CHK;
-            constexpr int TOT = kTile * CPR;
+        if constexpr (!QK && !QV) {
+            // fp16: each thread owns one 16-byte column chunk of rows r, r+RPI,
+            // ...; one row lookup serves K and V.
+            constexpr int CPR = D / 8;
+            constexpr int RPI = C::kThreads / CPR;
+            const int ch = tid % CPR;
+            const uint32_t dk = smem_addr(sk_), dv = smem_addr(sv_);
 #pragma unroll
-            for (int it = 0; it < (TOT + C::kThreads - 1) / C::kThreads; ++it) {
-                const int c = tid + it * C::kThreads;
-                if (TOT % C::kThreads != 0 && c >= TOT) break;
-                const int r = c / CPR;
-                const int ch = c % CPR;
-                const uint8_t *src = seg_ptr(a.k, a.k_row_bytes, SEGK, jt + r);
-                const uint32_t dst = smem_addr(sk_) + (QK ? static_cast<uint32_t>(r * SEGK + ch * CHK) : swz<D>(r, ch));
-                cp_async<CHK>(dst, src ? src + ch * CHK : a.k, src != nullptr);
+            for (int it = 0; it < kTile / RPI; ++it) {
+                const int r = tid / CPR + RPI * it;
+                const int64_t row = key_row(jt + r);
+                const bool ok = row >= 0;
+                const uint8_t *src_k = a.k + (ok ? row * stride_k + head_k + ch * 16 : 0);
+                const uint8_t *src_v = a.v + (ok ? row * stride_v + head_v + ch * 16 : 0);
+                cp_async16(dk + swz<D>(r, ch), src_k, ok ? 16 : 0);
+                cp_async16(dv + swz<D>(r, ch), src_v, ok ? 16 : 0);
             }
-        }
-        {
-            constexpr int CPR = SEGV / CHV;
-            constexpr int TOT = kTile * CPR;
+        } else {
+            {
+                constexpr int CPR = SEGK / CHK;
+                constexpr int TOT = kTile * CPR;
+                const uint32_t dk = smem_addr(sk_);
 #pragma unroll
-            for (int it = 0; it < (TOT + C::kThreads - 1) / C::kThreads; ++it) {
-                const int c = tid + it * C::kThreads;
-                if (TOT % C::kThreads != 0 && c >= TOT) break;
-                const int r = c / CPR;
-                const int ch = c % CPR;
-                const uint8_t *src = seg_ptr(a.v, a.v_row_bytes, SEGV, jt + r);
-                const uint32_t dst = smem_addr(sv_) + (QV ? static_cast<uint32_t>(r * SEGV + ch * CHV) : swz<D>(r, ch));
-                cp_async<CHV>(dst, src ? src + ch * CHV : a.v, src != nullptr);
+                for (int it = 0; it < (TOT + C::kThreads - 1) / C::kThreads; ++it) {
+                    const int c = tid + it * C::kThreads;
+                    if (TOT % C::kThreads != 0 && c >= TOT) break;
+                    const int r = c / CPR;
+                    const int ch = c - r * CPR;
+                    const int64_t row = key_row(jt + r);
+                    const bool ok = row >= 0;
+                    cp_async<CHK>(dk + static_cast<uint32_t>(r * SEGK + ch * CHK),
+                                  a.k + (ok ? row * stride_k + head_k + ch * CHK : 0), ok);
+                }
+            }
+            {
+                constexpr int CPR = SEGV / CHV;
+                constexpr int TOT = kTile * CPR;
+                const uint32_t dv = smem_addr(sv_);
+#pragma unroll
+                for (int it = 0; it < (TOT + C::kThreads - 1) / C::kThreads; ++it) {
+                    const int c = tid + it * C::kThreads;
+                    if (TOT % C::kThreads != 0 && c >= TOT) break;
+                    const int r = c / CPR;
+                    const int ch = c - r * CPR;
+                    const int64_t row = key_row(jt + r);
+                    const bool ok = row >= 0;
+                    cp_async<CHV>(dv + static_cast<uint32_t>(r * SEGV + ch * CHV),
+                                  a.v + (ok ? row * stride_v + head_v + ch * CHV : 0), ok);
+                }
             }
         }
     };
@@ -307,8 +339,8 @@ __global__ void __launch_bounds__(128) splitkv_decode_kernel(const DecodeArgs a)
         const int wrow = warp * 16;
         const int64_t jw = j_lo + static_cast<int64_t>(i) * kTile + wrow;   // first key of this warp
         const int r0 = lane >> 2;
-        const bool v0 = seg_ptr(a.k, a.k_row_bytes, SEGK, jw + r0) != nullptr;
-        const bool v1 = seg_ptr(a.k, a.k_row_bytes, SEGK, jw + r0 + 8) != nullptr;
+        const bool v0 = key_row(jw + r0) >= 0;
+        const bool v1 = key_row(jw + r0 + 8) >= 0;
         if (!__any_sync(0xffffffffu, v0 || v1)) continue;   // all 16 keys absent: nothing to do
 
         // S^T = K Q^T  (16 keys x 8 columns)

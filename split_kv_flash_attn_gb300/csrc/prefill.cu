@@ -278,28 +278,40 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const int64_t pos0 = a.key_pos0 + a.logical0 + key0;
             const int64_t lim_pos = static_cast<int64_t>(pos_row) - pos0;   // columns > lim_pos are masked
             const int64_t lim_end = j_hi - key0;                            // columns >= lim_end are outside the split
-            float mx = -INFINITY;
+            // Masking only where a tile reaches past a row's position or the
+            // split's end (warp-uniform test; most tiles skip it).
+            if (__any_sync(0xffffffffu, lim_pos < kPN - 1 || lim_end < kPN)) {
 #pragma unroll
-            for (int i = 0; i < kPN; ++i) {
-                float v = x[i] * a.scale_log2;
-                if (i > lim_pos || i >= lim_end) v = -INFINITY;
-                x[i] = v;
-                mx = fmaxf(mx, v);
+                for (int i = 0; i < kPN; ++i)
+                    if (i > lim_pos || i >= lim_end) x[i] = -INFINITY;
             }
+            // Row maximum on the raw scores (the scale is positive), four
+            // independent chains.
+            float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int i = 0; i < kPN; i += 4) {
+                mq[0] = fmaxf(mq[0], x[i]);
+                mq[1] = fmaxf(mq[1], x[i + 1]);
+                mq[2] = fmaxf(mq[2], x[i + 2]);
+                mq[3] = fmaxf(mq[3], x[i + 3]);
+            }
+            const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * a.scale_log2;
             const float m_new = fmaxf(m_ref, mx);
             const bool resc = m_new > m_ref + kRescaleLog2;   // true on the first finite maximum
             const float ref = resc ? m_new : m_ref;
             const float alpha = resc ? fast_exp2(m_ref - ref) : 1.f;
-            const float sub = ref == -INFINITY ? 0.f : ref;
-            float lsum = 0.f;
+            const float neg_ref = ref == -INFINITY ? 0.f : -ref;
+            // p = 2^(s * scale_log2 - ref): one FMA and one exp2 per score.
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
             uint32_t ph[kPN / 2];
 #pragma unroll
             for (int i = 0; i < kPN; i += 2) {
-                const float p0 = fast_exp2(x[i] - sub);
-                const float p1 = fast_exp2(x[i + 1] - sub);
-                lsum += p0 + p1;
+                const float p0 = fast_exp2(fmaf(x[i], a.scale_log2, neg_ref));
+                const float p1 = fast_exp2(fmaf(x[i + 1], a.scale_log2, neg_ref));
+                ls[(i >> 1) & 3] += p0 + p1;
                 ph[i / 2] = pack_half2(p0, p1);
             }
+            const float lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
             l_run = l_run * alpha + lsum;
             m_ref = ref;
             // P buffer and O are free once PV of the previous tile is done.
