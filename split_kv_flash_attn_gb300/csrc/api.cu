@@ -102,6 +102,40 @@ int64_t segment_bytes(int type, int D)
     }
 }
 
+// Split planning with a cost model: a launch of `total` CTAs runs in
+// ceil(total / wave) waves, and each CTA costs its key tiles plus a fixed
+// overhead (prologue, pipeline fill, epilogue, merge) of `overhead_tiles`.
+// The split count minimising waves x (tiles per split + overhead) wins; ties
+// go to fewer splits.
+int plan_splits_cost(int64_t n_keys, int64_t n_units, int sm_count, int ctas_per_sm, int tile, int64_t max_split,
+                     int overhead_tiles, int64_t *split_len, int32_t *n_splits)
+{
+    const int64_t tiles = (n_keys + tile - 1) / tile;
+    const int64_t wave = static_cast<int64_t>(sm_count) * ctas_per_sm;
+    const int64_t max_tps = max_split > 0 ? max_split / tile : tiles;
+    const int64_t min_tps = std::min<int64_t>(tiles, 2);   // at least two stages per CTA when possible
+    const int64_t s_max = std::min<int64_t>(tiles, std::max<int64_t>(1, 64 * wave / n_units + 1));
+    int64_t best_tps = -1;
+    double best_cost = 0.0;
+    for (int64_t s = 1; s <= s_max; ++s) {
+        const int64_t tps = std::max<int64_t>((tiles + s - 1) / s, min_tps);
+        if (tps > max_tps) continue;
+        const int64_t splits = (tiles + tps - 1) / tps;
+        const int64_t waves = (splits * n_units + wave - 1) / wave;
+        const double cost = static_cast<double>(waves) * static_cast<double>(tps + overhead_tiles);
+        if (best_tps < 0 || cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best_tps = tps;
+        }
+    }
+    if (best_tps < 0) best_tps = std::max<int64_t>(1, max_tps);
+    const int64_t splits = (tiles + best_tps - 1) / best_tps;
+    if (splits > 0x7fffffff) return SKV_EUNSUPPORTED;
+    *split_len = best_tps * tile;
+    *n_splits = static_cast<int32_t>(splits);
+    return SKV_OK;
+}
+
 int launch_decode(skv_handle *h, const DecodeArgs &a, int kt, int vt, int D, cudaStream_t st)
 {
     if (h->prof_before) cudaEventRecord(h->prof_before, st);
@@ -315,31 +349,7 @@ int skv_plan_splits(int64_t n_keys, int64_t n_units, int32_t sm_count, int32_t c
         *n_splits = 0;
         return SKV_OK;
     }
-    const int64_t tiles = (n_keys + tile - 1) / tile;
-    const int64_t wave = static_cast<int64_t>(sm_count) * ctas_per_sm;
-    const int64_t max_tps = max_split > 0 ? max_split / tile : tiles;
-    const int64_t min_tps = std::min<int64_t>(tiles, 2);   // at least two stages per CTA when possible
-    int64_t best_tps = -1;
-    double best_eff = -1.0;
-    for (int64_t w = 1; w <= 16; ++w) {
-        const int64_t want = std::max<int64_t>(1, (w * wave + n_units - 1) / n_units);
-        int64_t tps = std::max<int64_t>((tiles + want - 1) / want, min_tps);
-        if (tps > max_tps) continue;
-        const int64_t splits = (tiles + tps - 1) / tps;
-        const int64_t total = splits * n_units;
-        const int64_t waves = (total + wave - 1) / wave;
-        const double eff = static_cast<double>(total) / static_cast<double>(waves * wave);
-        if (eff > best_eff + 1e-9) {
-            best_eff = eff;
-            best_tps = tps;
-        }
-    }
-    if (best_tps < 0) best_tps = std::max<int64_t>(1, max_tps);
-    const int64_t splits = (tiles + best_tps - 1) / best_tps;
-    if (splits > 0x7fffffff) return SKV_EUNSUPPORTED;
-    *split_len = best_tps * tile;
-    *n_splits = static_cast<int32_t>(splits);
-    return SKV_OK;
+    return skv::plan_splits_cost(n_keys, n_units, sm_count, ctas_per_sm, tile, max_split, 1, split_len, n_splits);
 }
 
 int skv_attn_combine(skv_handle *h, int32_t n_parts, const float *o_parts, const float *lse_parts, int64_t rows,
@@ -382,7 +392,8 @@ int skv_attn_partial(skv_handle *h, const skv_shape *shape, const void *q, const
         const int64_t units_p = static_cast<int64_t>(shape->S) * prefill_units(shape);
         int64_t split_len = 0;
         int32_t n_splits = 0;
-        if ((rc = skv_plan_splits(n_local, units_p, h->sm_count, 1, kPrefillTile, 0, &split_len, &n_splits)))
+        if ((rc = plan_splits_cost(n_local, units_p, h->sm_count, 1, kPrefillTile, 0, kPrefillOverheadTiles,
+                                   &split_len, &n_splits)))
             return fail(h, rc, "split planning failed");
         if (units_p > kMaxUnits) return fail(h, SKV_EUNSUPPORTED, "too many query tiles");
         PrefillLaunch L;
@@ -501,10 +512,11 @@ int skv_attn_window_tail(skv_handle *h, const skv_shape *shape, const void *q, c
 
     int64_t w_len = 0, t_len = 0;
     int32_t w_splits = 0, t_splits = 0;
-    if ((rc = skv_plan_splits(n_win, units, h->sm_count, ctas, tile, 0, &w_len, &w_splits)))
+    const int overhead = use_tc ? kPrefillOverheadTiles : 1;
+    if ((rc = plan_splits_cost(n_win, units, h->sm_count, ctas, tile, 0, overhead, &w_len, &w_splits)))
         return fail(h, rc, "split planning failed");
     const int64_t n_tt = n_tail > 0 ? (n_tail + tile_rows - 1) / tile_rows : 0;
-    if (n_tt > 0 && (rc = skv_plan_splits(tile_rows, units, h->sm_count, ctas, tile, 0, &t_len, &t_splits)))
+    if (n_tt > 0 && (rc = plan_splits_cost(tile_rows, units, h->sm_count, ctas, tile, 0, overhead, &t_len, &t_splits)))
         return fail(h, rc, "split planning failed");
     // One merged part per launch (window, then each tail tile); each launch's
     // splits merge inside the decode kernel.

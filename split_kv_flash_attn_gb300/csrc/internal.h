@@ -126,6 +126,12 @@ bool prefill_eligible(const skv_shape *sh, const void *mask);
 int prefill_units(const skv_shape *sh);    // (KV head, 128-row query tile) pairs per sequence
 int launch_prefill(skv_handle *h, const PrefillLaunch &L, cudaStream_t st);
 constexpr int kPrefillTile = 128;
+// Per-CTA fixed cost of the prefill kernel in 128-key tiles (TMEM allocation,
+// barrier set-up, Q staging, pipeline fill, epilogue and split merge).
+constexpr int kPrefillOverheadTiles = 6;
+
+int plan_splits_cost(int64_t n_keys, int64_t n_units, int sm_count, int ctas_per_sm, int tile, int64_t max_split,
+                     int overhead_tiles, int64_t *split_len, int32_t *n_splits);
 
 int launch_dequant(int type, const void *blocks, int64_t n_values, float *out, cudaStream_t st);
 int launch_gather(const void *src, int64_t row_bytes, const int32_t *rows, int64_t n, void *dst,

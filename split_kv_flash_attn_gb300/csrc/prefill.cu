@@ -36,7 +36,9 @@ namespace {
 constexpr int kPM = 128;        // query rows per tile (TMEM lanes)
 constexpr int kPN = 128;        // keys per tile
 constexpr int kPD = 128;        // head dim
-constexpr int kPThreads = 192;  // warps 0-3 softmax, 4 TMA, 5 MMA
+constexpr int kSoftmaxWarps = 8;   // two warps per query-row group (one per column half)
+constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
+constexpr int kPThreads = kSoftmaxThreads + 64;  // + TMA warp + MMA warp
 constexpr int kTileBytes = kPN * kPD * 2;       // 32 KiB per K or V tile
 constexpr int kHalfTile = kTileBytes / 2;       // one 64-column swizzle block
 constexpr int kOffQ = 0;
@@ -89,6 +91,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
     __shared__ int s_abort;
     __shared__ int s_maxpos;
     __shared__ int s_last;
+    // [slot][column half][row]: partial row maxima by tile parity (slots 0, 1),
+    // then the halves' row sums (slot 2, so that no partner read is pending)
+    __shared__ float s_pair[3][2][kPM];
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -103,10 +108,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int64_t j_lo = static_cast<int64_t>(split) * a.split_len;
     const int64_t j_hi = min(a.n_local, j_lo + a.split_len);
 
-    // this thread's query row (softmax warps)
-    const int m = tid;
-    const int t_row = mt * tpt + (m & 127) / a.G;
-    const bool row_ok = tid < kPM && t_row < a.nq;
+    // Softmax threads: query row m = TMEM lane (warp % 4) * 32 + lane, and the
+    // column half hf (key columns hf*64 .. hf*64+63 of each 128-key tile).
+    const bool softmax = warp < kSoftmaxWarps;
+    const int m = (warp & 3) * 32 + lane;
+    const int hf = warp >> 2;
+    const int t_row = mt * tpt + m / a.G;
+    const bool row_ok = softmax && t_row < a.nq;
     const int32_t pos_row = (row_ok && a.q_pos) ? a.q_pos[static_cast<int64_t>(s) * a.nq + t_row] : INT32_MAX;
 
     if (tid == 0) {
@@ -114,12 +122,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
         s_maxpos = INT32_MIN;
     }
     __syncthreads();
-    if (a.q_pos && row_ok) atomicMax(&s_maxpos, pos_row);
+    if (a.q_pos && row_ok && hf == 0) atomicMax(&s_maxpos, pos_row);
     if (warp == 0) {
         tc::tmem_alloc<512>(smem_addr(&s_tmem));
         tc::tmem_relinquish();
     }
-    if (tid == 128) {
+    if (tid == kSoftmaxThreads) {
         tc::mbar_init(bar(B_KFULL), 1);
         tc::mbar_init(bar(B_KFULL + 1), 1);
         tc::mbar_init(bar(B_KEMPTY), 1);
@@ -128,12 +136,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
         tc::mbar_init(bar(B_VFULL + 1), 1);
         tc::mbar_init(bar(B_VEMPTY), 1);
         tc::mbar_init(bar(B_VEMPTY + 1), 1);
-        tc::mbar_init(bar(B_QFULL), kPM);
+        tc::mbar_init(bar(B_QFULL), kSoftmaxThreads);
         tc::mbar_init(bar(B_SFULL), 1);
         tc::mbar_init(bar(B_SFULL + 1), 1);
-        tc::mbar_init(bar(B_SFREE), kPM);
-        tc::mbar_init(bar(B_SFREE + 1), kPM);
-        tc::mbar_init(bar(B_PFULL), kPM);
+        tc::mbar_init(bar(B_SFREE), kSoftmaxThreads);
+        tc::mbar_init(bar(B_SFREE + 1), kSoftmaxThreads);
+        tc::mbar_init(bar(B_PFULL), kSoftmaxThreads);
         tc::mbar_init(bar(B_PVDONE), 1);
         tc::fence_barrier_init();
         tc::prefetch_tmap(&tmap_k);
@@ -163,10 +171,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
         fail_wait();
         return false;
     };
+    // The two warps that share rows (w and w + 4) meet on named barrier 1 + w%4.
+    auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;\n" ::"r"(1 + (warp & 3)) : "memory"); };
 
     float m_ref = -INFINITY, l_run = 0.f;
 
-    if (warp == 4) {
+    if (warp == kSoftmaxWarps) {
         // ---------------- TMA producer ------------------------------------
         if (lane == 0) {
             int k_issued = 0, v_issued = 0;
@@ -193,7 +203,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     tc::mbar_wait(bar(B_VFULL + (j & 1)), (j >> 1) & 1, nullptr, 100000000ull);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == kSoftmaxWarps + 1) {
         // ---------------- MMA issuer ----------------------------------------
         if (lane == 0 && n_tiles > 0) {
             bool ok = wait(B_QFULL, 0);
@@ -242,60 +252,68 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 tc::mbar_wait(bar(B_PVDONE), (committed_pv - 1) & 1, nullptr, 100000000ull);   // drain issued MMAs
         }
     } else {
-        // ---------------- softmax warps (thread = query row) -----------------
-        // Q row -> shared memory in the 128-byte-swizzled K-major layout.
+        // ---------------- softmax warps (two threads per query row) -----------
+        // Q: this thread's half of its row -> the 128-byte-swizzled K-major layout.
         {
             const __half *qp = a.q + ((static_cast<int64_t>(s) * a.nq + (row_ok ? t_row : 0)) * a.H + kh * a.G +
-                                      (m % a.G)) * kPD;
+                                      (m % a.G)) * kPD + hf * 64;
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                uint4 v = row_ok ? *reinterpret_cast<const uint4 *>(qp + c * 8) : make_uint4(0, 0, 0, 0);
-                const int blk = c >> 3, cc = c & 7;
-                *reinterpret_cast<uint4 *>(sm + kOffQ + blk * kHalfTile + m * 128 + ((cc ^ (m & 7)) << 4)) = v;
+            for (int cc = 0; cc < 8; ++cc) {
+                uint4 v = row_ok ? *reinterpret_cast<const uint4 *>(qp + cc * 8) : make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4 *>(sm + kOffQ + hf * kHalfTile + m * 128 + ((cc ^ (m & 7)) << 4)) = v;
             }
             tc::fence_proxy_async_smem();
             tc::mbar_arrive(bar(B_QFULL));
         }
-        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        constexpr int NC = kPN / 2;                 // columns per thread
+        // No early exit from this loop: the two warps of a row pair meet on a
+        // named barrier every tile, so both must run every iteration.  After
+        // a wait gives up, every later wait returns at once and the CTA runs
+        // through to its exit (its outputs are then invalid and the status
+        // word says so).
         for (int j = 0; j < n_tiles; ++j) {
             const int b = j & 1;
-            if (!__all_sync(0xffffffffu, wait(B_SFULL + b, (j >> 1) & 1))) break;
+            __all_sync(0xffffffffu, wait(B_SFULL + b, (j >> 1) & 1));
             tc::tc_fence_after();
-            uint32_t sr[kPN / 32][32];
+            uint32_t sr[NC / 32][32];
 #pragma unroll
-            for (int c = 0; c < kPN / 32; ++c) tc::tmem_ld32(lane_base + b * kPN + c * 32, sr[c]);
+            for (int c = 0; c < NC / 32; ++c) tc::tmem_ld32(lane_base + b * kPN + hf * NC + c * 32, sr[c]);
 #pragma unroll
-            for (int c = 0; c < kPN / 32; ++c) tc::tmem_wait_ld(sr[c]);
-            float x[kPN];
+            for (int c = 0; c < NC / 32; ++c) tc::tmem_wait_ld(sr[c]);
+            float x[NC];
 #pragma unroll
-            for (int c = 0; c < kPN / 32; ++c)
+            for (int c = 0; c < NC / 32; ++c)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(sr[c][i]);
             tc::tc_fence_before();
             tc::mbar_arrive(bar(B_SFREE + b));
 
-            const int64_t key0 = j_lo + static_cast<int64_t>(j) * kPN;       // local index of column 0
+            const int64_t key0 = j_lo + static_cast<int64_t>(j) * kPN + hf * NC;   // local index of column 0
             const int64_t pos0 = a.key_pos0 + a.logical0 + key0;
             const int64_t lim_pos = static_cast<int64_t>(pos_row) - pos0;   // columns > lim_pos are masked
             const int64_t lim_end = j_hi - key0;                            // columns >= lim_end are outside the split
             // Masking only where a tile reaches past a row's position or the
             // split's end (warp-uniform test; most tiles skip it).
-            if (__any_sync(0xffffffffu, lim_pos < kPN - 1 || lim_end < kPN)) {
+            if (__any_sync(0xffffffffu, lim_pos < NC - 1 || lim_end < NC)) {
 #pragma unroll
-                for (int i = 0; i < kPN; ++i)
+                for (int i = 0; i < NC; ++i)
                     if (i > lim_pos || i >= lim_end) x[i] = -INFINITY;
             }
-            // Row maximum on the raw scores (the scale is positive), four
-            // independent chains.
+            // Row maximum on the raw scores (the scale is positive): this
+            // half's four chains, then the partner half's value.
             float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int i = 0; i < kPN; i += 4) {
+            for (int i = 0; i < NC; i += 4) {
                 mq[0] = fmaxf(mq[0], x[i]);
                 mq[1] = fmaxf(mq[1], x[i + 1]);
                 mq[2] = fmaxf(mq[2], x[i + 2]);
                 mq[3] = fmaxf(mq[3], x[i + 3]);
             }
-            const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * a.scale_log2;
+            const float mh = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+            s_pair[b][hf][m] = mh;
+            pair_sync();
+            const float mx = fmaxf(mh, s_pair[b][hf ^ 1][m]) * a.scale_log2;
             const float m_new = fmaxf(m_ref, mx);
             const bool resc = m_new > m_ref + kRescaleLog2;   // true on the first finite maximum
             const float ref = resc ? m_new : m_ref;
@@ -303,78 +321,81 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const float neg_ref = ref == -INFINITY ? 0.f : -ref;
             // p = 2^(s * scale_log2 - ref): one FMA and one exp2 per score.
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
-            uint32_t ph[kPN / 2];
+            uint32_t ph[NC / 2];
 #pragma unroll
-            for (int i = 0; i < kPN; i += 2) {
+            for (int i = 0; i < NC; i += 2) {
                 const float p0 = fast_exp2(fmaf(x[i], a.scale_log2, neg_ref));
                 const float p1 = fast_exp2(fmaf(x[i + 1], a.scale_log2, neg_ref));
                 ls[(i >> 1) & 3] += p0 + p1;
                 ph[i / 2] = pack_half2(p0, p1);
             }
-            const float lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            l_run = l_run * alpha + lsum;
+            l_run = l_run * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));   // this half's columns
             m_ref = ref;
             // P buffer and O are free once PV of the previous tile is done.
             if (j > 0) {
-                if (!__all_sync(0xffffffffu, wait(B_PVDONE, (j - 1) & 1))) break;
+                __all_sync(0xffffffffu, wait(B_PVDONE, (j - 1) & 1));
                 tc::tc_fence_after();
                 if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-                    for (int c = 0; c < kPD / 32; ++c) {
+                    for (int c = 0; c < NC / 32; ++c) {
                         uint32_t r[32];
-                        tc::tmem_ld32(lane_base + 2 * kPN + c * 32, r);
+                        tc::tmem_ld32(lane_base + 2 * kPN + hf * NC + c * 32, r);
                         tc::tmem_wait_ld(r);
                         float v[32];
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * alpha;
-                        tc::tmem_st32(lane_base + 2 * kPN + c * 32, v);
+                        tc::tmem_st32(lane_base + 2 * kPN + hf * NC + c * 32, v);
                     }
                     tc::tmem_wait_st();
                 }
             }
+            // this half's 64 keys are exactly one 64-key swizzle block of P
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const int blk = c >> 3, cc = c & 7;
-                *reinterpret_cast<uint4 *>(sm + kOffP + blk * kHalfTile + m * 128 + ((cc ^ (m & 7)) << 4)) =
-                    make_uint4(ph[c * 4], ph[c * 4 + 1], ph[c * 4 + 2], ph[c * 4 + 3]);
-            }
+            for (int cc = 0; cc < 8; ++cc)
+                *reinterpret_cast<uint4 *>(sm + kOffP + hf * kHalfTile + m * 128 + ((cc ^ (m & 7)) << 4)) =
+                    make_uint4(ph[cc * 4], ph[cc * 4 + 1], ph[cc * 4 + 2], ph[cc * 4 + 3]);
             tc::fence_proxy_async_smem();
             tc::tc_fence_before();
             tc::mbar_arrive(bar(B_PFULL));
         }
         // ---------------- epilogue: O / l, lse -------------------------------
-        float ov[kPD];
+        float ov[NC];
         bool have = n_tiles > 0 && !*reinterpret_cast<volatile int *>(&s_abort);
         if (have) have = wait(B_PVDONE, (n_tiles - 1) & 1);
         have = __all_sync(0xffffffffu, have);
         if (have) {
             tc::tc_fence_after();
-            uint32_t orr[kPD / 32][32];
+            uint32_t orr[NC / 32][32];
 #pragma unroll
-            for (int c = 0; c < kPD / 32; ++c) tc::tmem_ld32(lane_base + 2 * kPN + c * 32, orr[c]);
+            for (int c = 0; c < NC / 32; ++c) tc::tmem_ld32(lane_base + 2 * kPN + hf * NC + c * 32, orr[c]);
 #pragma unroll
-            for (int c = 0; c < kPD / 32; ++c) tc::tmem_wait_ld(orr[c]);
+            for (int c = 0; c < NC / 32; ++c) tc::tmem_wait_ld(orr[c]);
 #pragma unroll
-            for (int c = 0; c < kPD / 32; ++c)
+            for (int c = 0; c < NC / 32; ++c)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) ov[c * 32 + i] = __uint_as_float(orr[c][i]);
         }
+        // the row's sum is the two halves' sums
+        s_pair[2][hf][m] = l_run;
+        pair_sync();
+        const float l_row = l_run + s_pair[2][hf ^ 1][m];
         if (row_ok) {
             const int64_t r = (static_cast<int64_t>(s) * a.nq + t_row) * a.H + kh * a.G + (m % a.G);
             const bool direct = a.n_splits == 1;
-            float *op = direct ? a.o_out + r * kPD : a.o_split + (static_cast<int64_t>(split) * a.R + r) * kPD;
+            float *op = (direct ? a.o_out + r * kPD : a.o_split + (static_cast<int64_t>(split) * a.R + r) * kPD) +
+                        hf * NC;
             float *lp = direct ? a.lse_out + r : a.lse_split + static_cast<int64_t>(split) * a.R + r;
-            if (!have || m_ref == -INFINITY || l_run <= 0.f) {
+            if (!have || m_ref == -INFINITY || l_row <= 0.f) {
 #pragma unroll
-                for (int i = 0; i < kPD; i += 4) *reinterpret_cast<float4 *>(op + i) = make_float4(0.f, 0.f, 0.f, 0.f);
-                *lp = -INFINITY;
+                for (int i = 0; i < NC; i += 4) *reinterpret_cast<float4 *>(op + i) = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (hf == 0) *lp = -INFINITY;
             } else {
-                const float inv = 1.f / l_run;
+                const float inv = 1.f / l_row;
 #pragma unroll
-                for (int i = 0; i < kPD; i += 4)
+                for (int i = 0; i < NC; i += 4)
                     *reinterpret_cast<float4 *>(op + i) =
                         make_float4(ov[i] * inv, ov[i + 1] * inv, ov[i + 2] * inv, ov[i + 3] * inv);
-                *lp = (m_ref + __log2f(l_run)) * 0.6931471805599453f;
+                if (hf == 0) *lp = (m_ref + __log2f(l_row)) * 0.6931471805599453f;
             }
         }
     }
@@ -394,26 +415,28 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (!s_last) return;
     __threadfence();
     if (row_ok) {
+        // thread (row, half) merges its 64 columns over the splits
         const int64_t r = (static_cast<int64_t>(s) * a.nq + t_row) * a.H + kh * a.G + (m % a.G);
         float M = -INFINITY;
         for (int sp = 0; sp < a.n_splits; ++sp) M = fmaxf(M, __ldcg(a.lse_split + static_cast<int64_t>(sp) * a.R + r));
-        float *op = a.o_out + r * kPD;
+        float *op = a.o_out + r * kPD + hf * 64;
         if (M == -INFINITY) {
-            for (int i = 0; i < kPD; i += 4) *reinterpret_cast<float4 *>(op + i) = make_float4(0.f, 0.f, 0.f, 0.f);
-            a.lse_out[r] = -INFINITY;
+            for (int i = 0; i < 64; i += 4) *reinterpret_cast<float4 *>(op + i) = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (hf == 0) a.lse_out[r] = -INFINITY;
         } else {
-            float acc[kPD];
+            float acc[64];
 #pragma unroll
-            for (int i = 0; i < kPD; ++i) acc[i] = 0.f;
+            for (int i = 0; i < 64; ++i) acc[i] = 0.f;
             float W = 0.f;
             for (int sp = 0; sp < a.n_splits; ++sp) {
                 const float l = __ldcg(a.lse_split + static_cast<int64_t>(sp) * a.R + r);
                 if (l == -INFINITY) continue;
                 const float w = fast_exp2((l - M) * 1.4426950408889634f);
                 W += w;
-                const float4 *src = reinterpret_cast<const float4 *>(a.o_split + (static_cast<int64_t>(sp) * a.R + r) * kPD);
+                const float4 *src = reinterpret_cast<const float4 *>(
+                    a.o_split + (static_cast<int64_t>(sp) * a.R + r) * kPD + hf * 64);
 #pragma unroll
-                for (int i = 0; i < kPD / 4; ++i) {
+                for (int i = 0; i < 16; ++i) {
                     const float4 v = __ldcg(src + i);
                     acc[4 * i] = fmaf(w, v.x, acc[4 * i]);
                     acc[4 * i + 1] = fmaf(w, v.y, acc[4 * i + 1]);
@@ -422,10 +445,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 }
             }
             const float inv = 1.f / W;
-            for (int i = 0; i < kPD; i += 4)
+            for (int i = 0; i < 64; i += 4)
                 *reinterpret_cast<float4 *>(op + i) = make_float4(acc[i] * inv, acc[i + 1] * inv, acc[i + 2] * inv,
                                                                   acc[i + 3] * inv);
-            a.lse_out[r] = M + __logf(W);
+            if (hf == 0) a.lse_out[r] = M + __logf(W);
         }
     }
     if (tid == 0) a.counters[unit] = 0;
