@@ -146,6 +146,26 @@ int skv_set_profile_events(skv_handle *h, void *before, void *after);
 int skv_plan_splits(int64_t n_keys, int64_t n_units, int32_t sm_count, int32_t ctas_per_sm,
                     int32_t tile, int64_t max_split, int64_t *split_len, int32_t *n_splits);
 
+/* Resident window size ("Rolling KV" page, position-axis residency sizing).
+ * budget = min(free_bytes, target_bytes if > 0) - reserve_bytes (floored at
+ * 0).  If per_cell_bytes * kv_size fits the budget the whole cache stays
+ * resident: *window_cells = kv_size.  Otherwise *window_cells is the largest
+ * cell count whose bytes fit, rounded down to align = max(n_pad (0: 32), 256),
+ * at least align, and at most kv_size - align (rounded down) so that a tail
+ * of at least one step remains.  per_cell_bytes is the K+V bytes of one
+ * position over every layer kept in the cache. */
+int skv_plan_window(int64_t per_cell_bytes, int64_t kv_size, int64_t free_bytes, int64_t target_bytes,
+                    int64_t reserve_bytes, int32_t n_pad, int64_t *window_cells);
+
+/* Tail tile size (same page, streaming forward's tile sizing): start from
+ * ceil(n_keys / target_keys) tiles (the page uses 32768 keys per tile to keep
+ * launches few), raise the count until n_slots slots of one tile (per_key_bytes
+ * each key) fit slot_cap_bytes (the page: 4 slots within 512 MiB), keep at
+ * most one tile per align-key block, and make every tile a whole number of
+ * blocks.  *tile_rows = rows per tile, *n_tiles = tiles covering n_keys. */
+int skv_plan_tail_tile(int64_t n_keys, int64_t per_key_bytes, int32_t n_slots, int64_t slot_cap_bytes,
+                       int64_t target_keys, int32_t align, int64_t *tile_rows, int32_t *n_tiles);
+
 /* ---- attention ------------------------------------------------------- */
 
 /* Attention of every (s, t, h) row over logical keys [kv_begin, kv_end) of a
@@ -210,7 +230,8 @@ int skv_attn_combine(skv_handle *h, int32_t n_parts, const float *o_parts, const
  * Logical keys [0, n_win) are window rows k_win/v_win (device); logical keys
  * [n_win, n_win + n_tail) are rows of k_tail_host/v_tail_host, which must be
  * page-locked host memory (SKV_ENOTPINNED otherwise).  The tail is cut into
- * tiles of tile_rows rows (<= 0: 32768); each tile's raw bytes (any of the
+ * tiles of tile_rows rows (<= 0: skv_plan_tail_tile with 32768 target keys,
+ * 2 ring slots within 512 MiB, 256-key blocks); each tile's raw bytes (any of the
  * three types) are copied in one cudaMemcpyAsync per K/V into a ring slot on
  * the handle's copy stream, while the window and earlier tiles compute on
  * `stream`; copy_done/compute_done events order slot reuse.  All partials

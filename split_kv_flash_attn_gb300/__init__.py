@@ -123,6 +123,26 @@ def plan_splits(n_keys, n_units, sm_count, ctas_per_sm, tile=64, max_split=0):
     return sl.value, ns.value
 
 
+def plan_window(per_cell_bytes, kv_size, free_bytes, target_bytes=0, reserve_bytes=1536 << 20, n_pad=256):
+    """Host-side resident-window sizing (no GPU needed): cells kept on the device."""
+    out = ctypes.c_int64()
+    rc = _lib.lib().skv_plan_window(int(per_cell_bytes), int(kv_size), int(free_bytes), int(target_bytes),
+                                    int(reserve_bytes), int(n_pad), ctypes.byref(out))
+    if rc != 0:
+        raise SplitKVError(rc, "skv_plan_window rejected its arguments")
+    return out.value
+
+
+def plan_tail_tile(n_keys, per_key_bytes, n_slots=4, slot_cap_bytes=512 << 20, target_keys=32768, align=256):
+    """Host-side tail-tile sizing (no GPU needed): (tile_rows, n_tiles)."""
+    rows, n = ctypes.c_int64(), ctypes.c_int32()
+    rc = _lib.lib().skv_plan_tail_tile(int(n_keys), int(per_key_bytes), int(n_slots), int(slot_cap_bytes),
+                                       int(target_keys), int(align), ctypes.byref(rows), ctypes.byref(n))
+    if rc != 0:
+        raise SplitKVError(rc, "skv_plan_tail_tile rejected its arguments")
+    return rows.value, n.value
+
+
 def _shape(q, Hk, k_type, v_type, k_row_bytes, v_row_bytes, scale):
     S, nq, H, D = (int(x) for x in q.shape)
     if k_row_bytes is None:

@@ -485,6 +485,14 @@ int skv_attn_window_tail(skv_handle *h, const skv_shape *shape, const void *q, c
         rc = launch_combine(0, nullptr, nullptr, R, D, o, lse, st);
         return rc == SKV_OK ? rc : cuda_fail(h, cudaGetLastError(), "fill launch");
     }
+    if (tile_rows <= 0 && n_tail > 0) {
+        // default: the tail-tile planner (32768-key tiles, the ring's slots
+        // within 512 MiB, whole 256-key blocks)
+        int32_t nt = 0;
+        if ((rc = skv_plan_tail_tile(n_tail, shape->k_row_bytes + shape->v_row_bytes, 2, int64_t(512) << 20, 32768,
+                                     256, &tile_rows, &nt)))
+            return fail(h, rc, "tail-tile planning failed");
+    }
     if (tile_rows <= 0) tile_rows = 32768;
     if (n_tail > 0) {
         if (!k_tail_host || !v_tail_host) return fail(h, SKV_EINVAL, "tail pointer is NULL");

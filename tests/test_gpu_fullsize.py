@@ -38,6 +38,35 @@ def test_unified_cache_full_size(skv, oracle_mod):
     h.close()
 
 
+def test_block_sparse_full_size(skv, oracle_mod):
+    """4 sequences x 4 KV heads x 512 of 4096 64-row blocks from a pinned
+    paged cache of 262144 rows through a 2048-page block cache (demand above
+    capacity): every output row against the oracle, and bit for bit against
+    the same paged attention with the whole cache resident."""
+    import torch
+    w = wl.block_sparse_decode()
+    sel = w.extra["sel"]
+    h = skv.Handle(0)
+    c = skv.BlockCache(h, pinned(w.k), pinned(w.v), n_blocks=w.extra["n_blocks"], block_rows=64, Hk=w.Hk, D=w.D,
+                       n_slots=w.extra["cache_pages"], max_lookups=sel.size)
+    q = dev(w.q)
+    o, l = c.attn(q, dev(sel))
+    br = w.extra["block_rows"]
+    rows = (sel[..., None] * br + np.arange(br, dtype=np.int32)).reshape(w.S, w.Hk, -1).astype(np.int32)
+    want_o, want_l = oracle_mod.attention(w.q, D=w.D, H=w.H, Hk=w.Hk, scale=w.scale, k0=w.k, v0=w.v,
+                                          n_rows0=w.extra["n_kv"], layout=oracle_mod.PAGED, page_rows=br,
+                                          n_keys=rows.shape[-1], kv_rows=rows, rows_per_head=True)
+    check_attention(o, l, want_o, want_l, float(np.abs(w.v.view(np.float16)).max()), "block sparse full")
+    ids = (sel * w.Hk + np.arange(w.Hk, dtype=np.int32)[None, :, None]).astype(np.int32)
+    r_o, r_l = skv.attn_paged(h, q, dev(w.k), dev(w.v), dev(ids), Hk=w.Hk, page_rows=br)
+    assert torch.equal(o, r_o) and torch.equal(l, r_l)
+    o2, l2 = c.attn(q, dev(sel))                       # warm call: same bits
+    assert torch.equal(o2, o) and torch.equal(l2, l)
+    assert c.check() == 0
+    c.close()
+    h.close()
+
+
 def _head_slice(rows, kh, seg):
     return np.ascontiguousarray(rows[:, kh * seg:(kh + 1) * seg])
 
