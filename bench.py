@@ -16,7 +16,8 @@ sample on the host cores, and the SM clocks sampled during the timed region.
 ``--impl reference`` times the CPU oracle as the reference arm instead.
 
 Extra measurements (window + host tail stream with q8_0/q4_0 rows, pinned
-host->device copy bandwidth, tiny decode latency) go under "extra".
+host->device copy bandwidth, the tensor-core prefill chunk, block-sparse decode
+through the block cache, KV appends, tiny decode latency) go under "extra".
 """
 from __future__ import annotations
 
@@ -426,6 +427,10 @@ def run_extras(torch, skv, wl, h, hbm_peak):
     except Exception as exc:  # noqa: BLE001
         out["block_sparse_error"] = repr(exc)[:300]
     try:
+        out["kv_append"] = bench_append(torch, skv, wl, h, hbm_peak)
+    except Exception as exc:  # noqa: BLE001
+        out["kv_append_error"] = repr(exc)[:300]
+    try:
         w = wl.tiny_decode()
         q = torch.from_numpy(w.q).cuda()
         kw_, vw_ = torch.from_numpy(w.k).cuda(), torch.from_numpy(w.v).cuda()
@@ -459,6 +464,27 @@ def _time_calls(torch, fn, n, warm=2):
     e1.record(s)
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) / n
+
+
+def _graph_us(torch, fn, per_graph=50, replays=20):
+    """Device time of one call of fn (a launch-bound call), from a CUDA graph
+    holding per_graph calls replayed `replays` times."""
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(per_graph):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(replays):
+        g.replay()
+    e1.record(s)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (per_graph * replays)
 
 
 def bench_prefill(torch, skv, wl, h):
@@ -503,6 +529,53 @@ def bench_prefill(torch, skv, wl, h):
             "peak_kind": f"{kind} bf16 dense (fp16 runs at the same tensor rate)",
             "call_ms_window_tail": call_ms, "call_TFLOPs": total_flop / call_ms / 1e9, "flop": total_flop,
             "tail_bytes": tail_bytes, "tail_GBps_if_copy_bound": tail_bytes / call_ms / 1e6}
+
+
+def bench_append(torch, skv, wl, h, hbm_peak):
+    """KV append: a 32768-row chunk of fp32 K (8 KV heads x 128) written into
+    a device window as fp16 / q8_0 / q4_0 (128 MiB read, more than L2), the
+    same chunk as fp16 into a pinned host tail, one decode step's row, and the
+    block cache's write-through append (host copy + resident pages)."""
+    Hk, D, n = 8, 128, 32768
+    rng = wl.generator(6, salt=7)
+    k, _ = wl.new_kv_values(rng, n, Hk, D)
+    x = torch.from_numpy(k).cuda()
+    pos = torch.arange(n, dtype=torch.int32, device="cuda")
+    out = {"rows": n, "Hk": Hk, "D": D}
+    for name, t in (("f16", wl.F16), ("q8_0", wl.Q8_0), ("q4_0", wl.Q4_0)):
+        rb = Hk * wl.segment_bytes(t, D)
+        win = torch.empty((n, rb), dtype=torch.uint8, device="cuda")
+        ms = _time_calls(torch, lambda: skv.kv_append(h, x, pos, win, None, type_=t, n_rows0=n, n_rows1=0), 10)
+        moved = x.numel() * 4 + n * rb
+        out[f"window_{name}"] = {"ms": ms, "bytes": moved, "GBps": moved / ms / 1e6,
+                                 "frac_hbm": moved / ms / 1e6 / hbm_peak}
+        del win
+    rb = Hk * 2 * D
+    tail = torch.empty((n, rb), dtype=torch.uint8).pin_memory()
+    ms = _time_calls(torch, lambda: skv.kv_append(h, x, pos, None, tail, n_rows0=0, n_rows1=n), 5)
+    out["tail_f16"] = {"ms": ms, "host_bytes_written": n * rb, "host_write_GBps": n * rb / ms / 1e6}
+    win = torch.empty((n, rb), dtype=torch.uint8, device="cuda")
+    one, x1 = pos[:1] + (n - 1), x[:1]
+    out["decode_step_row_us"] = _graph_us(torch, lambda: skv.kv_append(h, x1, one, win, None, n_rows0=n, n_rows1=0))
+    # block cache: 512 blocks of 64 rows, 256 resident pages; appends of one
+    # decode row and of a 4096-row chunk
+    nb, br = 512, 64
+    hk = torch.zeros((nb, Hk, br, D), dtype=torch.float16).pin_memory()
+    hv = torch.zeros_like(hk).pin_memory()
+    c = skv.BlockCache(h, hk, hv, n_blocks=nb, block_rows=br, Hk=Hk, D=D, n_slots=256, max_lookups=Hk * 32)
+    sel = torch.from_numpy(np.stack([np.arange(32, dtype=np.int32) * 16] * Hk)[None]).cuda()
+    c.resolve(sel)
+    chunk = 4096
+    xc = x[:chunk]
+    pc = torch.arange(chunk, dtype=torch.int32, device="cuda") * 8      # spread over all blocks
+    ms = _time_calls(torch, lambda: c.append(xc, xc, pc), 5)
+    out["bcache_chunk"] = {"rows": chunk, "ms": ms, "host_bytes_written": 2 * chunk * rb,
+                           "host_write_GBps": 2 * chunk * rb / ms / 1e6}
+    p1 = pc[:1]
+    out["bcache_decode_row_us"] = _graph_us(torch, lambda: c.append(x1, x1, p1))
+    c.close()
+    h.status()
+    return out
 
 
 def bench_block_sparse(torch, skv, wl, h, hbm_peak):

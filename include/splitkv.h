@@ -118,8 +118,10 @@ int skv_scratch_info(const skv_handle *h, size_t *workspace_bytes, size_t *ring_
 
 /* Wait for all work on the device, then read and clear the handle's device
  * status word.  SKV_ETIMEOUT: a bounded device-side wait (tensor-core
- * pipeline barriers) gave up; the affected outputs are not valid.  The word
- * (bit 0 = timeout) is stored in *dev_code when dev_code is not NULL. */
+ * pipeline barriers) gave up; the affected outputs are not valid.  SKV_EDEVICE:
+ * another bit is set (bit 1 = an append named a position outside its cache;
+ * that row was not written).  The word is stored in *dev_code when dev_code
+ * is not NULL. */
 int skv_status(skv_handle *h, int32_t *dev_code);
 
 /* Number of SMs of the handle's device. */
@@ -258,6 +260,33 @@ int skv_kv_dequant_q4_0(skv_handle *h, const void *blocks, int64_t n_values, flo
 int skv_gather_rows(skv_handle *h, const void *src, int64_t row_bytes, const int32_t *rows, int64_t n,
                     void *dst, void *stream);
 
+/* ---- appending rows (write routing and quantise-on-append) ------------- */
+
+/* Write n new rows of one tensor (K or V) into a cell-major cache of two
+ * regions (Rolling KV, "what ships": the K/V copies split between a device
+ * window [0, wc) and a pinned host tail [wc, n_kv)).
+ *   x          fp32 [n][Hk][D], device, 16-byte aligned; D is 64 or 128.
+ *   positions  int32 [n], device: row i goes to cache position positions[i];
+ *              position p < n_rows0 is window row p of dst0, otherwise tail
+ *              row p - n_rows0 of dst1; a negative position writes nothing;
+ *              a position >= n_rows0 + n_rows1 writes nothing and sets bit 1
+ *              of the handle's device status word (skv_status).  Two rows
+ *              with the same position: either one wins.
+ *   dst0/dst1  region bases, each device memory or page-locked device-mapped
+ *              host memory (SKV_ENOTPINNED otherwise); row stride row_bytes;
+ *              head k's segment sits at byte k*segment(type, D) of a row.
+ * type SKV_F16 rounds each value to nearest fp16.  SKV_Q8_0 quantises each
+ * 32-value block as on the Strata KV-streaming page (kv_append_q8): in fp32,
+ * d = fp16(amax / 127), q = rint(x / d) clamped to [-127, 127]; SKV_Q4_0 uses
+ * the same rule with d = fp16(amax / 7) and u = rint(x / d) + 8 clamped to
+ * [0, 15] (a reading: the pages give no q4_0 quantiser).  amax = 0 stores d = 0
+ * and zero codes.  Byte layouts are those skv_kv_dequant_* decode.  Alignment:
+ * bases and row_bytes 4-byte (fp16) or 2-byte (quantised), else
+ * SKV_EUNSUPPORTED.  Stream-ordered; allocates nothing. */
+int skv_kv_append(skv_handle *h, int32_t type, int32_t Hk, int32_t D, int64_t row_bytes, const float *x,
+                  const int32_t *positions, int32_t n, void *dst0, int64_t n_rows0, void *dst1, int64_t n_rows1,
+                  void *stream);
+
 /* ---- paged attention and the device block cache --------------------------
  *
  * A page is page_rows consecutive rows of ONE KV head, fp16, D values per
@@ -306,6 +335,19 @@ int skv_bcache_reset(skv_bcache *c, void *stream);
  * cache's own buffer) receives the pool page of each lookup (-1 for a block id
  * out of range).  Runs entirely on `stream`, no host synchronisation. */
 int skv_bcache_resolve(skv_bcache *c, const int32_t *sel, int32_t S, int32_t n_sel, int32_t *page_ids, void *stream);
+
+/* Write-through append ("Strata compare", KV streaming: writers write the
+ * host copy always and a VRAM page only while its block is resident, so
+ * resident pages never go stale).  k_new, v_new: fp32 [n][Hk][D], device,
+ * 16-byte aligned; positions int32 [n], device: cache position p is row
+ * p % block_rows of block p / block_rows.  Each row is rounded to fp16 and
+ * written into the host copy (through its mapped address; the host copy must
+ * be 16-byte aligned) and, when page (block, KV head) is resident, into its
+ * pool page.  A negative position writes nothing; one >= n_blocks*block_rows
+ * writes nothing and sets bit 1 of the handle's device status word.
+ * Stream-ordered with resolve and attention on the same stream. */
+int skv_bcache_append(skv_bcache *c, const float *k_new, const float *v_new, const int32_t *positions, int32_t n,
+                      void *stream);
 
 /* Resolve, then attention through the pool (skv_attn_paged with page_rows =
  * block_rows) for q of shape [S][nq][H][D]. */

@@ -76,6 +76,14 @@ def _load():
         lib.orc_set_threads.argtypes = [I]
         lib.orc_segment_bytes.argtypes = [I, I]
         lib.orc_segment_bytes.restype = L
+        lib.orc_float_to_half.argtypes = [ctypes.c_float]
+        lib.orc_float_to_half.restype = ctypes.c_uint16
+        lib.orc_quantize.argtypes = [I, P, L, P]
+        lib.orc_quantize.restype = I
+        lib.orc_kv_append.argtypes = [I, I, I, L, P, P, L, P, L, P, L]
+        lib.orc_kv_append.restype = L
+        lib.orc_paged_append.argtypes = [I, I, I, L, P, P, L, P]
+        lib.orc_paged_append.restype = L
         _lib = lib
         return lib
 
@@ -160,3 +168,49 @@ def combine(o_parts, lse_parts):
     if rc:
         raise ValueError("orc_combine rejected its arguments")
     return o, lse
+
+
+def float_to_half(x) -> np.ndarray:
+    """Binary16 bit patterns (uint16) of fp32 values, nearest-even rounding."""
+    lib = _load()
+    x = np.asarray(x, dtype=np.float32).ravel()
+    return np.array([lib.orc_float_to_half(float(v)) for v in x], dtype=np.uint16)
+
+
+def quantize(type_: int, x) -> np.ndarray:
+    """Encode fp32 values as fp16 / q8_0 / q4_0 bytes."""
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float32).ravel())
+    n = x.size
+    nbytes = 2 * n if type_ == F16 else segment_bytes(type_, 32) * (n // 32)
+    out = np.zeros(max(nbytes, 1), dtype=np.uint8)
+    if _load().orc_quantize(type_, _ptr(x), n, _ptr(out)):
+        raise ValueError("orc_quantize rejected its arguments")
+    return out[:nbytes]
+
+
+def kv_append(type_: int, x, positions, dst0, n_rows0: int, dst1, n_rows1: int, row_bytes: int) -> int:
+    """Write x ([n][Hk][D] fp32) into two cell-major uint8 regions in place;
+    returns how many positions fell outside both regions."""
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    n, Hk, D = x.shape
+    pos = np.ascontiguousarray(np.asarray(positions, dtype=np.int32))
+    for a in (dst0, dst1):
+        assert a is None or (a.dtype == np.uint8 and a.flags["C_CONTIGUOUS"])
+    bad = _load().orc_kv_append(type_, Hk, D, int(row_bytes), _ptr(x), _ptr(pos), n, _ptr(dst0), int(n_rows0),
+                                _ptr(dst1), int(n_rows1))
+    if bad < 0:
+        raise ValueError("orc_kv_append rejected its arguments")
+    return int(bad)
+
+
+def paged_append(x, positions, host, *, block_rows: int, n_blocks: int) -> int:
+    """Write x ([n][Hk][D] fp32) into a paged fp16 host copy (uint16
+    [n_blocks][Hk][block_rows][D]) in place; returns the out-of-range count."""
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    n, Hk, D = x.shape
+    pos = np.ascontiguousarray(np.asarray(positions, dtype=np.int32))
+    assert host.dtype == np.uint16 and host.flags["C_CONTIGUOUS"]
+    bad = _load().orc_paged_append(Hk, D, int(block_rows), int(n_blocks), _ptr(x), _ptr(pos), n, _ptr(host))
+    if bad < 0:
+        raise ValueError("orc_paged_append rejected its arguments")
+    return int(bad)

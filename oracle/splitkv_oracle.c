@@ -293,3 +293,155 @@ void orc_set_threads(int n)
     (void)n;
 #endif
 }
+
+/* ---- appending rows ------------------------------------------------------
+ *
+ * Definitions (write routing: "Rolling KV", opencoti patch 0070, the window /
+ * host-tail split of the K/V copies; write-through: "Strata compare", KV
+ * streaming, the kv_append writers and their identity-layout host copy;
+ * quantisation: the same page's kv_append_q8 kernel):
+ *  - fp16 rows: each fp32 value rounded to the nearest binary16, ties to even.
+ *  - q8_0 block of 32 values, fp32 arithmetic: d = fp16(amax / 127);
+ *    q = nearest integer (ties to even) of x / d, clamped to [-127, 127];
+ *    d = 0 gives all codes 0.  The page's scale covers 64 values; the cache
+ *    rows here are q8_0, whose scale covers 32.
+ *  - q4_0 block: d = fp16(amax / 7); u = nearest integer of x / d, plus 8,
+ *    clamped to [0, 15]; byte j holds u_j (low nibble) and u_{j+16} (high).
+ *    The pages give no q4_0 quantiser: this reading keeps the q8 rule.
+ */
+
+/* fp32 -> IEEE 754 binary16, round to nearest, ties to even, from the format's
+ * definition (value = 2^(e-15) * (1 + f/1024), subnormals 2^-24 * f).  The
+ * scalings below are by powers of two, so they are exact in double. */
+uint16_t orc_float_to_half(float xf)
+{
+    const double x = (double)xf;
+    const uint16_t sign = signbit(x) ? 0x8000 : 0;
+    const double a = fabs(x);
+    if (isnan(a)) return sign | 0x7e00;
+    if (isinf(a)) return sign | 0x7c00;
+    if (a < ldexp(1.0, -14)) {                       /* subnormal range: units of 2^-24 */
+        const double f = nearbyint(ldexp(a, 24));      /* 1024 here is the smallest normal */
+        return sign | (uint16_t)f;
+    }
+    int e2;
+    frexp(a, &e2);                                   /* a in [2^(e2-1), 2^e2) */
+    int e = e2 - 1;
+    double f = nearbyint(ldexp(a, 10 - e));          /* significand in units of 2^(e-10) */
+    if (f == 2048.0) {                               /* rounded up to the next binade */
+        f = 1024.0;
+        e += 1;
+    }
+    if (e + 15 >= 31) return sign | 0x7c00;          /* overflow to infinity */
+    return sign | (uint16_t)((e + 15) << 10) | (uint16_t)(f - 1024.0);
+}
+
+/* One 32-value block of q8_0 (34 bytes) or q4_0 (18 bytes). */
+static void quantize_block(int type, const float *x, uint8_t *blk)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < 32; ++i) {
+        const float a = fabsf(x[i]);
+        if (a > amax) amax = a;
+    }
+    const float qmax = type == ORC_Q8_0 ? 127.0f : 7.0f;
+    const uint16_t dbits = orc_float_to_half(amax / qmax);
+    const float d = (float)orc_half_to_double(dbits);
+    blk[0] = (uint8_t)(dbits & 0xff);                /* little-endian fp16 scale */
+    blk[1] = (uint8_t)(dbits >> 8);
+    int code[32];
+    for (int i = 0; i < 32; ++i) code[i] = d > 0.0f ? (int)rintf(x[i] / d) : 0;
+    if (type == ORC_Q8_0) {
+        for (int i = 0; i < 32; ++i) {
+            int q = code[i];
+            if (q < -127) q = -127;
+            if (q > 127) q = 127;
+            blk[2 + i] = (uint8_t)(int8_t)q;
+        }
+    } else {
+        for (int j = 0; j < 16; ++j) {
+            int lo = code[j] + 8, hi = code[j + 16] + 8;
+            lo = lo < 0 ? 0 : (lo > 15 ? 15 : lo);
+            hi = hi < 0 ? 0 : (hi > 15 ? 15 : hi);
+            blk[2 + j] = (uint8_t)(lo | (hi << 4));
+        }
+    }
+}
+
+/* Encode D values (one head) into its segment of the given type. */
+static void encode_segment(int type, const float *x, int D, uint8_t *seg)
+{
+    if (type == ORC_F16) {
+        for (int d = 0; d < D; ++d) {
+            const uint16_t b = orc_float_to_half(x[d]);
+            seg[2 * d] = (uint8_t)(b & 0xff);
+            seg[2 * d + 1] = (uint8_t)(b >> 8);
+        }
+        return;
+    }
+    const int blk = type == ORC_Q8_0 ? 34 : 18;
+    for (int b = 0; b < D / 32; ++b) quantize_block(type, x + 32 * b, seg + (int64_t)b * blk);
+}
+
+/* Exported: encode n_values (a multiple of 32 for quantised types) values. */
+int orc_quantize(int type, const float *x, int64_t n_values, void *out)
+{
+    if (orc_segment_bytes(type, 32) < 0 || n_values < 0 || (type != ORC_F16 && n_values % 32)) return 1;
+    uint8_t *o = (uint8_t *)out;
+    if (type == ORC_F16) {
+        encode_segment(ORC_F16, x, (int)n_values, o);
+        return 0;
+    }
+    const int blk = type == ORC_Q8_0 ? 34 : 18;
+    for (int64_t b = 0; b < n_values / 32; ++b) quantize_block(type, x + 32 * b, o + b * blk);
+    return 0;
+}
+
+/* Cell-major append: row i of x ([n][Hk][D] fp32) goes to cache position
+ * positions[i]; p < n_rows0 is row p of region 0, otherwise row p - n_rows0 of
+ * region 1 (row stride row_bytes, head k at byte k * segment).  Negative
+ * positions are skipped; positions >= n_rows0 + n_rows1 are skipped and
+ * counted.  Rows are written in order i = 0, 1, ...  Returns the count of
+ * out-of-range positions, or -1 for bad arguments. */
+int64_t orc_kv_append(int type, int Hk, int D, int64_t row_bytes, const float *x, const int32_t *positions,
+                      int64_t n, void *dst0, int64_t n_rows0, void *dst1, int64_t n_rows1)
+{
+    const int64_t seg = orc_segment_bytes(type, D);
+    if (seg < 0 || D % 32 || row_bytes < Hk * seg) return -1;
+    int64_t bad = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        const int64_t p = positions[i];
+        if (p < 0) continue;
+        if (p >= n_rows0 + n_rows1) {
+            ++bad;
+            continue;
+        }
+        uint8_t *row = p < n_rows0 ? (uint8_t *)dst0 + p * row_bytes : (uint8_t *)dst1 + (p - n_rows0) * row_bytes;
+        for (int k = 0; k < Hk; ++k) encode_segment(type, x + (i * Hk + k) * D, D, row + k * seg);
+    }
+    return bad;
+}
+
+/* Paged append into a host copy laid out [n_blocks][Hk][block_rows][D] fp16:
+ * position p, head k lands at page (p / block_rows) * Hk + k, row
+ * p % block_rows.  Same skipping and return value as orc_kv_append. */
+int64_t orc_paged_append(int Hk, int D, int block_rows, int64_t n_blocks, const float *x, const int32_t *positions,
+                         int64_t n, uint16_t *host)
+{
+    if (Hk <= 0 || D <= 0 || block_rows <= 0) return -1;
+    int64_t bad = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        const int64_t p = positions[i];
+        if (p < 0) continue;
+        if (p >= n_blocks * block_rows) {
+            ++bad;
+            continue;
+        }
+        const int64_t blk = p / block_rows, in_blk = p % block_rows;
+        for (int k = 0; k < Hk; ++k) {
+            uint16_t *dst = host + (((blk * Hk + k) * block_rows) + in_blk) * D;
+            for (int d = 0; d < D; ++d) dst[d] = orc_float_to_half(x[(i * Hk + k) * D + d]);
+        }
+    }
+    return bad;
+}

@@ -21,7 +21,7 @@ from . import _lib
 from ._lib import F16, Q4_0, Q8_0, SkvShape
 
 __all__ = ["Handle", "SplitKVError", "F16", "Q8_0", "Q4_0", "attn_partial", "attn_combine", "attn_window_tail",
-           "attn_paged", "BlockCache", "kv_dequant_q8_0", "kv_dequant_q4_0", "gather_rows", "plan_splits",
+           "attn_paged", "BlockCache", "kv_dequant_q8_0", "kv_dequant_q4_0", "gather_rows", "kv_append", "plan_splits",
            "segment_bytes"]
 
 
@@ -241,6 +241,11 @@ class BlockCache:
         self.h.check(_lib.lib().skv_bcache_resolve(self._c, _ptr(sel), S, n_sel, _ptr(page_ids), _stream(stream)))
         return page_ids
 
+    def append(self, k_new, v_new, positions, stream=None):
+        """Write-through append of fp32 rows [n][Hk][D] at cache positions."""
+        self.h.check(_lib.lib().skv_bcache_append(self._c, _ptr(k_new), _ptr(v_new), _ptr(positions),
+                                                  int(positions.numel()), _stream(stream)))
+
     def attn(self, q, sel, *, scale=None, o=None, lse=None, stream=None):
         sh = _shape(q, self.Hk, F16, F16, None, None, scale)
         o, lse = _outputs(q, o, lse)
@@ -303,3 +308,20 @@ def gather_rows(h: Handle, src, rows, *, row_bytes=None, out=None, stream=None):
     h.check(_lib.lib().skv_gather_rows(h.ptr, _ptr(src), int(row_bytes), _ptr(rows), n, _ptr(out),
                                        _stream(stream)))
     return out
+
+
+def kv_append(h: Handle, x, positions, dst0, dst1=None, *, type_=F16, n_rows0=None, n_rows1=None, row_bytes=None,
+              stream=None):
+    """Write x (fp32 [n][Hk][D], device) into a two-region cell-major cache:
+    position p < n_rows0 goes to row p of dst0, otherwise row p - n_rows0 of
+    dst1 (device or page-locked host).  Rows are converted to fp16 or
+    quantised to q8_0 / q4_0 according to type_."""
+    n, Hk, D = (int(s) for s in x.shape)
+    if row_bytes is None:
+        row_bytes = Hk * segment_bytes(type_, D)
+    if n_rows0 is None:
+        n_rows0 = 0 if dst0 is None else dst0.numel() * dst0.element_size() // row_bytes
+    if n_rows1 is None:
+        n_rows1 = 0 if dst1 is None else dst1.numel() * dst1.element_size() // row_bytes
+    h.check(_lib.lib().skv_kv_append(h.ptr, int(type_), Hk, D, int(row_bytes), _ptr(x), _ptr(positions), n,
+                                     _ptr(dst0), int(n_rows0), _ptr(dst1), int(n_rows1), _stream(stream)))

@@ -21,9 +21,9 @@ F16, Q8_0, Q4_0 = 0, 1, 2
 EXPORTS = [
     "skv_create", "skv_destroy", "skv_last_error", "skv_status_string", "skv_reserve", "skv_scratch_info",
     "skv_sm_count", "skv_status", "skv_set_profile_events", "skv_plan_splits", "skv_attn_partial", "skv_attn_combine", "skv_attn_window_tail",
-    "skv_kv_dequant_q8_0", "skv_kv_dequant_q4_0", "skv_gather_rows",
+    "skv_kv_dequant_q8_0", "skv_kv_dequant_q4_0", "skv_gather_rows", "skv_kv_append",
     "skv_attn_paged", "skv_bcache_create", "skv_bcache_destroy", "skv_bcache_reset", "skv_bcache_resolve",
-    "skv_bcache_attn", "skv_bcache_stats", "skv_bcache_check", "skv_bcache_pool",
+    "skv_bcache_append", "skv_bcache_attn", "skv_bcache_stats", "skv_bcache_check", "skv_bcache_pool",
     "skv_attn_partial_static", "skv_plan_window", "skv_plan_tail_tile",
 ]
 
@@ -60,6 +60,8 @@ def _declare(lib):
         "skv_kv_dequant_q8_0": ([P, P, I64, P, P], ctypes.c_int),
         "skv_kv_dequant_q4_0": ([P, P, I64, P, P], ctypes.c_int),
         "skv_gather_rows": ([P, P, I64, P, I64, P, P], ctypes.c_int),
+        "skv_kv_append": ([P, I32, I32, I32, I64, P, P, I32, P, I64, P, I64, P], ctypes.c_int),
+        "skv_bcache_append": ([P, P, P, P, I32, P], ctypes.c_int),
         "skv_plan_window": ([I64, I64, I64, I64, I64, I32, ctypes.POINTER(I64)], ctypes.c_int),
         "skv_plan_tail_tile": ([I64, I64, I32, I64, I64, I32, ctypes.POINTER(I64), ctypes.POINTER(I32)],
                                ctypes.c_int),

@@ -36,8 +36,8 @@ struct skv_bcache {
     int n_slots = 0;
     int64_t max_lookups = 0;
     int64_t page_bytes = 0;
-    const uint8_t *host_k = nullptr;   // device-accessible addresses of the pinned host copy
-    const uint8_t *host_v = nullptr;
+    uint8_t *host_k = nullptr;         // device-accessible addresses of the pinned host copy
+    uint8_t *host_v = nullptr;
     int32_t *page_table = nullptr;     // [n_blocks*Hk] slot, -1, or transient markers
     int32_t *slot_page = nullptr;      // [n_slots]
     int32_t *slot_epoch = nullptr;     // [n_slots]
@@ -239,6 +239,49 @@ __global__ void __launch_bounds__(256) bcache_fetch_kernel(const uint64_t *__res
     }
 }
 
+// Write-through append (the writers of the Strata KV-streaming page): cache
+// position p is row p % block_rows of block p / block_rows; each (position, KV
+// head) writes its fp16 K and V row into the host copy always and into the
+// pool page only when the page is resident (page_table >= 0), so a resident
+// page never differs from the host copy.  One warp per (position, KV head);
+// each lane converts 8 values into one 16-byte store.  Positions outside
+// [0, n_blocks * block_rows) are skipped and set bit 1 of *status.
+__global__ void __launch_bounds__(256) bcache_append_kernel(const float *__restrict__ k_new,
+                                                            const float *__restrict__ v_new,
+                                                            const int32_t *__restrict__ pos, int n, int Hk, int D,
+                                                            int block_rows, int64_t n_blocks,
+                                                            const int32_t *__restrict__ page_table, uint8_t *host_k,
+                                                            uint8_t *host_v, uint8_t *pool_k, uint8_t *pool_v,
+                                                            int64_t page_bytes, int *status)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t item = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (item >= static_cast<int64_t>(n) * Hk) return;
+    const int r = static_cast<int>(item / Hk);
+    const int k = static_cast<int>(item % Hk);
+    const int64_t p = pos[r];
+    if (p < 0) return;
+    if (p >= n_blocks * block_rows) {
+        if (lane == 0 && k == 0) atomicOr(status, 2);
+        return;
+    }
+    const int64_t page = (p / block_rows) * Hk + k;
+    const int slot = page_table[page];
+    const int64_t off = (p % block_rows) * D * 2;                 // byte offset of the row inside its page
+    const int chunks = D / 8;                                     // 16-byte chunks per row
+    for (int c = lane; c < 2 * chunks; c += 32) {
+        const bool is_v = c >= chunks;
+        const int cc = is_v ? c - chunks : c;
+        const float4 *src = reinterpret_cast<const float4 *>((is_v ? v_new : k_new) + item * D) + 2 * cc;
+        const float4 a = src[0], b = src[1];
+        __half2 h[4] = {__floats2half2_rn(a.x, a.y), __floats2half2_rn(a.z, a.w), __floats2half2_rn(b.x, b.y),
+                        __floats2half2_rn(b.z, b.w)};
+        const uint4 w = *reinterpret_cast<const uint4 *>(h);
+        reinterpret_cast<uint4 *>((is_v ? host_v : host_k) + page * page_bytes + off)[cc] = w;
+        if (slot >= 0) reinterpret_cast<uint4 *>((is_v ? pool_v : pool_k) + slot * page_bytes + off)[cc] = w;
+    }
+}
+
 __global__ void bcache_reset_kernel(int32_t *page_table, int64_t n_pages, int32_t *slot_page, int32_t *slot_epoch,
                                     int32_t *slot_ref, int n_slots, uint64_t *ctl)
 {
@@ -338,8 +381,8 @@ int skv_bcache_create(skv_handle *h, int64_t n_blocks, int32_t block_rows, int32
     c->n_slots = n_slots;
     c->max_lookups = max_lookups;
     c->page_bytes = static_cast<int64_t>(block_rows) * D * 2;
-    c->host_k = static_cast<const uint8_t *>(dk);
-    c->host_v = static_cast<const uint8_t *>(dv);
+    c->host_k = static_cast<uint8_t *>(const_cast<void *>(dk));
+    c->host_v = static_cast<uint8_t *>(const_cast<void *>(dv));
     const int64_t n_pages = n_blocks * Hk;
     const size_t pool_pages = static_cast<size_t>(n_slots) + static_cast<size_t>(max_lookups);
     cudaError_t e = cudaSuccess;
@@ -405,6 +448,27 @@ int skv_bcache_resolve(skv_bcache *c, const int32_t *sel, int32_t S, int32_t n_s
     bcache_fetch_kernel<<<2 * h->sm_count, 256, 0, st>>>(c->ctl, c->miss_page, c->miss_dest, c->host_k, c->host_v,
                                                          c->pool_k, c->pool_v, c->page_bytes);
     return cuda_fail(h, cudaGetLastError(), "fetch launch");
+}
+
+int skv_bcache_append(skv_bcache *c, const float *k_new, const float *v_new, const int32_t *positions, int32_t n,
+                      void *stream)
+{
+    if (!c) return SKV_EINVAL;
+    skv_handle *h = c->h;
+    h->err[0] = 0;
+    if (n < 0) return fail(h, SKV_EINVAL, "negative row count");
+    if (n == 0) return SKV_OK;
+    if (!k_new || !v_new || !positions) return fail(h, SKV_EINVAL, "NULL pointer");
+    if (reinterpret_cast<uintptr_t>(k_new) % 16 || reinterpret_cast<uintptr_t>(v_new) % 16)
+        return fail(h, SKV_EUNSUPPORTED, "k_new / v_new must be 16-byte aligned");
+    if (reinterpret_cast<uintptr_t>(c->host_k) % 16 || reinterpret_cast<uintptr_t>(c->host_v) % 16)
+        return fail(h, SKV_EUNSUPPORTED, "the host copy must be 16-byte aligned for appends");
+    const int64_t items = static_cast<int64_t>(n) * c->Hk;
+    if ((items + 7) / 8 > 0x7fffffffLL) return fail(h, SKV_EUNSUPPORTED, "too many rows for one launch");
+    bcache_append_kernel<<<static_cast<unsigned>((items + 7) / 8), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        k_new, v_new, positions, n, c->Hk, c->D, c->block_rows, c->n_blocks, c->page_table, c->host_k, c->host_v,
+        c->pool_k, c->pool_v, c->page_bytes, h->status);
+    return cuda_fail(h, cudaGetLastError(), "block-cache append");
 }
 
 int skv_bcache_stats(skv_bcache *c, skv_bcache_counters *out)

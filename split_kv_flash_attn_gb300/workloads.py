@@ -213,3 +213,17 @@ def redraw_selection(sel: np.ndarray, n_blocks: int, frac: float,
             row[drop] = add
             out[s, kh] = np.sort(row)
     return out
+
+
+def new_kv_values(rng: np.random.Generator, n: int, Hk: int, D: int, outlier_channels: int = 4):
+    """fp32 K and V values [n][Hk][D] for appends: standard normals, with a few
+    K channels per head scaled up 8x (the outlier channels of key activations)
+    and one row in 16 of V scaled by 1e-3 (tiny blocks reach fp16 subnormal
+    scales).  Returns (k, v)."""
+    k = rng.standard_normal((n, Hk, D), dtype=np.float32)
+    v = rng.standard_normal((n, Hk, D), dtype=np.float32)
+    for h in range(Hk):
+        ch = rng.choice(D, size=min(outlier_channels, D), replace=False)
+        k[:, h, ch] *= 8.0
+    v[::16] *= 1e-3
+    return k, v

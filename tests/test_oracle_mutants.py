@@ -1,8 +1,8 @@
 """The oracle's pins must catch plausible mistakes.
 
 Each case plants one mistake in a copy of oracle/splitkv_oracle.c (on the CPU),
-builds it, and runs the pin suite (tests/test_oracle_pins.py) against that
-build; the suite must fail.  A mutant that survived would mean a part of the
+builds it, and runs the pin suites (tests/test_oracle_pins.py and
+tests/test_oracle_append_pins.py) against that build; the suite must fail.  A mutant that survived would mean a part of the
 oracle is not pinned by anything but itself."""
 import os
 import subprocess
@@ -37,7 +37,24 @@ MUTANTS = [
     ("not_normalised", "for (int d = 0; d < D; ++d) o[d] = acc[d] / Z;", "for (int d = 0; d < D; ++d) o[d] = acc[d];"),
     ("combine_unweighted", "const double w = exp(l - M);", "const double w = 1.0;"),
     ("combine_lse", "lse[r] = M + log(W);", "lse[r] = log(W);"),
+    ("half_ties_away", "double f = nearbyint(ldexp(a, 10 - e));", "double f = floor(ldexp(a, 10 - e) + 0.5);"),
+    ("half_truncates", "double f = nearbyint(ldexp(a, 10 - e));", "double f = floor(ldexp(a, 10 - e));"),
+    ("half_subnormal_rounding", "const double f = nearbyint(ldexp(a, 24));", "const double f = floor(ldexp(a, 24));"),
+    ("q8_scale_128", "const float qmax = type == ORC_Q8_0 ? 127.0f : 7.0f;",
+     "const float qmax = type == ORC_Q8_0 ? 128.0f : 7.0f;"),
+    ("q4_scale_8", "const float qmax = type == ORC_Q8_0 ? 127.0f : 7.0f;",
+     "const float qmax = type == ORC_Q8_0 ? 127.0f : 8.0f;"),
+    ("codes_truncated", "code[i] = d > 0.0f ? (int)rintf(x[i] / d) : 0;", "code[i] = d > 0.0f ? (int)(x[i] / d) : 0;"),
+    ("q4_append_nibbles", "blk[2 + j] = (uint8_t)(lo | (hi << 4));", "blk[2 + j] = (uint8_t)(hi | (lo << 4));"),
+    ("append_input_transposed", "encode_segment(type, x + (i * Hk + k) * D, D, row + k * seg);",
+     "encode_segment(type, x + (k * n + i) * D, D, row + k * seg);"),
+    ("append_region_split", "uint8_t *row = p < n_rows0 ? (uint8_t *)dst0 + p * row_bytes",
+     "uint8_t *row = p < n_rows0 - 1 ? (uint8_t *)dst0 + p * row_bytes"),
+    ("paged_append_order", "uint16_t *dst = host + (((blk * Hk + k) * block_rows) + in_blk) * D;",
+     "uint16_t *dst = host + (((k * n_blocks + blk) * block_rows) + in_blk) * D;"),
 ]
+
+PIN_FILES = ["test_oracle_pins.py", "test_oracle_append_pins.py"]
 
 
 def _build(tmp_path, name, old, new):
@@ -57,6 +74,6 @@ def test_pins_catch_mutant(tmp_path, name, old, new):
     so = _build(tmp_path, name, old, new)
     env = dict(os.environ, SPLITKV_ORACLE_LIB=str(so), OMP_NUM_THREADS="2")
     res = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                          os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                          *[os.path.join(ROOT, "tests", f) for f in PIN_FILES]],
                          cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
     assert res.returncode != 0, f"mutant {name} survived the oracle pins:\n{res.stdout[-2000:]}"
