@@ -574,6 +574,25 @@ def bench_append(torch, skv, wl, h, hbm_peak):
     p1 = pc[:1]
     out["bcache_decode_row_us"] = _graph_us(torch, lambda: c.append(x1, x1, p1))
     c.close()
+    # ring layout: a 128-block ring (8192 cells) over the same host copy; one
+    # decode step = append one row + attention of 32 q heads over the last
+    # 4096 cells through the ring
+    r = skv.BlockCache(h, hk, hv, n_blocks=nb, block_rows=br, Hk=Hk, D=D, ring_blocks=128, max_seqs=1)
+    n_keys = nb * br - 64
+    r.ring_restore(n_keys)
+    q = torch.from_numpy(wl.normal_f16(rng, (1, 1, 4 * Hk, D))).cuda()
+    o = torch.empty((1, 1, 4 * Hk, D), dtype=torch.float32, device="cuda")
+    lse = torch.empty((1, 1, 4 * Hk), dtype=torch.float32, device="cuda")
+    pn = torch.full((1,), n_keys, dtype=torch.int32, device="cuda")
+
+    def ring_step():
+        r.append(x1, x1, pn)
+        r.ring_attn(q, n_keys + 1, 4096, o=o, lse=lse)
+    us = _graph_us(torch, ring_step, per_graph=20, replays=20)
+    out["ring_decode_step"] = {"window": 4096, "ring_cells": 128 * br, "us_per_step": us,
+                               "tokens_heads_per_s": 4 * Hk / (us * 1e-6),
+                               "kv_bytes_per_step": 4096 * Hk * 2 * D * 2}
+    r.close()
     h.status()
     return out
 

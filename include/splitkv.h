@@ -361,6 +361,35 @@ int skv_bcache_stats(skv_bcache *c, skv_bcache_counters *out);
  * inverse maps; no page left claimed); synchronises the device. */
 int skv_bcache_check(skv_bcache *c, int32_t *violations);
 
+/* Ring layout ("Strata compare", KV streaming: a reader that only ever reads
+ * its last cells uses the same host copy with a static table block ->
+ * block % n_slots and no resolve, and the ring is refilled from the host copy
+ * on a resume).  The cache holds ring_blocks blocks (ring_blocks * Hk pages):
+ * page (block b, KV head k) lives in pool page (b % ring_blocks) * Hk + k.
+ * skv_bcache_append then writes every row into the host copy and its ring
+ * page (a newer block overwrites the block ring_blocks before it);
+ * skv_bcache_resolve / skv_bcache_attn return SKV_EUNSUPPORTED.  max_seqs
+ * bounds shape->S of skv_bcache_ring_attn.  After creation or a reset the
+ * ring's contents are undefined until skv_bcache_ring_restore. */
+int skv_bcache_create_ring(skv_handle *h, int64_t n_blocks, int32_t block_rows, int32_t Hk, int32_t D,
+                           int32_t ring_blocks, int32_t max_seqs, const void *host_k, const void *host_v,
+                           skv_bcache **out);
+
+/* Refill the ring for a cache of n_keys cells: the pages of the last
+ * min(ring_blocks, blocks in use) blocks are copied from the host copy into
+ * their ring pages (stream-ordered; 0 <= n_keys <= n_blocks * block_rows). */
+int skv_bcache_ring_restore(skv_bcache *c, int64_t n_keys, void *stream);
+
+/* Attention of q [S][nq][H][D] over cells [max(0, n_keys - window), n_keys)
+ * read through the ring (window <= 0: every cell the ring holds, i.e. from the
+ * first cell of block max(0, last - ring_blocks + 1), last = (n_keys-1) /
+ * block_rows).  Every query token sees the same cells.  A window reaching
+ * past the ring's oldest cell is SKV_EINVAL.  Results are those of attention
+ * over the same cells of the host copy, provided the ring was restored and
+ * every later append went through skv_bcache_append. */
+int skv_bcache_ring_attn(skv_bcache *c, const skv_shape *shape, const void *q, int64_t n_keys, int64_t window,
+                         float *o, float *lse, void *stream);
+
 /* Device pointers of the page pool and of the last resolve's page ids. */
 int skv_bcache_pool(const skv_bcache *c, const void **k_pages, const void **v_pages, int64_t *n_pool_pages,
                     const int32_t **last_page_ids);

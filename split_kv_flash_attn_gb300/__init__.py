@@ -225,13 +225,32 @@ def attn_paged(h: Handle, q, k_pages, v_pages, page_ids, *, Hk, page_rows, scale
 class BlockCache:
     """Device block cache over a pinned paged host copy [n_blocks][Hk][block_rows][D] fp16."""
 
-    def __init__(self, h: Handle, host_k, host_v, *, n_blocks, block_rows, Hk, D, n_slots, max_lookups):
+    def __init__(self, h: Handle, host_k, host_v, *, n_blocks, block_rows, Hk, D, n_slots=0, max_lookups=0,
+                 ring_blocks=0, max_seqs=1):
+        """ring_blocks > 0 makes a ring (static table block -> block % ring_blocks)."""
         self.h = h
         self.Hk, self.D, self.block_rows = int(Hk), int(D), int(block_rows)
+        self.ring_blocks = int(ring_blocks)
         self._c = ctypes.c_void_p()
-        h.check(_lib.lib().skv_bcache_create(h.ptr, int(n_blocks), int(block_rows), int(Hk), int(D), int(n_slots),
-                                             int(max_lookups), _ptr(host_k), _ptr(host_v), ctypes.byref(self._c)))
+        if self.ring_blocks > 0:
+            h.check(_lib.lib().skv_bcache_create_ring(h.ptr, int(n_blocks), int(block_rows), int(Hk), int(D),
+                                                      self.ring_blocks, int(max_seqs), _ptr(host_k), _ptr(host_v),
+                                                      ctypes.byref(self._c)))
+        else:
+            h.check(_lib.lib().skv_bcache_create(h.ptr, int(n_blocks), int(block_rows), int(Hk), int(D),
+                                                 int(n_slots), int(max_lookups), _ptr(host_k), _ptr(host_v),
+                                                 ctypes.byref(self._c)))
         self._keep = (host_k, host_v)
+
+    def ring_restore(self, n_keys, stream=None):
+        self.h.check(_lib.lib().skv_bcache_ring_restore(self._c, int(n_keys), _stream(stream)))
+
+    def ring_attn(self, q, n_keys, window=0, *, scale=None, o=None, lse=None, stream=None):
+        sh = _shape(q, self.Hk, F16, F16, None, None, scale)
+        o, lse = _outputs(q, o, lse)
+        self.h.check(_lib.lib().skv_bcache_ring_attn(self._c, ctypes.byref(sh), _ptr(q), int(n_keys), int(window),
+                                                     _ptr(o), _ptr(lse), _stream(stream)))
+        return o, lse
 
     def reset(self, stream=None):
         self.h.check(_lib.lib().skv_bcache_reset(self._c, _stream(stream)))

@@ -24,6 +24,7 @@ EXPORTS = [
     "skv_kv_dequant_q8_0", "skv_kv_dequant_q4_0", "skv_gather_rows", "skv_kv_append",
     "skv_attn_paged", "skv_bcache_create", "skv_bcache_destroy", "skv_bcache_reset", "skv_bcache_resolve",
     "skv_bcache_append", "skv_bcache_attn", "skv_bcache_stats", "skv_bcache_check", "skv_bcache_pool",
+    "skv_bcache_create_ring", "skv_bcache_ring_restore", "skv_bcache_ring_attn",
     "skv_attn_partial_static", "skv_plan_window", "skv_plan_tail_tile",
 ]
 
@@ -62,6 +63,9 @@ def _declare(lib):
         "skv_gather_rows": ([P, P, I64, P, I64, P, P], ctypes.c_int),
         "skv_kv_append": ([P, I32, I32, I32, I64, P, P, I32, P, I64, P, I64, P], ctypes.c_int),
         "skv_bcache_append": ([P, P, P, P, I32, P], ctypes.c_int),
+        "skv_bcache_create_ring": ([P, I64, I32, I32, I32, I32, I32, P, P, ctypes.POINTER(P)], ctypes.c_int),
+        "skv_bcache_ring_restore": ([P, I64, P], ctypes.c_int),
+        "skv_bcache_ring_attn": ([P, SH, P, I64, I64, P, P, P], ctypes.c_int),
         "skv_plan_window": ([I64, I64, I64, I64, I64, I32, ctypes.POINTER(I64)], ctypes.c_int),
         "skv_plan_tail_tile": ([I64, I64, I32, I64, I64, I32, ctypes.POINTER(I64), ctypes.POINTER(I32)],
                                ctypes.c_int),

@@ -693,7 +693,19 @@ int skv_attn_paged(skv_handle *h, const skv_shape *shape, const void *q, const v
 {
     if (!h) return SKV_EINVAL;
     h->err[0] = 0;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return attn_paged_range(h, shape, q, k_pages, v_pages, page_rows, page_ids, pages_per_list, 0,
+                            static_cast<int64_t>(pages_per_list) * page_rows, o, lse,
+                            static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
+
+namespace skv {
+
+int attn_paged_range(skv_handle *h, const skv_shape *shape, const void *q, const void *k_pages, const void *v_pages,
+                     int32_t page_rows, const int32_t *page_ids, int32_t pages_per_list, int64_t key_lo,
+                     int64_t key_hi, float *o, float *lse, cudaStream_t st)
+{
     if (!shape) return fail(h, SKV_EINVAL, "shape is NULL");
     if (shape->k_type != SKV_F16 || shape->v_type != SKV_F16)
         return fail(h, SKV_EUNSUPPORTED, "paged attention reads fp16 pages");
@@ -710,8 +722,11 @@ int skv_attn_paged(skv_handle *h, const skv_shape *shape, const void *q, const v
         return fail(h, SKV_EUNSUPPORTED, "page pools must be 16-byte aligned");
     const int D = sh.D;
     const int64_t R = static_cast<int64_t>(sh.S) * sh.nq * sh.H;
-    const int64_t n_local = static_cast<int64_t>(pages_per_list) * page_rows;
-    if (n_local == 0) {
+    const int64_t n_local = key_hi;
+    if (key_lo < 0 || key_hi < key_lo || key_hi > static_cast<int64_t>(pages_per_list) * page_rows)
+        return fail(h, SKV_EINVAL, "key range [%lld, %lld) outside the page lists", (long long)key_lo,
+                    (long long)key_hi);
+    if (n_local == key_lo) {
         rc = launch_combine(0, nullptr, nullptr, R, D, o, lse, st);
         return rc == SKV_OK ? rc : cuda_fail(h, cudaGetLastError(), "fill launch");
     }
@@ -722,11 +737,12 @@ int skv_attn_paged(skv_handle *h, const skv_shape *shape, const void *q, const v
     int32_t n_splits = 0;
     // splits end on page boundaries so that each CTA's page list is whole
     const int64_t max_split = std::max<int64_t>(page_rows, (kMaxListSplit / page_rows) * page_rows);
-    rc = skv_plan_splits(n_local, units, h->sm_count, ctas, std::max(kDecodeTile, page_rows), max_split, &split_len,
-                         &n_splits);
+    rc = skv_plan_splits(n_local - key_lo, units, h->sm_count, ctas, std::max(kDecodeTile, page_rows), max_split,
+                         &split_len, &n_splits);
     if (rc) return fail(h, rc, "split planning failed");
     if (n_splits > kMaxSplits) return fail(h, SKV_EUNSUPPORTED, "%d splits exceed %d", n_splits, kMaxSplits);
     DecodeArgs a = base_args(&sh, G, n_cg, q, nullptr, 0, nullptr, 0);
+    a.key_lo = key_lo;
     a.k = static_cast<const uint8_t *>(k_pages);
     a.v = static_cast<const uint8_t *>(v_pages);
     a.row_mode = ROWS_PAGED;
@@ -750,4 +766,4 @@ int skv_attn_paged(skv_handle *h, const skv_shape *shape, const void *q, const v
     return launch_decode(h, a, SKV_F16, SKV_F16, D, st);
 }
 
-}  // extern "C"
+}  // namespace skv

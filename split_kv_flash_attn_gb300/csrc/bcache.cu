@@ -48,8 +48,9 @@ struct skv_bcache {
     int32_t *page_ids = nullptr;       // [max_lookups] of the last resolve
     uint64_t *ctl = nullptr;           // kCtlWords, see below
     int32_t *check = nullptr;          // invariant-violation counter
-    uint8_t *pool_k = nullptr;         // [(n_slots + max_lookups) pages][page_bytes]
+    uint8_t *pool_k = nullptr;         // [(n_slots + max_lookups) pages][page_bytes]; ring: [n_slots]
     uint8_t *pool_v = nullptr;
+    int64_t ring_blocks = 0;           // > 0: ring layout, page (b, k) -> slot (b % ring_blocks) * Hk + k
 };
 
 namespace skv {
@@ -313,6 +314,61 @@ __global__ void bcache_check_kernel(const int32_t *page_table, int64_t n_pages, 
     }
 }
 
+// Ring layout (the Strata KV-streaming page's ring for a reader of the last
+// cells only): a static table, page (block b, head k) -> slot
+// (b % ring_blocks) * Hk + k, no resolve.  Appends then write the host copy
+// and the ring slot of every row; a newer block overwrites the slot of the
+// block ring_blocks before it.
+__global__ void ring_init_kernel(int32_t *page_table, int64_t n_pages, int Hk, int64_t ring_blocks,
+                                 int32_t *slot_page, int n_slots, uint64_t *ctl)
+{
+    const int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t st = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t p = i0; p < n_pages; p += st)
+        page_table[p] = static_cast<int32_t>(((p / Hk) % ring_blocks) * Hk + p % Hk);
+    for (int64_t i = i0; i < n_slots; i += st) slot_page[i] = -1;
+    if (i0 < kCtlWords) ctl[i0] = 0;
+}
+
+// Refill: the pages of blocks [first, first + n_blk) become the fetch list
+// (page -> its ring slot); the fetch kernel then copies them from the host.
+__global__ void ring_restore_kernel(int64_t first, int n_blk, int Hk, int64_t ring_blocks, int32_t *miss_page,
+                                    int32_t *miss_dest, int32_t *slot_page, uint64_t *ctl)
+{
+    const int n = n_blk * Hk;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int64_t b = first + i / Hk;
+        const int k = i % Hk;
+        const int32_t slot = static_cast<int32_t>((b % ring_blocks) * Hk + k);
+        miss_page[i] = static_cast<int32_t>(b * Hk + k);
+        miss_dest[i] = slot;
+        slot_page[slot] = static_cast<int32_t>(b * Hk + k);
+    }
+    if (threadIdx.x == 0) ctl[9] = static_cast<uint64_t>(n);
+}
+
+// Page lists [S][Hk][n_blk] of blocks first .. first + n_blk - 1 through the ring.
+__global__ void ring_ids_kernel(int64_t first, int n_blk, int S, int Hk, int64_t ring_blocks, int32_t *ids)
+{
+    const int64_t n = static_cast<int64_t>(S) * Hk * n_blk;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int j = static_cast<int>(i % n_blk);
+        const int k = static_cast<int>((i / n_blk) % Hk);
+        ids[i] = static_cast<int32_t>(((first + j) % ring_blocks) * Hk + k);
+    }
+}
+
+// Ring invariant: every page maps to its static slot.
+__global__ void ring_check_kernel(const int32_t *page_table, int64_t n_pages, int Hk, int64_t ring_blocks,
+                                  int32_t *violations)
+{
+    const int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t st = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t p = i0; p < n_pages; p += st)
+        if (page_table[p] != ((p / Hk) % ring_blocks) * Hk + p % Hk) atomicAdd(violations, 1);
+}
+
 }  // namespace skv
 
 using namespace skv;
@@ -342,13 +398,19 @@ int skv_bcache_reset(skv_bcache *c, void *stream)
 {
     if (!c) return SKV_EINVAL;
     const int64_t n_pages = c->n_blocks * c->Hk;
-    bcache_reset_kernel<<<256, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        c->page_table, n_pages, c->slot_page, c->slot_epoch, c->slot_ref, c->n_slots, c->ctl);
+    if (c->ring_blocks > 0)
+        ring_init_kernel<<<256, 256, 0, static_cast<cudaStream_t>(stream)>>>(c->page_table, n_pages, c->Hk,
+                                                                            c->ring_blocks, c->slot_page,
+                                                                            c->n_slots, c->ctl);
+    else
+        bcache_reset_kernel<<<256, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+            c->page_table, n_pages, c->slot_page, c->slot_epoch, c->slot_ref, c->n_slots, c->ctl);
     return cuda_fail(c->h, cudaGetLastError(), "block-cache reset");
 }
 
-int skv_bcache_create(skv_handle *h, int64_t n_blocks, int32_t block_rows, int32_t Hk, int32_t D, int32_t n_slots,
-                      int64_t max_lookups, const void *host_k, const void *host_v, skv_bcache **out)
+static int bcache_create_impl(skv_handle *h, int64_t n_blocks, int32_t block_rows, int32_t Hk, int32_t D,
+                              int32_t n_slots, int64_t max_lookups, int64_t ring_blocks, const void *host_k,
+                              const void *host_v, skv_bcache **out)
 {
     if (!h || !out) return SKV_EINVAL;
     h->err[0] = 0;
@@ -380,11 +442,12 @@ int skv_bcache_create(skv_handle *h, int64_t n_blocks, int32_t block_rows, int32
     c->D = D;
     c->n_slots = n_slots;
     c->max_lookups = max_lookups;
+    c->ring_blocks = ring_blocks;
     c->page_bytes = static_cast<int64_t>(block_rows) * D * 2;
     c->host_k = static_cast<uint8_t *>(const_cast<void *>(dk));
     c->host_v = static_cast<uint8_t *>(const_cast<void *>(dv));
     const int64_t n_pages = n_blocks * Hk;
-    const size_t pool_pages = static_cast<size_t>(n_slots) + static_cast<size_t>(max_lookups);
+    const size_t pool_pages = static_cast<size_t>(n_slots) + (ring_blocks > 0 ? 0 : static_cast<size_t>(max_lookups));
     cudaError_t e = cudaSuccess;
     auto A = [&](void **p, size_t bytes) {
         if (e == cudaSuccess) e = cudaMalloc(p, bytes);
@@ -416,11 +479,33 @@ int skv_bcache_create(skv_handle *h, int64_t n_blocks, int32_t block_rows, int32
     return SKV_OK;
 }
 
+int skv_bcache_create(skv_handle *h, int64_t n_blocks, int32_t block_rows, int32_t Hk, int32_t D, int32_t n_slots,
+                      int64_t max_lookups, const void *host_k, const void *host_v, skv_bcache **out)
+{
+    return bcache_create_impl(h, n_blocks, block_rows, Hk, D, n_slots, max_lookups, 0, host_k, host_v, out);
+}
+
+int skv_bcache_create_ring(skv_handle *h, int64_t n_blocks, int32_t block_rows, int32_t Hk, int32_t D,
+                           int32_t ring_blocks, int32_t max_seqs, const void *host_k, const void *host_v,
+                           skv_bcache **out)
+{
+    if (!h || !out) return SKV_EINVAL;
+    h->err[0] = 0;
+    if (ring_blocks <= 0 || ring_blocks > n_blocks || max_seqs <= 0 || Hk <= 0)
+        return fail(h, SKV_EINVAL, "ring of %d blocks over %lld blocks, %d sequences", ring_blocks,
+                    (long long)n_blocks, max_seqs);
+    const int64_t slots = static_cast<int64_t>(ring_blocks) * Hk;
+    if (slots > 0x7fffffffLL || slots * max_seqs > 0x7fffffffLL) return fail(h, SKV_EUNSUPPORTED, "ring too large");
+    return bcache_create_impl(h, n_blocks, block_rows, Hk, D, static_cast<int32_t>(slots), slots * max_seqs,
+                              ring_blocks, host_k, host_v, out);
+}
+
 int skv_bcache_resolve(skv_bcache *c, const int32_t *sel, int32_t S, int32_t n_sel, int32_t *page_ids, void *stream)
 {
     if (!c) return SKV_EINVAL;
     skv_handle *h = c->h;
     h->err[0] = 0;
+    if (c->ring_blocks > 0) return fail(h, SKV_EUNSUPPORTED, "a ring cache has a static table and no resolve");
     if (!sel || S <= 0 || n_sel <= 0) return fail(h, SKV_EINVAL, "bad selection");
     const int64_t n_look = static_cast<int64_t>(S) * c->Hk * n_sel;
     if (n_look > c->max_lookups) return fail(h, SKV_EINVAL, "%lld lookups exceed max_lookups %lld",
@@ -493,7 +578,10 @@ int skv_bcache_check(skv_bcache *c, int32_t *violations)
     if (!c || !violations) return SKV_EINVAL;
     cudaError_t e = cudaMemset(c->check, 0, sizeof(int32_t));
     if (e != cudaSuccess) return cuda_fail(c->h, e, "check reset");
-    bcache_check_kernel<<<128, 256>>>(c->page_table, c->n_blocks * c->Hk, c->slot_page, c->n_slots, c->check);
+    if (c->ring_blocks > 0)
+        ring_check_kernel<<<128, 256>>>(c->page_table, c->n_blocks * c->Hk, c->Hk, c->ring_blocks, c->check);
+    else
+        bcache_check_kernel<<<128, 256>>>(c->page_table, c->n_blocks * c->Hk, c->slot_page, c->n_slots, c->check);
     e = cudaGetLastError();
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e == cudaSuccess) e = cudaMemcpy(violations, c->check, sizeof(int32_t), cudaMemcpyDeviceToHost);
@@ -506,7 +594,7 @@ int skv_bcache_pool(const skv_bcache *c, const void **k_pages, const void **v_pa
     if (!c) return SKV_EINVAL;
     if (k_pages) *k_pages = c->pool_k;
     if (v_pages) *v_pages = c->pool_v;
-    if (n_pool_pages) *n_pool_pages = c->n_slots + c->max_lookups;
+    if (n_pool_pages) *n_pool_pages = c->n_slots + (c->ring_blocks > 0 ? 0 : c->max_lookups);
     if (last_page_ids) *last_page_ids = c->page_ids;
     return SKV_OK;
 }
@@ -523,4 +611,58 @@ extern "C" int skv_bcache_attn(skv_bcache *c, const skv_shape *shape, const void
     int rc = skv_bcache_resolve(c, sel, shape->S, n_sel, c->page_ids, stream);
     if (rc) return rc;
     return skv_attn_paged(c->h, shape, q, c->pool_k, c->pool_v, c->block_rows, c->page_ids, n_sel, o, lse, stream);
+}
+
+extern "C" int skv_bcache_ring_restore(skv_bcache *c, int64_t n_keys, void *stream)
+{
+    if (!c) return SKV_EINVAL;
+    skv_handle *h = c->h;
+    h->err[0] = 0;
+    if (c->ring_blocks <= 0) return skv::fail(h, SKV_EINVAL, "not a ring cache");
+    if (n_keys < 0 || n_keys > c->n_blocks * c->block_rows)
+        return skv::fail(h, SKV_EINVAL, "n_keys %lld outside the cache", (long long)n_keys);
+    if (n_keys == 0) return SKV_OK;
+    const int64_t last = (n_keys - 1) / c->block_rows;
+    const int64_t first = std::max<int64_t>(0, last - c->ring_blocks + 1);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    ring_restore_kernel<<<1, 256, 0, st>>>(first, static_cast<int>(last - first + 1), c->Hk, c->ring_blocks,
+                                          c->miss_page, c->miss_dest, c->slot_page, c->ctl);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return skv::cuda_fail(h, e, "ring restore launch");
+    bcache_fetch_kernel<<<2 * h->sm_count, 256, 0, st>>>(c->ctl, c->miss_page, c->miss_dest, c->host_k, c->host_v,
+                                                         c->pool_k, c->pool_v, c->page_bytes);
+    return skv::cuda_fail(h, cudaGetLastError(), "ring fetch launch");
+}
+
+extern "C" int skv_bcache_ring_attn(skv_bcache *c, const skv_shape *shape, const void *q, int64_t n_keys,
+                                    int64_t window, float *o, float *lse, void *stream)
+{
+    if (!c || !shape) return SKV_EINVAL;
+    skv_handle *h = c->h;
+    h->err[0] = 0;
+    if (c->ring_blocks <= 0) return skv::fail(h, SKV_EINVAL, "not a ring cache");
+    if (shape->Hk != c->Hk || shape->D != c->D)
+        return skv::fail(h, SKV_EINVAL, "shape (Hk=%d, D=%d) does not match the cache (Hk=%d, D=%d)", shape->Hk,
+                         shape->D, c->Hk, c->D);
+    if (n_keys < 0 || n_keys > c->n_blocks * c->block_rows)
+        return skv::fail(h, SKV_EINVAL, "n_keys %lld outside the cache", (long long)n_keys);
+    const int64_t br = c->block_rows;
+    const int64_t last = n_keys > 0 ? (n_keys - 1) / br : 0;
+    const int64_t ring_first = std::max<int64_t>(0, last - c->ring_blocks + 1) * br;   // oldest cell in the ring
+    const int64_t lo = window > 0 ? std::max<int64_t>(0, n_keys - window) : ring_first;
+    if (lo < ring_first)
+        return skv::fail(h, SKV_EINVAL, "window of %lld cells reaches past the ring (oldest cell %lld)",
+                         (long long)window, (long long)ring_first);
+    const int64_t first_blk = lo / br;
+    const int n_blk = n_keys > lo ? static_cast<int>(last - first_blk + 1) : 0;
+    if (static_cast<int64_t>(shape->S) * c->Hk * std::max(n_blk, 1) > c->max_lookups)
+        return skv::fail(h, SKV_EINVAL, "%d sequences exceed the ring's page-list capacity", shape->S);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (n_blk > 0) {
+        ring_ids_kernel<<<64, 256, 0, st>>>(first_blk, n_blk, shape->S, c->Hk, c->ring_blocks, c->page_ids);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return skv::cuda_fail(h, e, "ring page-list launch");
+    }
+    return skv::attn_paged_range(h, shape, q, c->pool_k, c->pool_v, c->block_rows, c->page_ids, std::max(n_blk, 1),
+                                 lo - first_blk * br, n_keys - first_blk * br, o, lse, st);
 }

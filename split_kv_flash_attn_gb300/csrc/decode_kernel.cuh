@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(128) splitkv_decode_kernel(const DecodeArgs a)
     const int split = blockIdx.y;
     const int s = blockIdx.z;
     const int unit = (s * a.Hk + kh) * a.n_cg + cg;
-    const int64_t j_lo = static_cast<int64_t>(split) * a.split_len;
+    const int64_t j_lo = a.key_lo + static_cast<int64_t>(split) * a.split_len;
     const int64_t j_hi = min(a.n_local, j_lo + a.split_len);
     const int64_t list = a.rows_per_head ? (static_cast<int64_t>(s) * a.Hk + kh) : s;
     const int lg_pr = a.row_mode == ROWS_PAGED ? (31 - __clz(a.page_rows)) : 0;

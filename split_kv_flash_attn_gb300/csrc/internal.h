@@ -67,7 +67,8 @@ struct DecodeArgs {
     const int32_t *q_pos;       // [S][nq] or null
     int64_t key_pos0;           // causal position of logical key 0
     int64_t logical0;           // logical index of local key 0
-    int64_t n_local;            // local keys of this launch
+    int64_t n_local;            // local keys of this launch are [key_lo, n_local)
+    int64_t key_lo;             // first local key; splits start here (0 unless a range starts mid-page)
     int S, nq, H, Hk, G;
     float scale_log2;           // scale * log2(e)
     int n_cg;                   // column groups (8 query columns each) per (s, k)
@@ -132,6 +133,12 @@ constexpr int kPrefillOverheadTiles = 6;
 
 int plan_splits_cost(int64_t n_keys, int64_t n_units, int sm_count, int ctas_per_sm, int tile, int64_t max_split,
                      int overhead_tiles, int64_t *split_len, int32_t *n_splits);
+
+// Paged attention over local keys [key_lo, key_hi) of page lists of
+// pages_per_list pages (skv_attn_paged is the whole range).
+int attn_paged_range(skv_handle *h, const skv_shape *shape, const void *q, const void *k_pages, const void *v_pages,
+                     int32_t page_rows, const int32_t *page_ids, int32_t pages_per_list, int64_t key_lo,
+                     int64_t key_hi, float *o, float *lse, cudaStream_t st);
 
 int launch_dequant(int type, const void *blocks, int64_t n_values, float *out, cudaStream_t st);
 int launch_gather(const void *src, int64_t row_bytes, const int32_t *rows, int64_t n, void *dst,
