@@ -427,6 +427,10 @@ def run_extras(torch, skv, wl, h, hbm_peak):
     except Exception as exc:  # noqa: BLE001
         out["block_sparse_error"] = repr(exc)[:300]
     try:
+        out["prefill_variants"] = bench_prefill_variants(torch, skv, wl, h)
+    except Exception as exc:  # noqa: BLE001
+        out["prefill_variants_error"] = repr(exc)[:300]
+    try:
         out["kv_append"] = bench_append(torch, skv, wl, h, hbm_peak)
     except Exception as exc:  # noqa: BLE001
         out["kv_append_error"] = repr(exc)[:300]
@@ -529,6 +533,66 @@ def bench_prefill(torch, skv, wl, h):
             "peak_kind": f"{kind} bf16 dense (fp16 runs at the same tensor rate)",
             "call_ms_window_tail": call_ms, "call_TFLOPs": total_flop / call_ms / 1e9, "flop": total_flop,
             "tail_bytes": tail_bytes, "tail_GBps_if_copy_bound": tail_bytes / call_ms / 1e6}
+
+
+def bench_prefill_variants(torch, skv, wl, h):
+    """Tensor-core prefill with software producers: (a) 512 causal tokens x 32
+    heads over a 32768-row q8_0-K / q4_0-V window (keys split exactly into two
+    fp16 operands, so QK^T takes twice the MMAs); (b) 8 sequences x 64 tokens
+    x 32 heads, each over its own 32768 rows of the 1 GiB unified fp16 cache
+    through a row list.  FLOP counted as 4*D per (query row, visible key)."""
+    _, bf16_peak, _ = peaks()
+    out = {}
+    s = torch.cuda.current_stream()
+    b, a = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def kernel_ms(fn, n=5):
+        fn()
+        torch.cuda.synchronize()
+        b.record(s)
+        a.record(s)
+        h.set_profile_events(b, a)
+        ks = []
+        for _ in range(n):
+            fn()
+            torch.cuda.synchronize()
+            ks.append(b.elapsed_time(a))
+        h.set_profile_events(None, None)
+        return statistics.median(ks)
+
+    rng = wl.generator(4, salt=77)
+    nq, H, Hk, D, n = 512, 32, 8, 128, 32768
+    q = torch.from_numpy(wl.normal_f16(rng, (1, nq, H, D))).cuda()
+    K = torch.from_numpy(wl.cache_rows(rng, wl.Q8_0, n, Hk, D)).cuda()
+    V = torch.from_numpy(wl.cache_rows(rng, wl.Q4_0, n, Hk, D)).cuda()
+    qp = torch.arange(n - nq, n, dtype=torch.int32, device="cuda").reshape(1, nq)
+    o = torch.empty((1, nq, H, D), dtype=torch.float32, device="cuda")
+    lse = torch.empty((1, nq, H), dtype=torch.float32, device="cuda")
+    ms = kernel_ms(lambda: skv.attn_partial(h, q, K, V, Hk=Hk, k_type=wl.Q8_0, v_type=wl.Q4_0, q_pos=qp, o=o,
+                                            lse=lse))
+    pairs = float(np.arange(n - nq, n, dtype=np.int64).sum() + nq)
+    flop = 4.0 * D * H * pairs
+    out["quant_window_q8k_q4v"] = {"rows": n, "nq": nq, "kernel_ms": ms, "TFLOPs": flop / ms / 1e9,
+                                   "frac_of_bf16_peak": flop / ms / 1e9 / bf16_peak,
+                                   "bytes": K.numel() + V.numel()}
+    del K, V
+    w = wl.unified_decode()
+    S, nq2 = w.S, 64
+    q2 = torch.from_numpy(wl.normal_f16(rng, (S, nq2, w.H, w.D))).cuda()
+    kc, vc = torch.from_numpy(w.k).cuda(), torch.from_numpy(w.v).cuda()
+    rows = torch.from_numpy(w.kv_rows).cuda()
+    n_list = w.kv_rows.shape[1]
+    qp2 = (torch.arange(nq2, dtype=torch.int32, device="cuda") + (n_list - nq2)).repeat(S, 1).contiguous()
+    o2 = torch.empty((S, nq2, w.H, w.D), dtype=torch.float32, device="cuda")
+    l2 = torch.empty((S, nq2, w.H), dtype=torch.float32, device="cuda")
+    ms = kernel_ms(lambda: skv.attn_partial(h, q2, kc, vc, Hk=w.Hk, kv_rows=rows, q_pos=qp2, o=o2, lse=l2))
+    pairs = S * float(np.arange(n_list - nq2, n_list, dtype=np.int64).sum() + nq2)
+    flop = 4.0 * w.D * w.H * pairs
+    out["row_list_unified_cache"] = {"S": S, "nq": nq2, "rows_per_seq": n_list, "kernel_ms": ms,
+                                     "TFLOPs": flop / ms / 1e9, "frac_of_bf16_peak": flop / ms / 1e9 / bf16_peak,
+                                     "gathered_GBps": S * n_list * w.Hk * w.D * 4 / ms / 1e6}
+    h.status()
+    return out
 
 
 def bench_append(torch, skv, wl, h, hbm_peak):

@@ -387,8 +387,9 @@ int skv_attn_partial(skv_handle *h, const skv_shape *shape, const void *q, const
         rc = launch_combine(0, nullptr, nullptr, R, D, o, lse, st);
         return rc == SKV_OK ? rc : cuda_fail(h, cudaGetLastError(), "fill launch");
     }
-    if (!kv_rows && prefill_eligible(shape, mask)) {
-        // Many query rows per KV head over a dense range: the tensor-core path.
+    if (prefill_eligible(shape, mask)) {
+        // Many query rows per KV head: the tensor-core path (dense fp16 ranges
+        // by TMA; row lists and quantised rows by its software producers).
         const int64_t units_p = static_cast<int64_t>(shape->S) * prefill_units(shape);
         int64_t split_len = 0;
         int32_t n_splits = 0;
@@ -403,9 +404,13 @@ int skv_attn_partial(skv_handle *h, const skv_shape *shape, const void *q, const
         L.k = k;
         L.v = v;
         L.n_rows = kv_end;
-        L.row0 = kv_begin;
+        L.row0 = kv_rows ? 0 : kv_begin;
         L.n_local = n_local;
         L.logical0 = kv_begin;
+        L.rows = kv_rows;
+        L.rows_ld = kv_rows_ld;
+        L.rows_off = kv_begin;
+        L.rows_per_head = kv_rows_per_head ? 1 : 0;
         L.q_pos = q_pos;
         L.key_pos0 = key_pos0;
         L.n_splits = n_splits;

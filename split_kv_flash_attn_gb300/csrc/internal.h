@@ -122,6 +122,10 @@ struct PrefillLaunch {
     float *lse_split;
     float *o_out;
     float *lse_out;
+    const int32_t *rows;        // row lists (entry rows_off = local key 0), or null for a dense range
+    int64_t rows_ld;
+    int64_t rows_off;
+    int rows_per_head;
 };
 bool prefill_eligible(const skv_shape *sh, const void *mask);
 int prefill_units(const skv_shape *sh);    // (KV head, 128-row query tile) pairs per sequence

@@ -1,0 +1,682 @@
+// prefill_kernel.cuh -- prefill-chunk attention on the 5th-generation tensor
+// cores (template; instantiated in prefill.cu and prefill_sw.cu).
+//
+// The only place in the path where the work is a dense contraction: nq new
+// tokens x G heads of one KV head against a range of keys.  One CTA owns a
+// 128-row query tile (128/G tokens x G heads of KV head k, the GQA packing) and
+// one split of the key range, and walks it in 128-key tiles:
+//
+//   producer      : K_j, V_j tiles (128 keys x 128 d, fp16, 128-byte swizzle)
+//                   into a 2-deep K ring and a 2-deep V ring.  MODE 0: one
+//                   thread issues TMA loads over a dense fp16 region.  MODE 1:
+//                   two warps, two key rows per thread, fetch the rows through
+//                   a row list (padding entries read nothing) or a dense range;
+//                   fp16 rows go straight to the swizzled tile by cp.async,
+//                   q8_0 / q4_0 rows are loaded, decoded to fp16(d*q) and
+//                   stored in the same layout.
+//   MMA warp      : S_j = Q K_j^T        tcgen05.mma kind::f16, M=N=128, into
+//                                        one of two TMEM S buffers (fp32);
+//                   O  += P_j V_j        into the TMEM O accumulator; V is the
+//                                        B operand in MN-major layout.
+//   softmax (0-7) : two threads per query row (TMEM lane), 64 key columns
+//                   each: tcgen05.ld S_j, causal / padding mask, online
+//                   softmax in log2 units, P_j (fp16) to shared memory.  O is
+//                   rescaled in TMEM only when a row maximum grows by more than
+//                   2^8 (the stale maximum stays the reference otherwise,
+//                   exactly as in the plain online softmax with another shift).
+//
+// The per-split result (O normalised, lse) is merged across splits by the
+// last CTA of each (sequence, KV head, query tile), as in the decode kernel.
+// Every mbarrier wait is bounded; a wait that gives up sets the handle's
+// device status word and the CTA stops issuing work, drains what it issued
+// and frees its TMEM.
+#pragma once
+
+#include <string.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "tc.cuh"
+
+namespace skv {
+namespace pf {
+
+constexpr int kPM = 128;        // query rows per tile (TMEM lanes)
+constexpr int kPN = 128;        // keys per tile
+constexpr int kPD = 128;        // head dim
+constexpr int kSoftmaxWarps = 8;   // two warps per query-row group (one per column half)
+constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
+constexpr int kTileBytes = kPN * kPD * 2;       // 32 KiB per K or V tile
+constexpr int kHalfTile = kTileBytes / 2;       // one 64-column swizzle block
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + kTileBytes;       // 2 stages (quantised keys: hi and lo of one stage)
+constexpr int kOffV = kOffK + 2 * kTileBytes;   // 2 stages
+constexpr int kOffP = kOffV + 2 * kTileBytes;
+constexpr int kOffBar = kOffP + kTileBytes;
+constexpr int kSmem = kOffBar + 256 + 1024;     // + barriers + alignment slack
+constexpr uint32_t kIdescS = tc::idesc_f16(kPM, kPN, false);
+constexpr uint32_t kIdescPV = tc::idesc_f16(kPM, kPD, true);
+constexpr float kRescaleLog2 = 8.0f;            // rescale O only when the max grows by > 2^8
+
+// Producer warps and thread count per mode (MODE 0: TMA, MODE 1: software).
+template <int MODE>
+struct Cfg {
+    // 11 warps: at most 3 per SM sub-partition, so the softmax warps keep up
+    // to 168 registers (13 warps would cap them at 128)
+    static constexpr int kProducerWarps = MODE == 0 ? 1 : 2;
+    static constexpr int kMmaWarp = kSoftmaxWarps + kProducerWarps;
+    static constexpr int kThreads = (kMmaWarp + 1) * 32;
+    static constexpr uint32_t kFullCount = MODE == 0 ? 1 : kProducerWarps * 32;
+};
+
+// barrier slots (8 bytes each) inside the barrier area
+enum { B_KFULL = 0, B_KEMPTY = 2, B_VFULL = 4, B_VEMPTY = 6, B_QFULL = 8, B_SFULL = 9, B_SFREE = 11, B_PFULL = 13,
+       B_PVDONE = 14, B_COUNT = 15 };
+
+struct PrefillArgs {
+    const __half *q;          // [S][nq][H][D]
+    int S, nq, H, Hk, G;
+    float scale_log2;
+    const int32_t *q_pos;     // [S][nq] or null
+    int64_t key_pos0;
+    int64_t logical0;
+    int64_t row0;             // row of local key 0 (dense ranges)
+    int64_t n_local;
+    int m_tiles;
+    int n_splits;
+    int64_t split_len;
+    float *o_split;
+    float *lse_split;
+    int *counters;
+    float *o_out;
+    float *lse_out;
+    int64_t R;
+    int *status;
+    // software producers
+    const uint8_t *k;         // region bases
+    const uint8_t *v;
+    int64_t k_row_bytes;
+    int64_t v_row_bytes;
+    const int32_t *rows;      // row lists or null (dense)
+    int64_t rows_ld;
+    int64_t rows_off;         // list entry of local key 0
+    int rows_per_head;
+};
+
+// Byte offset of 16-byte chunk c (values 8c .. 8c+7) of key row r in a
+// 128-key x 128-value fp16 tile with the 128-byte swizzle (the layout a TMA
+// load of two 64-value boxes writes).
+__device__ __forceinline__ uint32_t tile_off(int r, int c)
+{
+    return static_cast<uint32_t>((c >> 3) * kHalfTile + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+// Two code bytes of a word (byte pair at bit 16*hi) -> half2(1024 + b0, 1024 + b1).
+template <int HI>
+__device__ __forceinline__ __half2 code_pair(uint32_t w)
+{
+    const uint32_t h = __byte_perm(w, 0x64646464u, HI ? 0x4342 : 0x4140);
+    return *reinterpret_cast<const __half2 *>(&h);
+}
+
+// One key row of a tile from a row segment (nullptr: a padding key, zeros).
+// T = SKV_F16: sixteen 16-byte cp.async (the caller commits and waits).
+// q8_0 / q4_0: the segment's bytes are loaded with 8-byte loads and every
+// value d*q is written as fp16, 16 swizzled 16-byte chunks per row.  With
+// LO (keys), the value is split exactly into hi = fp16(d*q) in `tile` and
+// lo = fp16(d*q - hi) in `tile_lo` (one fused multiply-add: d*q has at most
+// 18 significant bits, so hi + lo is d*q whenever lo is a normal fp16);
+// without LO (values) only fp16(d*q) is written, rounded once.
+template <int T, bool LO = false>
+__device__ __forceinline__ void produce_row(const uint8_t *seg, const uint8_t *any_valid, uint8_t *tile,
+                                            uint32_t tile_s, int r, uint8_t *tile_lo = nullptr)
+{
+    if constexpr (T == SKV_F16) {
+        // a padding row copies nothing (source size 0 zero-fills) from a
+        // valid address
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+            cp_async16(tile_s + tile_off(r, c), seg ? seg + 16 * c : any_valid, seg ? 16 : 0);
+    } else {
+        constexpr int SEG = T == SKV_Q8_0 ? 136 : 72;   // 4 blocks of 34 or 18 bytes
+        constexpr int NW = SEG / 4;
+        if (!seg) {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                *reinterpret_cast<uint4 *>(tile + tile_off(r, c)) = make_uint4(0, 0, 0, 0);
+                if (LO) *reinterpret_cast<uint4 *>(tile_lo + tile_off(r, c)) = make_uint4(0, 0, 0, 0);
+            }
+            return;
+        }
+        uint32_t w[NW];
+#pragma unroll
+        for (int i = 0; i < NW / 2; ++i) {
+            const uint2 x = __ldg(reinterpret_cast<const uint2 *>(seg) + i);
+            w[2 * i] = x.x;
+            w[2 * i + 1] = x.y;
+        }
+        // a byte pair at even offset o lives in word o/4, half (o/2)&1
+#define SKV_PAIR_WORD(o) w[(o) >> 2]
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            constexpr int BLK = SEG / 4;
+            const int o_d = b * BLK;
+            const uint32_t dw = SKV_PAIR_WORD(o_d);
+            const __half d = __ushort_as_half(static_cast<unsigned short>((o_d & 2) ? (dw >> 16) : (dw & 0xffff)));
+            const __half2 dd = __half2half2(d);
+            if constexpr (T == SKV_Q8_0) {
+                const __half2 bias = __half2half2(__ushort_as_half(0x6480));   // 1152 = 1024 + 128
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {            // values 8c .. 8c+7 of the block
+                    uint32_t out[4], out_lo[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int o = o_d + 2 + 8 * c + 2 * i;
+                        const uint32_t x = SKV_PAIR_WORD(o) ^ 0x80808080u;   // int8 q -> byte q + 128
+                        const __half2 qv = __hsub2((o & 2) ? code_pair<1>(x) : code_pair<0>(x), bias);
+                        const __half2 val = __hmul2(qv, dd);
+                        out[i] = *reinterpret_cast<const uint32_t *>(&val);
+                        if (LO) {
+                            const __half2 lo = __hfma2(qv, dd, __hneg2(val));
+                            out_lo[i] = *reinterpret_cast<const uint32_t *>(&lo);
+                        }
+                    }
+                    *reinterpret_cast<uint4 *>(tile + tile_off(r, 4 * b + c)) = make_uint4(out[0], out[1], out[2], out[3]);
+                    if (LO)
+                        *reinterpret_cast<uint4 *>(tile_lo + tile_off(r, 4 * b + c)) =
+                            make_uint4(out_lo[0], out_lo[1], out_lo[2], out_lo[3]);
+                }
+            } else {
+                const __half2 bias = __half2half2(__ushort_as_half(0x6408));   // 1032 = 1024 + 8
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {            // c 0,1: low nibbles of bytes 0-7, 8-15; c 2,3: high
+                    uint32_t out[4], out_lo[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int o = o_d + 2 + 8 * (c & 1) + 2 * i;
+                        const uint32_t raw = SKV_PAIR_WORD(o);
+                        const uint32_t x = (c & 2) ? ((raw >> 4) & 0x0F0F0F0Fu) : (raw & 0x0F0F0F0Fu);
+                        const __half2 qv = __hsub2((o & 2) ? code_pair<1>(x) : code_pair<0>(x), bias);
+                        const __half2 val = __hmul2(qv, dd);
+                        out[i] = *reinterpret_cast<const uint32_t *>(&val);
+                        if (LO) {
+                            const __half2 lo = __hfma2(qv, dd, __hneg2(val));
+                            out_lo[i] = *reinterpret_cast<const uint32_t *>(&lo);
+                        }
+                    }
+                    *reinterpret_cast<uint4 *>(tile + tile_off(r, 4 * b + c)) = make_uint4(out[0], out[1], out[2], out[3]);
+                    if (LO)
+                        *reinterpret_cast<uint4 *>(tile_lo + tile_off(r, 4 * b + c)) =
+                            make_uint4(out_lo[0], out_lo[1], out_lo[2], out_lo[3]);
+                }
+            }
+        }
+#undef SKV_PAIR_WORD
+    }
+}
+
+template <int MODE, int KT, int VT>
+__global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
+    splitkv_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                           const PrefillArgs a)
+{
+    using C = Cfg<MODE>;
+    // Quantised keys: one K stage holding the (hi, lo) pair of fp16 tiles in
+    // the two K slots, and S = Q hi^T + Q lo^T (16 k-steps), so that scores
+    // use the exact key values; fp16 keys: a 2-deep K ring.
+    constexpr bool KLO = KT != SKV_F16;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_addr(sm);
+    const uint32_t bar0 = sbase + kOffBar;
+    auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+    __shared__ int s_maxpos;
+    __shared__ int s_last;
+    // [slot][column half][row]: partial row maxima by tile parity (slots 0, 1),
+    // then the halves' row sums (slot 2, so that no partner read is pending)
+    __shared__ float s_pair[3][2][kPM];
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int mt = blockIdx.x % a.m_tiles;
+    const int kh = blockIdx.x / a.m_tiles;
+    const int split = blockIdx.y;
+    const int s = blockIdx.z;
+    const int unit = (s * a.Hk + kh) * a.m_tiles + mt;
+    const int tpt = kPM / a.G;                       // tokens per query tile
+    const int64_t list = a.rows_per_head ? static_cast<int64_t>(s) * a.Hk + kh : s;
+    const int32_t *lrow = a.rows ? a.rows + list * a.rows_ld + a.rows_off : nullptr;   // entry of local key 0
+
+    const int64_t j_lo = static_cast<int64_t>(split) * a.split_len;
+    const int64_t j_hi = min(a.n_local, j_lo + a.split_len);
+
+    // Softmax threads: query row m = TMEM lane (warp % 4) * 32 + lane, and the
+    // column half hf (key columns hf*64 .. hf*64+63 of each 128-key tile).
+    const bool softmax = warp < kSoftmaxWarps;
+    const int m = (warp & 3) * 32 + lane;
+    const int hf = warp >> 2;
+    const int t_row = mt * tpt + m / a.G;
+    const bool row_ok = softmax && t_row < a.nq;
+    const int32_t pos_row = (row_ok && a.q_pos) ? a.q_pos[static_cast<int64_t>(s) * a.nq + t_row] : INT32_MAX;
+
+    if (tid == 0) {
+        s_abort = 0;
+        s_maxpos = INT32_MIN;
+    }
+    __syncthreads();
+    if (a.q_pos && row_ok && hf == 0) atomicMax(&s_maxpos, pos_row);
+    if (warp == 0) {
+        tc::tmem_alloc<512>(smem_addr(&s_tmem));
+        tc::tmem_relinquish();
+    }
+    if (tid == kSoftmaxThreads) {
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(bar(B_KFULL + i), C::kFullCount);
+            tc::mbar_init(bar(B_KEMPTY + i), 1);
+            tc::mbar_init(bar(B_VFULL + i), C::kFullCount);
+            tc::mbar_init(bar(B_VEMPTY + i), 1);
+            tc::mbar_init(bar(B_SFULL + i), 1);
+            tc::mbar_init(bar(B_SFREE + i), kSoftmaxThreads);
+        }
+        tc::mbar_init(bar(B_QFULL), kSoftmaxThreads);
+        tc::mbar_init(bar(B_PFULL), kSoftmaxThreads);
+        tc::mbar_init(bar(B_PVDONE), 1);
+        tc::fence_barrier_init();
+        if (MODE == 0) {
+            tc::prefetch_tmap(&tmap_k);
+            tc::prefetch_tmap(&tmap_v);
+        }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = s_tmem;
+
+    // Keys past the largest query position of the tile are invisible to all
+    // its rows: the tile walk stops there.
+    int64_t j_end = j_hi;
+    if (a.q_pos) {
+        const int64_t last_visible = static_cast<int64_t>(s_maxpos) - a.key_pos0 - a.logical0;   // local index
+        j_end = min(j_end, last_visible + 1);
+    }
+    const int n_tiles = j_end > j_lo ? static_cast<int>((j_end - j_lo + kPN - 1) / kPN) : 0;
+
+    auto fail_wait = [&]() {
+        s_abort = 1;
+        if (a.status) atomicOr(a.status, 1);
+    };
+    auto wait = [&](int b, uint32_t parity) -> bool {
+        if (*reinterpret_cast<volatile int *>(&s_abort)) return false;
+        if (tc::mbar_wait(bar(b), parity, a.status)) return true;
+        fail_wait();
+        return false;
+    };
+    // The two warps that share rows (w and w + 4) meet on named barrier 1 + w%4.
+    auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;\n" ::"r"(1 + (warp & 3)) : "memory"); };
+
+    float m_ref = -INFINITY, l_run = 0.f;
+
+    if (warp >= kSoftmaxWarps && warp < C::kMmaWarp) {
+        if constexpr (MODE == 0) {
+            // ---------------- TMA producer --------------------------------
+            if (lane == 0) {
+                int k_issued = 0, v_issued = 0;
+                for (int j = 0; j < n_tiles; ++j) {
+                    const int b = j & 1;
+                    const int y = static_cast<int>(a.row0 + j_lo + static_cast<int64_t>(j) * kPN);
+                    const int x = kh * kPD;
+                    if (j >= 2 && !wait(B_KEMPTY + b, ((j >> 1) - 1) & 1)) break;
+                    tc::mbar_expect_tx(bar(B_KFULL + b), kTileBytes);
+                    tc::tma_load_2d(sbase + kOffK + b * kTileBytes, &tmap_k, x, y, bar(B_KFULL + b));
+                    tc::tma_load_2d(sbase + kOffK + b * kTileBytes + kHalfTile, &tmap_k, x + 64, y, bar(B_KFULL + b));
+                    ++k_issued;
+                    if (j >= 2 && !wait(B_VEMPTY + b, ((j >> 1) - 1) & 1)) break;
+                    tc::mbar_expect_tx(bar(B_VFULL + b), kTileBytes);
+                    tc::tma_load_2d(sbase + kOffV + b * kTileBytes, &tmap_v, x, y, bar(B_VFULL + b));
+                    tc::tma_load_2d(sbase + kOffV + b * kTileBytes + kHalfTile, &tmap_v, x + 64, y, bar(B_VFULL + b));
+                    ++v_issued;
+                }
+                if (*reinterpret_cast<volatile int *>(&s_abort)) {
+                    // drain: every issued load must land before the CTA exits
+                    for (int j = (k_issued > 2 ? k_issued - 2 : 0); j < k_issued; ++j)
+                        tc::mbar_wait(bar(B_KFULL + (j & 1)), (j >> 1) & 1, nullptr, 100000000ull);
+                    for (int j = (v_issued > 2 ? v_issued - 2 : 0); j < v_issued; ++j)
+                        tc::mbar_wait(bar(B_VFULL + (j & 1)), (j >> 1) & 1, nullptr, 100000000ull);
+                }
+            }
+        } else {
+            // ---------------- software producers: each thread two key rows ------
+            // K_j is published (KFULL) only after V_j's stage was found free, so
+            // the wait order is KEMPTY, VEMPTY; VEMPTY(j) needs PV(j-2), which the
+            // MMA warp issues before it needs K_j: no cycle.
+            constexpr int NPT = C::kProducerWarps * 32;      // producer threads
+            constexpr int RPT = kPN / NPT;                   // rows per thread
+            const int r0 = tid - kSoftmaxThreads;
+            constexpr int SEGK = KT == SKV_F16 ? 256 : (KT == SKV_Q8_0 ? 136 : 72);
+            constexpr int SEGV = VT == SKV_F16 ? 256 : (VT == SKV_Q8_0 ? 136 : 72);
+            for (int j = 0; j < n_tiles; ++j) {
+                const int b = j & 1;
+                const uint8_t *sk[RPT], *sv[RPT];
+#pragma unroll
+                for (int u = 0; u < RPT; ++u) {
+                    const int64_t key = j_lo + static_cast<int64_t>(j) * kPN + r0 + u * NPT;
+                    int64_t row = -1;
+                    if (key < j_hi) row = lrow ? static_cast<int64_t>(__ldg(lrow + key)) : a.row0 + key;
+                    sk[u] = row >= 0 ? a.k + row * a.k_row_bytes + static_cast<int64_t>(kh) * SEGK : nullptr;
+                    sv[u] = row >= 0 ? a.v + row * a.v_row_bytes + static_cast<int64_t>(kh) * SEGV : nullptr;
+                }
+                const int kb = KLO ? 0 : b;                      // K stage of this tile
+                if (KLO ? (j >= 1 && !wait(B_KEMPTY, (j - 1) & 1)) : (j >= 2 && !wait(B_KEMPTY + b, ((j >> 1) - 1) & 1)))
+                    break;
+#pragma unroll
+                for (int u = 0; u < RPT; ++u)
+                    produce_row<KT, KLO>(sk[u], a.k, sm + kOffK + kb * kTileBytes, sbase + kOffK + kb * kTileBytes,
+                                         r0 + u * NPT, sm + kOffK + kTileBytes);
+                cp_async_commit();
+                if (j >= 2 && !wait(B_VEMPTY + b, ((j >> 1) - 1) & 1)) break;
+#pragma unroll
+                for (int u = 0; u < RPT; ++u)
+                    produce_row<VT>(sv[u], a.v, sm + kOffV + b * kTileBytes, sbase + kOffV + b * kTileBytes,
+                                    r0 + u * NPT);
+                cp_async_commit();
+                cp_async_wait<1>();
+                tc::fence_proxy_async_smem();
+                tc::mbar_arrive(bar(B_KFULL + kb));
+                cp_async_wait<0>();
+                tc::fence_proxy_async_smem();
+                tc::mbar_arrive(bar(B_VFULL + b));
+            }
+            cp_async_wait<0>();
+        }
+    } else if (warp == C::kMmaWarp) {
+        // ---------------- MMA issuer ----------------------------------------
+        if (lane == 0 && n_tiles > 0) {
+            bool ok = wait(B_QFULL, 0);
+            tc::tc_fence_after();
+            int committed_pv = 0;
+            for (int jj = 0; ok && jj <= n_tiles; ++jj) {
+                if (jj < n_tiles) {
+                    const int b = jj & 1;
+                    const int kb = KLO ? 0 : b;
+                    if (!wait(B_KFULL + kb, KLO ? (jj & 1) : ((jj >> 1) & 1))) break;
+                    if (jj >= 2 && !wait(B_SFREE + b, ((jj >> 1) - 1) & 1)) break;
+                    tc::tc_fence_after();
+                    const uint32_t d_s = tmem + static_cast<uint32_t>(b * kPN);
+                    constexpr int KSTEPS = (KLO ? 2 : 1) * kPD / 16;   // hi then lo
+#pragma unroll
+                    for (int ks = 0; ks < KSTEPS; ++ks) {
+                        const int kk = ks % (kPD / 16);
+                        const uint32_t off = (kk >> 2) * kHalfTile + (kk & 3) * 32;
+                        const uint64_t ad = tc::smem_desc(sbase + kOffQ + off, 16, 1024);
+                        const uint64_t bd = tc::smem_desc(
+                            sbase + kOffK + (KLO ? (ks / (kPD / 16)) : b) * kTileBytes + off, 16, 1024);
+                        tc::mma_f16(d_s, ad, bd, kIdescS, ks > 0);
+                    }
+                    tc::mma_commit(bar(B_SFULL + b));
+                    tc::mma_commit(bar(B_KEMPTY + kb));
+                }
+                if (jj >= 1) {
+                    const int j = jj - 1;
+                    const int b = j & 1;
+                    if (!wait(B_PFULL, j & 1)) break;
+                    if (!wait(B_VFULL + b, (j >> 1) & 1)) break;
+                    tc::tc_fence_after();
+                    const uint32_t d_o = tmem + 2 * kPN;
+#pragma unroll
+                    for (int kk = 0; kk < kPN / 16; ++kk) {
+                        const uint32_t poff = (kk >> 2) * kHalfTile + (kk & 3) * 32;
+                        const uint64_t ad = tc::smem_desc(sbase + kOffP + poff, 16, 1024);
+                        // V tile as B in MN-major layout: 16 keys = 2048 bytes per k-step;
+                        // the second 64-wide d block is kHalfTile away (leading offset),
+                        // 8-key row groups are 1024 bytes apart (stride offset).
+                        const uint64_t bd = tc::smem_desc(sbase + kOffV + b * kTileBytes + kk * 2048, kHalfTile, 1024);
+                        tc::mma_f16(d_o, ad, bd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc::mma_commit(bar(B_PVDONE));
+                    tc::mma_commit(bar(B_VEMPTY + b));
+                    ++committed_pv;
+                }
+            }
+            if (*reinterpret_cast<volatile int *>(&s_abort) && committed_pv > 0)
+                tc::mbar_wait(bar(B_PVDONE), (committed_pv - 1) & 1, nullptr, 100000000ull);   // drain issued MMAs
+        }
+    } else {
+        // ---------------- softmax warps (two threads per query row) -----------
+        // Q: this thread's half of its row -> the 128-byte-swizzled K-major layout.
+        {
+            const __half *qp = a.q + ((static_cast<int64_t>(s) * a.nq + (row_ok ? t_row : 0)) * a.H + kh * a.G +
+                                      (m % a.G)) * kPD + hf * 64;
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) {
+                uint4 v = row_ok ? *reinterpret_cast<const uint4 *>(qp + cc * 8) : make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4 *>(sm + kOffQ + hf * kHalfTile + m * 128 + ((cc ^ (m & 7)) << 4)) = v;
+            }
+            tc::fence_proxy_async_smem();
+            tc::mbar_arrive(bar(B_QFULL));
+        }
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        constexpr int NC = kPN / 2;                 // columns per thread
+        // No early exit from this loop: the two warps of a row pair meet on a
+        // named barrier every tile, so both must run every iteration.  After
+        // a wait gives up, every later wait returns at once and the CTA runs
+        // through to its exit (its outputs are then invalid and the status
+        // word says so).
+        for (int j = 0; j < n_tiles; ++j) {
+            const int b = j & 1;
+            const int64_t key0 = j_lo + static_cast<int64_t>(j) * kPN + hf * NC;   // local index of column 0
+            // Padding entries of a row list: one bit per column of this half
+            // (entries past the split count as present; lim_end masks them).
+            uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+            if (lrow) {
+                const int64_t ka = key0 + lane, kb = key0 + 32 + lane;
+                vm0 = __ballot_sync(0xffffffffu, ka >= j_hi || __ldg(lrow + ka) >= 0);
+                vm1 = __ballot_sync(0xffffffffu, kb >= j_hi || __ldg(lrow + kb) >= 0);
+            }
+            __all_sync(0xffffffffu, wait(B_SFULL + b, (j >> 1) & 1));
+            tc::tc_fence_after();
+            uint32_t sr[NC / 32][32];
+#pragma unroll
+            for (int c = 0; c < NC / 32; ++c) tc::tmem_ld32(lane_base + b * kPN + hf * NC + c * 32, sr[c]);
+#pragma unroll
+            for (int c = 0; c < NC / 32; ++c) tc::tmem_wait_ld(sr[c]);
+            float x[NC];
+#pragma unroll
+            for (int c = 0; c < NC / 32; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(sr[c][i]);
+            tc::tc_fence_before();
+            tc::mbar_arrive(bar(B_SFREE + b));
+
+            const int64_t pos0 = a.key_pos0 + a.logical0 + key0;
+            const int64_t lim_pos = static_cast<int64_t>(pos_row) - pos0;   // columns > lim_pos are masked
+            const int64_t lim_end = j_hi - key0;                            // columns >= lim_end are outside the split
+            // Masking only where a tile reaches past a row's position or the
+            // split's end, or holds padding (warp-uniform test; most tiles
+            // skip it).
+            if (__any_sync(0xffffffffu, lim_pos < NC - 1 || lim_end < NC || (vm0 & vm1) != 0xffffffffu)) {
+#pragma unroll
+                for (int i = 0; i < NC; ++i) {
+                    const bool present = ((i < 32 ? vm0 : vm1) >> (i & 31)) & 1u;
+                    if (i > lim_pos || i >= lim_end || !present) x[i] = -INFINITY;
+                }
+            }
+            // Row maximum on the raw scores (the scale is positive): this
+            // half's four chains, then the partner half's value.
+            float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int i = 0; i < NC; i += 4) {
+                mq[0] = fmaxf(mq[0], x[i]);
+                mq[1] = fmaxf(mq[1], x[i + 1]);
+                mq[2] = fmaxf(mq[2], x[i + 2]);
+                mq[3] = fmaxf(mq[3], x[i + 3]);
+            }
+            const float mh = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+            s_pair[b][hf][m] = mh;
+            pair_sync();
+            const float mx = fmaxf(mh, s_pair[b][hf ^ 1][m]) * a.scale_log2;
+            const float m_new = fmaxf(m_ref, mx);
+            const bool resc = m_new > m_ref + kRescaleLog2;   // true on the first finite maximum
+            const float ref = resc ? m_new : m_ref;
+            const float alpha = resc ? fast_exp2(m_ref - ref) : 1.f;
+            const float neg_ref = ref == -INFINITY ? 0.f : -ref;
+            // p = 2^(s * scale_log2 - ref): one FMA and one exp2 per score.
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t ph[NC / 2];
+#pragma unroll
+            for (int i = 0; i < NC; i += 2) {
+                const float p0 = fast_exp2(fmaf(x[i], a.scale_log2, neg_ref));
+                const float p1 = fast_exp2(fmaf(x[i + 1], a.scale_log2, neg_ref));
+                ls[(i >> 1) & 3] += p0 + p1;
+                ph[i / 2] = pack_half2(p0, p1);
+            }
+            l_run = l_run * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));   // this half's columns
+            m_ref = ref;
+            // P buffer and O are free once PV of the previous tile is done.
+            if (j > 0) {
+                __all_sync(0xffffffffu, wait(B_PVDONE, (j - 1) & 1));
+                tc::tc_fence_after();
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                    for (int c = 0; c < NC / 32; ++c) {
+                        uint32_t rr[32];
+                        tc::tmem_ld32(lane_base + 2 * kPN + hf * NC + c * 32, rr);
+                        tc::tmem_wait_ld(rr);
+                        float v[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(rr[i]) * alpha;
+                        tc::tmem_st32(lane_base + 2 * kPN + hf * NC + c * 32, v);
+                    }
+                    tc::tmem_wait_st();
+                }
+            }
+            // this half's 64 keys are exactly one 64-key swizzle block of P
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc)
+                *reinterpret_cast<uint4 *>(sm + kOffP + hf * kHalfTile + m * 128 + ((cc ^ (m & 7)) << 4)) =
+                    make_uint4(ph[cc * 4], ph[cc * 4 + 1], ph[cc * 4 + 2], ph[cc * 4 + 3]);
+            tc::fence_proxy_async_smem();
+            tc::tc_fence_before();
+            tc::mbar_arrive(bar(B_PFULL));
+        }
+        // ---------------- epilogue: O / l, lse -------------------------------
+        float ov[NC];
+        bool have = n_tiles > 0 && !*reinterpret_cast<volatile int *>(&s_abort);
+        if (have) have = wait(B_PVDONE, (n_tiles - 1) & 1);
+        have = __all_sync(0xffffffffu, have);
+        if (have) {
+            tc::tc_fence_after();
+            uint32_t orr[NC / 32][32];
+#pragma unroll
+            for (int c = 0; c < NC / 32; ++c) tc::tmem_ld32(lane_base + 2 * kPN + hf * NC + c * 32, orr[c]);
+#pragma unroll
+            for (int c = 0; c < NC / 32; ++c) tc::tmem_wait_ld(orr[c]);
+#pragma unroll
+            for (int c = 0; c < NC / 32; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) ov[c * 32 + i] = __uint_as_float(orr[c][i]);
+        }
+        // the row's sum is the two halves' sums
+        s_pair[2][hf][m] = l_run;
+        pair_sync();
+        const float l_row = l_run + s_pair[2][hf ^ 1][m];
+        if (row_ok) {
+            const int64_t r = (static_cast<int64_t>(s) * a.nq + t_row) * a.H + kh * a.G + (m % a.G);
+            const bool direct = a.n_splits == 1;
+            float *op = (direct ? a.o_out + r * kPD : a.o_split + (static_cast<int64_t>(split) * a.R + r) * kPD) +
+                        hf * NC;
+            float *lp = direct ? a.lse_out + r : a.lse_split + static_cast<int64_t>(split) * a.R + r;
+            if (!have || m_ref == -INFINITY || l_row <= 0.f) {
+#pragma unroll
+                for (int i = 0; i < NC; i += 4) *reinterpret_cast<float4 *>(op + i) = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (hf == 0) *lp = -INFINITY;
+            } else {
+                const float inv = 1.f / l_row;
+#pragma unroll
+                for (int i = 0; i < NC; i += 4)
+                    *reinterpret_cast<float4 *>(op + i) =
+                        make_float4(ov[i] * inv, ov[i + 1] * inv, ov[i + 2] * inv, ov[i + 3] * inv);
+                if (hf == 0) *lp = (m_ref + __log2f(l_row)) * 0.6931471805599453f;
+            }
+        }
+    }
+
+    // ---------------- teardown, then the cross-split merge --------------------
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc<512>(tmem);
+    }
+    if (a.n_splits == 1) return;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(a.counters + unit, 1) == a.n_splits - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (row_ok) {
+        // thread (row, half) merges its 64 columns over the splits
+        const int64_t r = (static_cast<int64_t>(s) * a.nq + t_row) * a.H + kh * a.G + (m % a.G);
+        float M = -INFINITY;
+        for (int sp = 0; sp < a.n_splits; ++sp) M = fmaxf(M, __ldcg(a.lse_split + static_cast<int64_t>(sp) * a.R + r));
+        float *op = a.o_out + r * kPD + hf * 64;
+        if (M == -INFINITY) {
+            for (int i = 0; i < 64; i += 4) *reinterpret_cast<float4 *>(op + i) = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (hf == 0) a.lse_out[r] = -INFINITY;
+        } else {
+            float acc[64];
+#pragma unroll
+            for (int i = 0; i < 64; ++i) acc[i] = 0.f;
+            float W = 0.f;
+            for (int sp = 0; sp < a.n_splits; ++sp) {
+                const float l = __ldcg(a.lse_split + static_cast<int64_t>(sp) * a.R + r);
+                if (l == -INFINITY) continue;
+                const float w = fast_exp2((l - M) * 1.4426950408889634f);
+                W += w;
+                const float4 *src = reinterpret_cast<const float4 *>(
+                    a.o_split + (static_cast<int64_t>(sp) * a.R + r) * kPD + hf * 64);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float4 v = __ldcg(src + i);
+                    acc[4 * i] = fmaf(w, v.x, acc[4 * i]);
+                    acc[4 * i + 1] = fmaf(w, v.y, acc[4 * i + 1]);
+                    acc[4 * i + 2] = fmaf(w, v.z, acc[4 * i + 2]);
+                    acc[4 * i + 3] = fmaf(w, v.w, acc[4 * i + 3]);
+                }
+            }
+            const float inv = 1.f / W;
+            for (int i = 0; i < 64; i += 4)
+                *reinterpret_cast<float4 *>(op + i) = make_float4(acc[i] * inv, acc[i + 1] * inv, acc[i + 2] * inv,
+                                                                  acc[i + 3] * inv);
+            if (hf == 0) a.lse_out[r] = M + __logf(W);
+        }
+    }
+    if (tid == 0) a.counters[unit] = 0;
+}
+
+// Launch one instance (sets its shared-memory attribute once per process).
+template <int MODE, int KT, int VT>
+int launch_prefill_t(skv_handle *h, const CUtensorMap &mk, const CUtensorMap &mv, const PrefillArgs &a, dim3 grid,
+                     cudaStream_t st)
+{
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(splitkv_prefill_kernel<MODE, KT, VT>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        if (e != cudaSuccess) return cuda_fail(h, e, "cudaFuncSetAttribute(prefill)");
+        attr_done = true;
+    }
+    if (h->prof_before) cudaEventRecord(h->prof_before, st);
+    splitkv_prefill_kernel<MODE, KT, VT><<<grid, Cfg<MODE>::kThreads, kSmem, st>>>(mk, mv, a);
+    if (h->prof_after) cudaEventRecord(h->prof_after, st);
+    return cuda_fail(h, cudaGetLastError(), "prefill kernel launch");
+}
+
+// Software-producer instances (prefill_sw.cu).
+int launch_prefill_sw(skv_handle *h, const PrefillArgs &a, int kt, int vt, dim3 grid, cudaStream_t st);
+
+}  // namespace pf
+}  // namespace skv
