@@ -47,7 +47,70 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-extras", action="store_true")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline sample")
+    p.add_argument("--profile-case", choices=sorted(PROFILE_CASES), default=None,
+                   help="run one kernel case twice (no timing, no JSON line): the command profiles/ captures")
     return p.parse_args()
+
+
+PROFILE_CASES = ("decode_unified", "decode_q8q4_window", "prefill_window", "prefill_q8q4_window",
+                 "prefill_row_list", "append_q8_0")
+
+
+def run_profile_case(name: str) -> int:
+    """One workload's call, twice (the second is the one a profiler captures),
+    with the inputs the bench times: the unified-cache decode, the q8_0/q4_0
+    long-context window (131072 rows), the prefill chunk's window (512 tokens
+    over 32768 fp16 keys), the same prefill over q8_0-K / q4_0-V rows, the
+    8-sequence row-list prefill over the unified cache, and a 32768-row
+    q8_0 append."""
+    import torch
+    import split_kv_flash_attn_gb300 as skv
+    from split_kv_flash_attn_gb300 import build as skv_build
+    from split_kv_flash_attn_gb300 import workloads as wl
+    if not os.path.exists(skv_build.LIB):
+        skv_build.build()
+    h = skv.Handle(0)
+    cu = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()   # noqa: E731
+    if name == "decode_unified":
+        w = wl.unified_decode()
+        q, k, v, rows = cu(w.q), cu(w.k), cu(w.v), cu(w.kv_rows)
+        call = lambda: skv.attn_partial(h, q, k, v, Hk=w.Hk, kv_rows=rows)   # noqa: E731
+    elif name == "decode_q8q4_window":
+        w = wl.long_context_decode()
+        q, k, v = cu(w.q), cu(w.k), cu(w.v)
+        call = lambda: skv.attn_partial(h, q, k, v, Hk=w.Hk, k_type=w.k_type, v_type=w.v_type)   # noqa: E731
+    elif name == "prefill_window":
+        w = wl.prefill_chunk()
+        q, k, v, qp = cu(w.q), cu(w.k), cu(w.v), cu(w.q_pos)
+        call = lambda: skv.attn_partial(h, q, k, v, Hk=w.Hk, q_pos=qp)   # noqa: E731
+    elif name == "prefill_q8q4_window":
+        rng = wl.generator(4, salt=77)
+        nq, H, Hk, D, n = 512, 32, 8, 128, 32768
+        q = cu(wl.normal_f16(rng, (1, nq, H, D)))
+        k, v = cu(wl.cache_rows(rng, wl.Q8_0, n, Hk, D)), cu(wl.cache_rows(rng, wl.Q4_0, n, Hk, D))
+        qp = torch.arange(n - nq, n, dtype=torch.int32, device="cuda").reshape(1, nq)
+        call = lambda: skv.attn_partial(h, q, k, v, Hk=Hk, k_type=wl.Q8_0, v_type=wl.Q4_0, q_pos=qp)   # noqa: E731
+    elif name == "prefill_row_list":
+        w = wl.unified_decode()
+        rng = wl.generator(4, salt=77)
+        nq, n_list = 64, w.kv_rows.shape[1]
+        q = cu(wl.normal_f16(rng, (w.S, nq, w.H, w.D)))
+        k, v, rows = cu(w.k), cu(w.v), cu(w.kv_rows)
+        qp = (torch.arange(nq, dtype=torch.int32, device="cuda") + (n_list - nq)).repeat(w.S, 1).contiguous()
+        call = lambda: skv.attn_partial(h, q, k, v, Hk=w.Hk, kv_rows=rows, q_pos=qp)   # noqa: E731
+    else:
+        rng = wl.generator(6, salt=7)
+        Hk, D, n = 8, 128, 32768
+        x = cu(wl.new_kv_values(rng, n, Hk, D)[0])
+        pos = torch.arange(n, dtype=torch.int32, device="cuda")
+        dst = torch.empty((n, Hk * wl.segment_bytes(wl.Q8_0, D)), dtype=torch.uint8, device="cuda")
+        call = lambda: skv.kv_append(h, x, pos, dst, None, type_=wl.Q8_0, n_rows0=n, n_rows1=0)   # noqa: E731
+    for _ in range(2):
+        call()
+    torch.cuda.synchronize()
+    h.status()
+    print(f"profile case {name}: ok")
+    return 0
 
 
 def dist_env():
@@ -194,6 +257,8 @@ def run_reference(args):
 
 def main():
     args = parse()
+    if args.profile_case:
+        return run_profile_case(args.profile_case)
     if args.impl == "reference":
         return run_reference(args)
     import torch
