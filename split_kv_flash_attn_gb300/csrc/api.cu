@@ -426,13 +426,18 @@ int skv_attn_partial(skv_handle *h, const skv_shape *shape, const void *q, const
         }
         return launch_prefill(h, L, st);
     }
-    const int ctas = decode_ctas_per_sm(h, shape->k_type, shape->v_type, D);
+    // Dense quantised ranges: the whole-row kernel (all KV heads per CTA).
+    const bool rows_k = !kv_rows && decode_rows_eligible(shape, k, v, mask);
+    const int ctas = rows_k ? decode_rows_ctas_per_sm(shape) : decode_ctas_per_sm(h, shape->k_type, shape->v_type, D);
     if (ctas <= 0) return fail(h, SKV_EUNSUPPORTED, "no decode kernel for this type pairing / head dim");
-    const int64_t units = static_cast<int64_t>(shape->S) * shape->Hk * n_cg;
+    const int64_t units = static_cast<int64_t>(shape->S) * (rows_k ? 1 : shape->Hk) * n_cg;
     int64_t split_len = 0;
     int32_t n_splits = 0;
-    rc = skv_plan_splits(n_local, units, h->sm_count, ctas, kDecodeTile, kv_rows ? kMaxListSplit : 0, &split_len,
-                         &n_splits);
+    if (rows_k)
+        rc = plan_splits_cost(n_local, units, h->sm_count, ctas, kRowsTile, 0, 1, &split_len, &n_splits);
+    else
+        rc = skv_plan_splits(n_local, units, h->sm_count, ctas, kDecodeTile, kv_rows ? kMaxListSplit : 0, &split_len,
+                             &n_splits);
     if (rc) return fail(h, rc, "split planning failed");
 
     if (n_splits > kMaxSplits) return fail(h, SKV_EUNSUPPORTED, "%d splits exceed %d", n_splits, kMaxSplits);
@@ -466,6 +471,7 @@ int skv_attn_partial(skv_handle *h, const skv_shape *shape, const void *q, const
         a.o_split = static_cast<float *>(h->workspace);
         a.lse_split = reinterpret_cast<float *>(static_cast<uint8_t *>(h->workspace) + o_bytes);
     }
+    if (rows_k) return launch_decode_rows(h, a, shape->k_type, shape->v_type, st);
     return launch_decode(h, a, shape->k_type, shape->v_type, D, st);
 }
 
@@ -517,11 +523,17 @@ int skv_attn_window_tail(skv_handle *h, const skv_shape *shape, const void *q, c
     // Many query rows per KV head: the tensor-core prefill kernel; else the
     // split-KV decode kernel.
     const bool use_tc = prefill_eligible(shape, mask);
-    const int ctas = use_tc ? 1 : decode_ctas_per_sm(h, shape->k_type, shape->v_type, D);
+    // quantised rows: the whole-row decode kernel (ring slots are 256-byte aligned)
+    const bool use_rows = !use_tc && decode_rows_eligible(shape, n_win > 0 ? k_win : nullptr,
+                                                          n_win > 0 ? v_win : nullptr, mask);
+    const int ctas = use_tc ? 1
+                     : use_rows ? decode_rows_ctas_per_sm(shape)
+                                : decode_ctas_per_sm(h, shape->k_type, shape->v_type, D);
     if (ctas <= 0) return fail(h, SKV_EUNSUPPORTED, "no decode kernel for this type pairing / head dim");
     const int64_t units = use_tc ? static_cast<int64_t>(shape->S) * prefill_units(shape)
-                                 : static_cast<int64_t>(shape->S) * shape->Hk * n_cg;
-    const int tile = use_tc ? kPrefillTile : kDecodeTile;
+                          : use_rows ? static_cast<int64_t>(shape->S) * n_cg
+                                     : static_cast<int64_t>(shape->S) * shape->Hk * n_cg;
+    const int tile = use_tc ? kPrefillTile : use_rows ? kRowsTile : kDecodeTile;
 
     int64_t w_len = 0, t_len = 0;
     int32_t w_splits = 0, t_splits = 0;
@@ -591,6 +603,7 @@ int skv_attn_window_tail(skv_handle *h, const skv_shape *shape, const void *q, c
     }
     // One launch over a dense region (window or ring slot) of n_rows rows.
     auto run = [&](int64_t n_rows) -> int {
+        if (use_rows) return launch_decode_rows(h, a, shape->k_type, shape->v_type, st);
         if (!use_tc) return launch_decode(h, a, shape->k_type, shape->v_type, D, st);
         PrefillLaunch L;
         memset(&L, 0, sizeof(L));

@@ -80,6 +80,7 @@ struct DecodeArgs {
     float *o_out;               // merged result of this launch [R][D]
     float *lse_out;             // [R]
     int64_t R;                  // S*nq*H
+    int *status;                // device status word (kernels with bounded waits)
 };
 
 // Splits of one launch merged by the last-arriving CTA of each unit are
@@ -100,6 +101,14 @@ int decode_ctas_quant(skv_handle *h, int k_type, int v_type, int D);
 // take in list/paged mode.
 constexpr int kDecodeTile = 64;
 constexpr int kMaxListSplit = 2048;
+
+// Decode over a dense range of quantised rows (q8_0 / q4_0, D = 128, no
+// additive mask, Hk <= 8): one CTA per (sequence, column group, split) for
+// all KV heads, whole-row stages by bulk copy; splits merged by a combine.
+constexpr int kRowsTile = 32;   // keys per stage
+bool decode_rows_eligible(const skv_shape *sh, const void *k, const void *v, const void *mask);
+int decode_rows_ctas_per_sm(const skv_shape *sh);
+int launch_decode_rows(skv_handle *h, const DecodeArgs &a, int kt, int vt, cudaStream_t st);
 
 int launch_combine(int n_parts, const float *o_parts, const float *lse_parts, int64_t rows, int D, float *o,
                    float *lse, cudaStream_t st);
