@@ -441,8 +441,12 @@ def run_extras(torch, skv, wl, h, hbm_peak):
         h.set_profile_events(None, None)
         win_bytes = w.k.nbytes + w.v.nbytes
         win_ms = statistics.median(ks)
+        # the whole window call: the decode kernel plus the combine of its splits
+        call_ms = _time_calls(torch, lambda: skv.attn_partial(h, q, kw_, vw_, Hk=w.Hk, k_type=w.k_type,
+                                                              v_type=w.v_type, o=o, lse=lse), 20)
         out["long_context_window"] = {"rows": w.k.shape[0], "bytes": win_bytes, "kernel_ms": win_ms,
-                                      "GBps": win_bytes / win_ms / 1e6, "frac_hbm": win_bytes / win_ms / 1e6 / hbm_peak}
+                                      "GBps": win_bytes / win_ms / 1e6, "frac_hbm": win_bytes / win_ms / 1e6 / hbm_peak,
+                                      "call_ms": call_ms, "call_GBps": win_bytes / call_ms / 1e6}
         # whole call: window + 28 streamed tail tiles + combine
         for _ in range(2):
             skv.attn_window_tail(h, q, kw_, vw_, kt, vt, Hk=w.Hk, tile_rows=w.tile_rows, k_type=w.k_type,

@@ -223,7 +223,9 @@ int skv_attn_partial_static(const skv_shape *shape, const void *q, const void *k
  * results: o_parts fp32 [n_parts][rows][D], lse_parts fp32 [n_parts][rows]
  * -> o [rows][D], lse [rows].  A part with lse = -inf contributes nothing
  * (its o is never read); every part -inf gives o = 0, lse = -inf.
- * n_parts = 0 is allowed (fills o = 0, lse = -inf). */
+ * n_parts = 0 is allowed (fills o = 0, lse = -inf).  Limits: n_parts <= 4096,
+ * D <= 128 and a multiple of 4, o_parts and o 16-byte aligned
+ * (SKV_EUNSUPPORTED otherwise). */
 int skv_attn_combine(skv_handle *h, int32_t n_parts, const float *o_parts, const float *lse_parts,
                      int64_t rows, int32_t D, float *o, float *lse, void *stream);
 

@@ -359,6 +359,8 @@ int skv_attn_combine(skv_handle *h, int32_t n_parts, const float *o_parts, const
     h->err[0] = 0;
     if (n_parts < 0 || rows < 0 || D <= 0 || D > 128) return fail(h, SKV_EINVAL, "bad combine sizes");
     if (!o || !lse || (n_parts > 0 && (!o_parts || !lse_parts))) return fail(h, SKV_EINVAL, "NULL pointer");
+    if (n_parts > 4096 || D % 4 || (reinterpret_cast<uintptr_t>(o_parts) | reinterpret_cast<uintptr_t>(o)) % 16)
+        return fail(h, SKV_EUNSUPPORTED, "combine needs n_parts <= 4096, D a multiple of 4, 16-byte aligned o");
     int rc = launch_combine(n_parts, o_parts, lse_parts, rows, D, o, lse, static_cast<cudaStream_t>(stream));
     return rc == SKV_OK ? rc : cuda_fail(h, cudaGetLastError(), "combine launch");
 }

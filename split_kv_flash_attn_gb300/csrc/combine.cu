@@ -9,62 +9,116 @@
 
 namespace skv {
 
-// One CTA of 128 threads per output row: the lse of all parts are read in
-// parallel (one part per thread) for the maximum, then in chunks of 128 the
-// weights go to shared memory and thread d accumulates element d over the
-// chunk's parts, whose loads are independent of one another.
-__global__ void __launch_bounds__(128) splitkv_combine_kernel(int n_parts, const float *__restrict__ o_parts,
-                                                              const float *__restrict__ lse_parts, int64_t rows,
-                                                              int D, float *__restrict__ o, float *__restrict__ lse)
+// One CTA of 256 threads per output row.  The parts' weights are computed
+// in parallel into shared memory (after the maximum); then warp w takes parts
+// w, w + 8, ... and lane l elements 4l .. 4l+3 (16-byte loads), so each warp
+// keeps several parts' loads in flight; the eight warps' sums are added in
+// shared memory.
+constexpr int kCombineThreads = 256;
+constexpr int kCombineMaxParts = 4096;
+
+__global__ void __launch_bounds__(kCombineThreads) splitkv_combine_kernel(int n_parts,
+                                                                          const float *__restrict__ o_parts,
+                                                                          const float *__restrict__ lse_parts,
+                                                                          int64_t rows, int D, float *__restrict__ o,
+                                                                          float *__restrict__ lse)
 {
-    __shared__ float w_s[128];
-    __shared__ float red[4];
+    __shared__ float w_s[kCombineMaxParts];
+    __shared__ float red[kCombineThreads / 32];
+    __shared__ float4 acc_s[kCombineThreads / 32][32];
     const int64_t row = blockIdx.x;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float M = -INFINITY;
-    for (int p = tid; p < n_parts; p += 128) M = fmaxf(M, lse_parts[static_cast<int64_t>(p) * rows + row]);
+    for (int p = tid; p < n_parts; p += kCombineThreads) M = fmaxf(M, lse_parts[static_cast<int64_t>(p) * rows + row]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    if ((tid & 31) == 0) red[tid >> 5] = M;
+    if (lane == 0) red[warp] = M;
     __syncthreads();
-    M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    M = red[0];
+#pragma unroll
+    for (int w = 1; w < kCombineThreads / 32; ++w) M = fmaxf(M, red[w]);
     if (M == -INFINITY) {
-        if (tid < D) o[row * D + tid] = 0.f;
+        for (int d = tid; d < D; d += kCombineThreads) o[row * D + d] = 0.f;
         if (tid == 0) lse[row] = -INFINITY;
         return;
     }
-    float acc = 0.f;
     float W = 0.f;
-    for (int base = 0; base < n_parts; base += 128) {
-        const int cnt = min(128, n_parts - base);
-        __syncthreads();
-        if (tid < cnt) {
-            const float l = lse_parts[static_cast<int64_t>(base + tid) * rows + row];
-            w_s[tid] = l == -INFINITY ? 0.f : expf(l - M);
-        }
-        __syncthreads();
-        if (tid < D) {
-            const float *op = o_parts + (static_cast<int64_t>(base) * rows + row) * D + tid;
-            const int64_t stride = rows * D;
-#pragma unroll 8
-            for (int i = 0; i < cnt; ++i) {
-                const float w = w_s[i];
-                const float x = op[i * stride];
-                acc = w != 0.f ? fmaf(w, x, acc) : acc;
+    for (int p = tid; p < n_parts; p += kCombineThreads) {
+        const float l = lse_parts[static_cast<int64_t>(p) * rows + row];
+        const float w = l == -INFINITY ? 0.f : expf(l - M);
+        w_s[p] = w;
+        W += w;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
+    __syncthreads();                                  // w_s complete; red[] free again
+    if (lane == 0) red[warp] = W;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int d0 = 4 * lane;
+    if (d0 < D) {
+        const int64_t stride = rows * D;
+        const float *base = o_parts + row * D + d0;
+        int p = warp;
+        for (; p + 3 * (kCombineThreads / 32) < n_parts; p += 4 * (kCombineThreads / 32)) {
+            float4 x[4];
+            float w[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int q = p + u * (kCombineThreads / 32);
+                x[u] = *reinterpret_cast<const float4 *>(base + q * stride);
+                w[u] = w_s[q];
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (w[u] != 0.f) {
+                    acc.x = fmaf(w[u], x[u].x, acc.x);
+                    acc.y = fmaf(w[u], x[u].y, acc.y);
+                    acc.z = fmaf(w[u], x[u].z, acc.z);
+                    acc.w = fmaf(w[u], x[u].w, acc.w);
+                }
             }
         }
-        for (int i = 0; i < cnt; ++i) W += w_s[i];
+        for (; p < n_parts; p += kCombineThreads / 32) {
+            const float w = w_s[p];
+            if (w != 0.f) {
+                const float4 x = *reinterpret_cast<const float4 *>(base + p * stride);
+                acc.x = fmaf(w, x.x, acc.x);
+                acc.y = fmaf(w, x.y, acc.y);
+                acc.z = fmaf(w, x.z, acc.z);
+                acc.w = fmaf(w, x.w, acc.w);
+            }
+        }
     }
-    if (tid < D) o[row * D + tid] = acc / W;
-    if (tid == 0) lse[row] = M + logf(W);
+    acc_s[warp][lane] = acc;
+    __syncthreads();
+    if (warp == 0) {
+        float Wt = 0.f;
+#pragma unroll
+        for (int w = 0; w < kCombineThreads / 32; ++w) Wt += red[w];
+        if (d0 < D) {
+            float4 t = acc_s[0][lane];
+#pragma unroll
+            for (int w = 1; w < kCombineThreads / 32; ++w) {
+                const float4 u = acc_s[w][lane];
+                t.x += u.x;
+                t.y += u.y;
+                t.z += u.z;
+                t.w += u.w;
+            }
+            const float inv = 1.f / Wt;
+            *reinterpret_cast<float4 *>(o + row * D + d0) = make_float4(t.x * inv, t.y * inv, t.z * inv, t.w * inv);
+        }
+        if (lane == 0) lse[row] = M + logf(Wt);
+    }
 }
 
 int launch_combine(int n_parts, const float *o_parts, const float *lse_parts, int64_t rows, int D, float *o,
                    float *lse, cudaStream_t st)
 {
     if (rows <= 0) return SKV_OK;
-    if (rows > 0x7fffffff) return SKV_EUNSUPPORTED;
-    splitkv_combine_kernel<<<static_cast<unsigned>(rows), 128, 0, st>>>(n_parts, o_parts, lse_parts, rows, D, o, lse);
+    if (rows > 0x7fffffff || n_parts > kCombineMaxParts || D > 128 || D % 4) return SKV_EUNSUPPORTED;
+    splitkv_combine_kernel<<<static_cast<unsigned>(rows), kCombineThreads, 0, st>>>(n_parts, o_parts, lse_parts, rows,
+                                                                                   D, o, lse);
     return cudaGetLastError() == cudaSuccess ? SKV_OK : SKV_ECUDA;
 }
 

@@ -3,9 +3,10 @@
 // key split) covering every KV head.
 //
 // A cell-major row holds all KV heads, so a range of rows is one contiguous
-// span: each 32-row stage of K and of V arrives by a single bulk copy
-// (cp.async.bulk, completion counted on an mbarrier) instead of one copy per
-// head segment.  Warp w owns KV head w: for its 32 keys per stage it
+// span: each 32-row stage of K and of V arrives as 16 bulk copies of two
+// whole rows each (cp.async.bulk, completion counted on an mbarrier), padded
+// apart in shared memory against bank conflicts, instead of one copy per head
+// segment.  Warp w owns KV head w: for its 32 keys per stage it
 //   * builds the m16n8k16 A fragments of K straight from the raw codes in
 //     shared memory (no converted tile): the head dimension is permuted so
 //     that each thread's eight values of a 32-value block are eight adjacent
@@ -37,6 +38,18 @@ struct QB {
     static constexpr int seg = 4 * blk;                    // bytes per head segment
 };
 
+// Pad after each 2-row chunk (16-byte multiple) that makes the chunk stride
+// 8 banks mod 32, for rows whose byte stride is a multiple of 16.
+__host__ __device__ __forceinline__ uint32_t chunk_pad(int64_t row_bytes)
+{
+    const int64_t words = 2 * (row_bytes / 4);
+    return static_cast<uint32_t>(((8 - words % 32) % 32 + 32) % 32) * 4;
+}
+__host__ __device__ __forceinline__ int64_t rows_stage_bytes(int64_t krb, int64_t vrb)
+{
+    return (kRRows / 2) * (2 * krb + chunk_pad(krb) + 2 * vrb + chunk_pad(vrb));
+}
+
 __device__ __forceinline__ uint32_t ld_s16(const uint8_t *p) { return *reinterpret_cast<const uint16_t *>(p); }
 
 // Bytes 0,1 (SEL = 0x4140) or 2,3 (SEL = 0x4342) of w -> half2(1024 + b, ...)
@@ -53,21 +66,52 @@ constexpr uint32_t kBias8 = 0x64806480u;   // half2(1152): byte q ^ 0x80 = q + 1
 constexpr uint32_t kBias4 = 0x64086408u;   // half2(1032): nibble u -> u - 8
 
 // K A-fragment values of one key row for block b: h[0], h[1] feed k-slice 0
-// (columns 2t..2t+1 and 2t+8..2t+9), h[2], h[3] k-slice 1.
+// (columns 2t..2t+1 and 2t+8..2t+9), h[2], h[3] k-slice 1.  `seg` is 8-byte
+// aligned; the loads are as wide as each block's code offset allows.
 template <int KT>
 __device__ __forceinline__ void k_codes(const uint8_t *seg, int b, int t, uint32_t (&h)[4])
 {
     if constexpr (KT == SKV_Q8_0) {
-        const uint8_t *p = seg + 34 * b + 2 + 8 * t;             // codes 8t .. 8t+7 of the block
-#pragma unroll
-        for (int i = 0; i < 4; ++i) h[i] = to_h2<0x4140>(ld_s16(p + 2 * i) ^ 0x8080u, kBias8);
+        // codes 8t .. 8t+7 of the block start at byte 34b + 2 + 8t, which is
+        // 2, 4, 6, 0 mod 8 for b = 0..3
+        const uint8_t *p = seg + 34 * b + 2 + 8 * t;
+        if (b == 3) {
+            const uint2 w = *reinterpret_cast<const uint2 *>(p);
+            const uint32_t w0 = w.x ^ 0x80808080u, w1 = w.y ^ 0x80808080u;
+            h[0] = to_h2<0x4140>(w0, kBias8);
+            h[1] = to_h2<0x4342>(w0, kBias8);
+            h[2] = to_h2<0x4140>(w1, kBias8);
+            h[3] = to_h2<0x4342>(w1, kBias8);
+        } else if (b == 1) {
+            const uint32_t w0 = *reinterpret_cast<const uint32_t *>(p) ^ 0x80808080u;
+            const uint32_t w1 = *reinterpret_cast<const uint32_t *>(p + 4) ^ 0x80808080u;
+            h[0] = to_h2<0x4140>(w0, kBias8);
+            h[1] = to_h2<0x4342>(w0, kBias8);
+            h[2] = to_h2<0x4140>(w1, kBias8);
+            h[3] = to_h2<0x4342>(w1, kBias8);
+        } else {                                                  // 2 mod 4: three aligned words
+            const uint32_t *q = reinterpret_cast<const uint32_t *>(p - 2);
+            const uint32_t w0 = q[0] ^ 0x80808080u, w1 = q[1] ^ 0x80808080u, w2 = q[2] ^ 0x80808080u;
+            h[0] = to_h2<0x4342>(w0, kBias8);
+            h[1] = to_h2<0x4140>(w1, kBias8);
+            h[2] = to_h2<0x4342>(w1, kBias8);
+            h[3] = to_h2<0x4140>(w2, kBias8);
+        }
     } else {
-        const uint8_t *p = seg + 18 * b + 2 + 4 * t;             // bytes 4t .. 4t+3 of the block
-        const uint32_t u0 = ld_s16(p), u1 = ld_s16(p + 2);
-        h[0] = to_h2<0x4140>(u0 & 0x0F0Fu, kBias4);              // values 4t, 4t+1
-        h[1] = to_h2<0x4140>(u1 & 0x0F0Fu, kBias4);              // values 4t+2, 4t+3
-        h[2] = to_h2<0x4140>((u0 >> 4) & 0x0F0Fu, kBias4);       // values 16+4t, 16+4t+1
-        h[3] = to_h2<0x4140>((u1 >> 4) & 0x0F0Fu, kBias4);       // values 16+4t+2, 16+4t+3
+        // bytes 4t .. 4t+3 of the block start at 18b + 2 + 4t: 2, 0, 2, 0 mod 4
+        const uint8_t *p = seg + 18 * b + 2 + 4 * t;
+        uint32_t w;                                               // the four code bytes
+        if (b & 1) {
+            w = *reinterpret_cast<const uint32_t *>(p);
+        } else {
+            const uint32_t *q = reinterpret_cast<const uint32_t *>(p - 2);
+            w = __byte_perm(q[0], q[1], 0x5432);
+        }
+        const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
+        h[0] = to_h2<0x4140>(lo, kBias4);                         // values 4t, 4t+1
+        h[1] = to_h2<0x4342>(lo, kBias4);                         // values 4t+2, 4t+3
+        h[2] = to_h2<0x4140>(hi, kBias4);                         // values 16+4t, 16+4t+1
+        h[3] = to_h2<0x4342>(hi, kBias4);                         // values 16+4t+2, 16+4t+3
     }
 }
 
@@ -100,6 +144,8 @@ __global__ void __launch_bounds__(256) splitkv_decode_rows_kernel(const DecodeAr
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t full_bar[kRStages];
     __shared__ int s_abort;
+    __shared__ int s_done[kRStages];             // warps finished with the stage's current tile
+    __shared__ int s_issued;                     // tiles issued so far
 
     const int tid = threadIdx.x;
     const int kh = tid >> 5;                     // warp = KV head
@@ -112,38 +158,59 @@ __global__ void __launch_bounds__(256) splitkv_decode_rows_kernel(const DecodeAr
     const int64_t j_hi = min(a.n_local, j_lo + a.split_len);
     const int n_tiles = j_hi > j_lo ? static_cast<int>((j_hi - j_lo + kRRows - 1) / kRRows) : 0;
     const int64_t krb = a.k_row_bytes, vrb = a.v_row_bytes;
-    const uint32_t stage_k = static_cast<uint32_t>(kRRows * krb);
-    const uint32_t stage_bytes = stage_k + static_cast<uint32_t>(kRRows * vrb);
+    // Rows land in 2-row chunks separated by a pad that shifts consecutive
+    // chunks by 8 banks, so the 8 key rows one instruction reads sit on
+    // different banks.
+    const uint32_t chunk_k = static_cast<uint32_t>(2 * krb) + chunk_pad(krb);
+    const uint32_t chunk_v = static_cast<uint32_t>(2 * vrb) + chunk_pad(vrb);
+    const uint32_t stage_k = (kRRows / 2) * chunk_k;
+    const uint32_t stage_bytes = stage_k + (kRRows / 2) * chunk_v;
+    auto krow = [&](int r) { return (r >> 1) * chunk_k + (r & 1) * static_cast<uint32_t>(krb); };
+    auto vrow = [&](int r) { return (r >> 1) * chunk_v + (r & 1) * static_cast<uint32_t>(vrb); };
     const uint32_t sbase = smem_addr(smem);
     auto bar = [&](int st) { return smem_addr(&full_bar[st]); };
 
     if (tid == 0) {
         s_abort = 0;
-        for (int i = 0; i < kRStages; ++i) tc::mbar_init(bar(i), 1);
+        s_issued = 0;
+        for (int i = 0; i < kRStages; ++i) {
+            tc::mbar_init(bar(i), 1);
+            s_done[i] = 0;
+        }
         tc::fence_barrier_init();
     }
     __syncthreads();
 
-    // One thread issues a stage: the K rows then the V rows of keys
-    // [j_lo + 32 tile, ...), all heads, as two bulk copies.
-    int issued = 0;                              // tiles issued (thread 0)
+    // One warp issues a stage: lane l < 16 copies K rows 2l, 2l+1 of keys
+    // [j_lo + 32 tile, ...) (all heads), lane 16 + l the same V rows.  The
+    // first stages are issued by warp 0; afterwards the last warp to finish
+    // with a stage refills it, so no warp waits for the others.
     auto issue = [&](int tile) {
-        ++issued;
+        if (lane == 0) s_issued = tile + 1;
         const int st = tile % kRStages;
         const int64_t k0 = j_lo + static_cast<int64_t>(tile) * kRRows;
         const int rows = static_cast<int>(min(j_hi - k0, static_cast<int64_t>(kRRows)));
-        const int64_t r0 = a.row0 + k0;
-        const uint32_t kb = static_cast<uint32_t>(rows * krb), vb = static_cast<uint32_t>(rows * vrb);
-        tc::mbar_expect_tx(bar(st), kb + vb);
-        tc::bulk_load(sbase + st * stage_bytes, a.k + r0 * krb, kb, bar(st));
-        tc::bulk_load(sbase + st * stage_bytes + stage_k, a.v + r0 * vrb, vb, bar(st));
+        if (lane == 0)
+            tc::mbar_expect_tx(bar(st), static_cast<uint32_t>(rows * (krb + vrb)));
+        __syncwarp();
+        const int c = lane & 15;
+        const int n = min(2, rows - 2 * c);
+        if (n > 0) {
+            const int64_t r = a.row0 + k0 + 2 * c;
+            if (lane < 16)
+                tc::bulk_load(sbase + st * stage_bytes + c * chunk_k, a.k + r * krb, static_cast<uint32_t>(n * krb),
+                              bar(st));
+            else
+                tc::bulk_load(sbase + st * stage_bytes + stage_k + c * chunk_v, a.v + r * vrb,
+                              static_cast<uint32_t>(n * vrb), bar(st));
+        }
     };
-    if (tid == 0)
-        for (int p = 0; p < kRStages - 1 && p < n_tiles; ++p) issue(p);
+    if (tid < 32)
+        for (int p = 0; p < kRStages && p < n_tiles; ++p) issue(p);
 
     // This warp's columns: column n = g of the query fragment; the thread's
     // accumulator columns 2t, 2t+1.
-    const bool head_ok = kh < a.Hk;
+    const bool head_ok = true;                   // one warp per KV head: blockDim = 32 * Hk
     uint32_t qf[4][4];
     {
         const int c = cg * 8 + g;
@@ -171,9 +238,8 @@ __global__ void __launch_bounds__(256) splitkv_decode_rows_kernel(const DecodeAr
     float m_run[2] = {-INFINITY, -INFINITY};
     float l_run[2] = {0.f, 0.f};
 
+    __syncwarp();
     for (int i = 0; i < n_tiles; ++i) {
-        // the stage consumed in iteration i-1 is free (trailing barrier)
-        if (tid == 0 && i + kRStages - 1 < n_tiles) issue(i + kRStages - 1);
         const int st = i % kRStages;
         bool ok = !*reinterpret_cast<volatile int *>(&s_abort) &&
                   tc::mbar_wait(bar(st), (i / kRStages) & 1, a.status);
@@ -182,10 +248,9 @@ __global__ void __launch_bounds__(256) splitkv_decode_rows_kernel(const DecodeAr
                 s_abort = 1;
                 atomicOr(a.status, 1);
             }
+            break;
         }
-        __syncthreads();
-        if (*reinterpret_cast<volatile int *>(&s_abort)) break;
-        if (head_ok) {
+        {
             const uint8_t *sk = smem + st * stage_bytes + kh * SEGK;
             const uint8_t *sv = smem + st * stage_bytes + stage_k + kh * SEGV;
             const int64_t key0 = j_lo + static_cast<int64_t>(i) * kRRows;    // local index of stage row 0
@@ -193,8 +258,8 @@ __global__ void __launch_bounds__(256) splitkv_decode_rows_kernel(const DecodeAr
             float x[2][4];
 #pragma unroll
             for (int mh = 0; mh < 2; ++mh) {
-                const uint8_t *kg = sk + (mh * 16 + g) * krb;
-                const uint8_t *kg8 = kg + 8 * krb;
+                const uint8_t *kg = sk + krow(mh * 16 + g);
+                const uint8_t *kg8 = sk + krow(mh * 16 + g + 8);
                 float sacc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int b = 0; b < 4; ++b) {
@@ -254,13 +319,13 @@ __global__ void __launch_bounds__(256) splitkv_decode_rows_kernel(const DecodeAr
             // ---- O^T += V^T P^T, one 16-key k-slice per m-tile of keys ----
 #pragma unroll
             for (int mh = 0; mh < 2; ++mh) {
-                const uint8_t *vg = sv + (mh * 16 + g) * vrb;            // this thread's P rows: keys g, g+8
-                const uint8_t *vg8 = vg + 8 * vrb;
+                const uint8_t *vg = sv + vrow(mh * 16 + g);              // this thread's P rows: keys g, g+8
+                const uint8_t *vg8 = sv + vrow(mh * 16 + g + 8);
                 const bool ok0 = key0 + mh * 16 + g < j_hi, ok1 = key0 + mh * 16 + g + 8 < j_hi;
-                const uint8_t *va = sv + (mh * 16 + 2 * t) * vrb;        // A-fragment keys 2t, 2t+1, 2t+8, 2t+9
-                const uint8_t *vb = va + vrb;
-                const uint8_t *vc = va + 8 * vrb;
-                const uint8_t *vd = vc + vrb;
+                const uint8_t *va = sv + vrow(mh * 16 + 2 * t);          // A-fragment keys 2t, 2t+1, 2t+8, 2t+9
+                const uint8_t *vb = sv + vrow(mh * 16 + 2 * t + 1);
+                const uint8_t *vc = sv + vrow(mh * 16 + 2 * t + 8);
+                const uint8_t *vd = sv + vrow(mh * 16 + 2 * t + 9);
 #pragma unroll
                 for (int b = 0; b < 4; ++b) {
                     const float d0 = ok0 ? __half2float(__ushort_as_half(static_cast<unsigned short>(ld_s16(vg + BLKV * b)))) : 0.f;
@@ -294,14 +359,27 @@ __global__ void __launch_bounds__(256) splitkv_decode_rows_kernel(const DecodeAr
                 }
             }
         }
-        __syncthreads();                                              // stage st may be refilled
+        // The last warp done with stage st refills it with tile i + kRStages.
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+            __threadfence_block();
+            last = atomicAdd(&s_done[st], 1) == a.Hk - 1;
+            if (last) s_done[st] = 0;
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last && i + kRStages < n_tiles) {
+            tc::fence_proxy_async_smem();        // our reads of the stage before the copy's writes
+            issue(i + kRStages);
+        }
     }
+    __syncthreads();
     if (*reinterpret_cast<volatile int *>(&s_abort) && tid == 0) {
         // drain: every issued copy must land before the CTA exits
+        const int issued = s_issued;
         for (int j = max(0, issued - kRStages); j < issued; ++j)
             tc::mbar_wait(bar(j % kRStages), (j / kRStages) & 1, nullptr, 100000000ull);
     }
-    if (!head_ok) return;
 
     // ---- normalised partial O (this warp's head, 8 columns) and lse ----
 #pragma unroll
@@ -332,7 +410,7 @@ __global__ void __launch_bounds__(256) splitkv_decode_rows_kernel(const DecodeAr
 template <int KT, int VT>
 int launch_rows_t(skv_handle *h, const DecodeArgs &a, cudaStream_t st)
 {
-    const int smem = kRStages * kRRows * static_cast<int>(a.k_row_bytes + a.v_row_bytes);
+    const int smem = kRStages * static_cast<int>(rows_stage_bytes(a.k_row_bytes, a.v_row_bytes));
     static int attr_smem = 0;   // per process: the attribute is per function
     if (smem > attr_smem) {
         cudaError_t e = cudaFuncSetAttribute(splitkv_decode_rows_kernel<KT, VT>,
@@ -372,7 +450,7 @@ bool decode_rows_eligible(const skv_shape *sh, const void *k, const void *v, con
 {
     const bool qk = sh->k_type == SKV_Q8_0 || sh->k_type == SKV_Q4_0;
     const bool qv = sh->v_type == SKV_Q8_0 || sh->v_type == SKV_Q4_0;
-    const int64_t smem = static_cast<int64_t>(kRStages) * kRRows * (sh->k_row_bytes + sh->v_row_bytes);
+    const int64_t smem = kRStages * rows_stage_bytes(sh->k_row_bytes, sh->v_row_bytes);
     return qk && qv && sh->D == kRD && mask == nullptr && sh->Hk >= 1 && sh->Hk <= 8 && sh->k_row_bytes % 16 == 0 &&
            sh->v_row_bytes % 16 == 0 && (reinterpret_cast<uintptr_t>(k) % 16) == 0 &&
            (reinterpret_cast<uintptr_t>(v) % 16) == 0 && smem <= 200 * 1024;
@@ -380,7 +458,7 @@ bool decode_rows_eligible(const skv_shape *sh, const void *k, const void *v, con
 
 int decode_rows_ctas_per_sm(const skv_shape *sh)
 {
-    const int smem = kRStages * kRRows * static_cast<int>(sh->k_row_bytes + sh->v_row_bytes);
+    const int smem = kRStages * static_cast<int>(rows_stage_bytes(sh->k_row_bytes, sh->v_row_bytes));
     const int kt = sh->k_type, vt = sh->v_type, th = 32 * sh->Hk;
     if (kt == SKV_Q8_0 && vt == SKV_Q8_0) return rows_ctas_t<SKV_Q8_0, SKV_Q8_0>(smem, th);
     if (kt == SKV_Q8_0 && vt == SKV_Q4_0) return rows_ctas_t<SKV_Q8_0, SKV_Q4_0>(smem, th);
