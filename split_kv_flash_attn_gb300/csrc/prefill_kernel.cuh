@@ -20,10 +20,13 @@
 //                                        B operand in MN-major layout.
 //   softmax (0-7) : two threads per query row (TMEM lane), 64 key columns
 //                   each: tcgen05.ld S_j, causal / padding mask, online
-//                   softmax in log2 units, P_j (fp16) to shared memory.  O is
+//                   softmax in log2 units, P_j (fp16) back into tensor memory
+//                   over S_j's columns, where the PV MMA reads it as its A
+//                   operand; S_j's buffer is reused once that PV is done.  O is
 //                   rescaled in TMEM only when a row maximum grows by more than
 //                   2^8 (the stale maximum stays the reference otherwise,
-//                   exactly as in the plain online softmax with another shift).
+//                   exactly as in the plain online softmax with another shift),
+//                   so the softmax waits for the previous PV only then.
 //
 // The per-split result (O normalised, lse) is merged across splits by the
 // last CTA of each (sequence, KV head, query tile), as in the decode kernel.
@@ -51,8 +54,7 @@ constexpr int kHalfTile = kTileBytes / 2;       // one 64-column swizzle block
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kTileBytes;       // 2 stages (quantised keys: hi and lo of one stage)
 constexpr int kOffV = kOffK + 2 * kTileBytes;   // 2 stages
-constexpr int kOffP = kOffV + 2 * kTileBytes;
-constexpr int kOffBar = kOffP + kTileBytes;
+constexpr int kOffBar = kOffV + 2 * kTileBytes;   // (P lives in tensor memory, over its S buffer)
 constexpr int kSmem = kOffBar + 256 + 1024;     // + barriers + alignment slack
 constexpr uint32_t kIdescS = tc::idesc_f16(kPM, kPN, false);
 constexpr uint32_t kIdescPV = tc::idesc_f16(kPM, kPD, true);
@@ -70,8 +72,10 @@ struct Cfg {
 };
 
 // barrier slots (8 bytes each) inside the barrier area
+// (P full is per S buffer: the softmax of tile j+1 may publish P before the MMA
+// warp has seen tile j's, and one barrier would then run two phases ahead.)
 enum { B_KFULL = 0, B_KEMPTY = 2, B_VFULL = 4, B_VEMPTY = 6, B_QFULL = 8, B_SFULL = 9, B_SFREE = 11, B_PFULL = 13,
-       B_PVDONE = 14, B_COUNT = 15 };
+       B_PVDONE = 15, B_COUNT = 16 };
 
 struct PrefillArgs {
     const __half *q;          // [S][nq][H][D]
@@ -279,10 +283,11 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
             tc::mbar_init(bar(B_VFULL + i), C::kFullCount);
             tc::mbar_init(bar(B_VEMPTY + i), 1);
             tc::mbar_init(bar(B_SFULL + i), 1);
-            tc::mbar_init(bar(B_SFREE + i), kSoftmaxThreads);
+            tc::mbar_init(bar(B_SFREE + i), 1);     // S buffer free: PV of its tile has read P
         }
         tc::mbar_init(bar(B_QFULL), kSoftmaxThreads);
         tc::mbar_init(bar(B_PFULL), kSoftmaxThreads);
+        tc::mbar_init(bar(B_PFULL + 1), kSoftmaxThreads);
         tc::mbar_init(bar(B_PVDONE), 1);
         tc::fence_barrier_init();
         if (MODE == 0) {
@@ -421,27 +426,33 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                 if (jj >= 1) {
                     const int j = jj - 1;
                     const int b = j & 1;
-                    if (!wait(B_PFULL, j & 1)) break;
+                    if (!wait(B_PFULL + b, (j >> 1) & 1)) break;
                     if (!wait(B_VFULL + b, (j >> 1) & 1)) break;
                     tc::tc_fence_after();
                     const uint32_t d_o = tmem + 2 * kPN;
 #pragma unroll
                     for (int kk = 0; kk < kPN / 16; ++kk) {
-                        const uint32_t poff = (kk >> 2) * kHalfTile + (kk & 3) * 32;
-                        const uint64_t ad = tc::smem_desc(sbase + kOffP + poff, 16, 1024);
+                        // P of keys 16kk .. 16kk+15: fp16 pairs in columns (kk/4)*64 + (kk%4)*8
+                        // of the tile's S buffer
+                        const uint32_t a_t = tmem + static_cast<uint32_t>(b * kPN + (kk >> 2) * 64 + (kk & 3) * 8);
                         // V tile as B in MN-major layout: 16 keys = 2048 bytes per k-step;
                         // the second 64-wide d block is kHalfTile away (leading offset),
                         // 8-key row groups are 1024 bytes apart (stride offset).
                         const uint64_t bd = tc::smem_desc(sbase + kOffV + b * kTileBytes + kk * 2048, kHalfTile, 1024);
-                        tc::mma_f16(d_o, ad, bd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                        tc::mma_f16_ts(d_o, a_t, bd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
                     }
                     tc::mma_commit(bar(B_PVDONE));
                     tc::mma_commit(bar(B_VEMPTY + b));
+                    tc::mma_commit(bar(B_SFREE + b));
                     ++committed_pv;
                 }
             }
             if (*reinterpret_cast<volatile int *>(&s_abort) && committed_pv > 0)
-                tc::mbar_wait(bar(B_PVDONE), (committed_pv - 1) & 1, nullptr, 100000000ull);   // drain issued MMAs
+            {   // drain issued MMAs (the last two PV phases, in order)
+                if (committed_pv >= 2)
+                    tc::mbar_wait(bar(B_PVDONE), (committed_pv - 2) & 1, nullptr, 100000000ull);
+                tc::mbar_wait(bar(B_PVDONE), (committed_pv - 1) & 1, nullptr, 100000000ull);
+            }
         }
     } else {
         // ---------------- softmax warps (two threads per query row) -----------
@@ -487,8 +498,6 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
             for (int c = 0; c < NC / 32; ++c)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(sr[c][i]);
-            tc::tc_fence_before();
-            tc::mbar_arrive(bar(B_SFREE + b));
 
             const int64_t pos0 = a.key_pos0 + a.logical0 + key0;
             const int64_t lim_pos = static_cast<int64_t>(pos_row) - pos0;   // columns > lim_pos are masked
@@ -534,36 +543,37 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
             }
             l_run = l_run * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));   // this half's columns
             m_ref = ref;
-            // P buffer and O are free once PV of the previous tile is done.
-            if (j > 0) {
+            // O may be rescaled only once PV of the previous tile is done; the
+            // wait is taken only when this warp rescales (the reference
+            // maximum moves rarely).
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
                 __all_sync(0xffffffffu, wait(B_PVDONE, (j - 1) & 1));
                 tc::tc_fence_after();
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-                    for (int c = 0; c < NC / 32; ++c) {
-                        uint32_t rr[32];
-                        tc::tmem_ld32(lane_base + 2 * kPN + hf * NC + c * 32, rr);
-                        tc::tmem_wait_ld(rr);
-                        float v[32];
+                for (int c = 0; c < NC / 32; ++c) {
+                    uint32_t rr[32];
+                    tc::tmem_ld32(lane_base + 2 * kPN + hf * NC + c * 32, rr);
+                    tc::tmem_wait_ld(rr);
+                    float v[32];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(rr[i]) * alpha;
-                        tc::tmem_st32(lane_base + 2 * kPN + hf * NC + c * 32, v);
-                    }
-                    tc::tmem_wait_st();
+                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(rr[i]) * alpha;
+                    tc::tmem_st32(lane_base + 2 * kPN + hf * NC + c * 32, v);
                 }
             }
-            // this half's 64 keys are exactly one 64-key swizzle block of P
-#pragma unroll
-            for (int cc = 0; cc < 8; ++cc)
-                *reinterpret_cast<uint4 *>(sm + kOffP + hf * kHalfTile + m * 128 + ((cc ^ (m & 7)) << 4)) =
-                    make_uint4(ph[cc * 4], ph[cc * 4 + 1], ph[cc * 4 + 2], ph[cc * 4 + 3]);
-            tc::fence_proxy_async_smem();
+            // P (fp16 pairs) over the first 32 columns of this half's S columns:
+            // this thread already read them, and its partner reads only its own
+            tc::tmem_st32u(lane_base + b * kPN + hf * NC, ph);
+            tc::tmem_wait_st();
             tc::tc_fence_before();
-            tc::mbar_arrive(bar(B_PFULL));
+            tc::mbar_arrive(bar(B_PFULL + b));
         }
         // ---------------- epilogue: O / l, lse -------------------------------
         float ov[NC];
         bool have = n_tiles > 0 && !*reinterpret_cast<volatile int *>(&s_abort);
+        // PV completions are tracked by parity, so wait for the last two in
+        // order: a wait on the last alone could alias a phase two ahead (the
+        // softmax waits for a PV only when it rescales O).
+        if (have && n_tiles >= 2) have = wait(B_PVDONE, (n_tiles - 2) & 1);
         if (have) have = wait(B_PVDONE, (n_tiles - 1) & 1);
         have = __all_sync(0xffffffffu, have);
         if (have) {
