@@ -15,7 +15,9 @@
 //                   q8_0 / q4_0 rows are loaded, decoded to fp16(d*q) and
 //                   stored in the same layout.
 //   MMA warp      : S_j = Q K_j^T        tcgen05.mma kind::f16, M=N=128, into
-//                                        one of two TMEM S buffers (fp32);
+//                                        one of three TMEM S buffers (fp32),
+//                                        so S_j never waits for the PV that
+//                                        read the buffer last (tile j-3);
 //                   O  += P_j V_j        into the TMEM O accumulator; V is the
 //                                        B operand in MN-major layout.
 //   softmax (0-7) : two threads per query row (TMEM lane), 64 key columns
@@ -72,10 +74,18 @@ struct Cfg {
 };
 
 // barrier slots (8 bytes each) inside the barrier area
-// (P full is per S buffer: the softmax of tile j+1 may publish P before the MMA
-// warp has seen tile j's, and one barrier would then run two phases ahead.)
-enum { B_KFULL = 0, B_KEMPTY = 2, B_VFULL = 4, B_VEMPTY = 6, B_QFULL = 8, B_SFULL = 9, B_SFREE = 11, B_PFULL = 13,
-       B_PVDONE = 15, B_COUNT = 16 };
+// S buffers: kSBuf in tensor memory (P overlays its S), O after them.  S full,
+// S free (= the PV of the buffer's tile is done) and P full are per S buffer,
+// so that no waiter can be two phases away from the phase it waits for
+// (mbarrier waits are by phase parity): tile j's barriers are buffer j % kSBuf,
+// phase j / kSBuf.  A commit arrives once every earlier MMA of the issuing
+// thread is done, so "PV of tile j done" also means every earlier PV is.
+constexpr int kSBuf = 3;
+constexpr int kOCol = kSBuf * kPN;              // first TMEM column of O
+enum { B_KFULL = 0, B_KEMPTY = 2, B_VFULL = 4, B_VEMPTY = 6, B_QFULL = 8, B_SFULL = 9, B_SFREE = 9 + kSBuf,
+       B_PFULL = 9 + 2 * kSBuf, B_COUNT = 9 + 3 * kSBuf };
+static_assert(B_COUNT * 8 <= 256, "barrier area");
+static_assert(kOCol + kPD <= 512, "tensor memory columns");
 
 struct PrefillArgs {
     const __half *q;          // [S][nq][H][D]
@@ -282,13 +292,13 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
             tc::mbar_init(bar(B_KEMPTY + i), 1);
             tc::mbar_init(bar(B_VFULL + i), C::kFullCount);
             tc::mbar_init(bar(B_VEMPTY + i), 1);
+        }
+        for (int i = 0; i < kSBuf; ++i) {
             tc::mbar_init(bar(B_SFULL + i), 1);
             tc::mbar_init(bar(B_SFREE + i), 1);     // S buffer free: PV of its tile has read P
+            tc::mbar_init(bar(B_PFULL + i), kSoftmaxThreads);
         }
         tc::mbar_init(bar(B_QFULL), kSoftmaxThreads);
-        tc::mbar_init(bar(B_PFULL), kSoftmaxThreads);
-        tc::mbar_init(bar(B_PFULL + 1), kSoftmaxThreads);
-        tc::mbar_init(bar(B_PVDONE), 1);
         tc::fence_barrier_init();
         if (MODE == 0) {
             tc::prefetch_tmap(&tmap_k);
@@ -327,29 +337,28 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
     if (warp >= kSoftmaxWarps && warp < C::kMmaWarp) {
         if constexpr (MODE == 0) {
             // ---------------- TMA producer --------------------------------
-            if (lane == 0) {
-                int k_issued = 0, v_issued = 0;
+            // Lane 0 streams K tiles and lane 1 V tiles, each waiting only for
+            // its own ring slot: a K load never waits for a PV to finish.
+            if (lane < 2) {
+                const bool is_v = lane == 1;
+                const int b_empty = is_v ? B_VEMPTY : B_KEMPTY, b_full = is_v ? B_VFULL : B_KFULL;
+                const uint32_t off = is_v ? kOffV : kOffK;
+                const CUtensorMap *map = is_v ? &tmap_v : &tmap_k;
+                int issued = 0;
                 for (int j = 0; j < n_tiles; ++j) {
                     const int b = j & 1;
                     const int y = static_cast<int>(a.row0 + j_lo + static_cast<int64_t>(j) * kPN);
                     const int x = kh * kPD;
-                    if (j >= 2 && !wait(B_KEMPTY + b, ((j >> 1) - 1) & 1)) break;
-                    tc::mbar_expect_tx(bar(B_KFULL + b), kTileBytes);
-                    tc::tma_load_2d(sbase + kOffK + b * kTileBytes, &tmap_k, x, y, bar(B_KFULL + b));
-                    tc::tma_load_2d(sbase + kOffK + b * kTileBytes + kHalfTile, &tmap_k, x + 64, y, bar(B_KFULL + b));
-                    ++k_issued;
-                    if (j >= 2 && !wait(B_VEMPTY + b, ((j >> 1) - 1) & 1)) break;
-                    tc::mbar_expect_tx(bar(B_VFULL + b), kTileBytes);
-                    tc::tma_load_2d(sbase + kOffV + b * kTileBytes, &tmap_v, x, y, bar(B_VFULL + b));
-                    tc::tma_load_2d(sbase + kOffV + b * kTileBytes + kHalfTile, &tmap_v, x + 64, y, bar(B_VFULL + b));
-                    ++v_issued;
+                    if (j >= 2 && !wait(b_empty + b, ((j >> 1) - 1) & 1)) break;
+                    tc::mbar_expect_tx(bar(b_full + b), kTileBytes);
+                    tc::tma_load_2d(sbase + off + b * kTileBytes, map, x, y, bar(b_full + b));
+                    tc::tma_load_2d(sbase + off + b * kTileBytes + kHalfTile, map, x + 64, y, bar(b_full + b));
+                    ++issued;
                 }
                 if (*reinterpret_cast<volatile int *>(&s_abort)) {
                     // drain: every issued load must land before the CTA exits
-                    for (int j = (k_issued > 2 ? k_issued - 2 : 0); j < k_issued; ++j)
-                        tc::mbar_wait(bar(B_KFULL + (j & 1)), (j >> 1) & 1, nullptr, 100000000ull);
-                    for (int j = (v_issued > 2 ? v_issued - 2 : 0); j < v_issued; ++j)
-                        tc::mbar_wait(bar(B_VFULL + (j & 1)), (j >> 1) & 1, nullptr, 100000000ull);
+                    for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j)
+                        tc::mbar_wait(bar(b_full + (j & 1)), (j >> 1) & 1, nullptr, 100000000ull);
                 }
             }
         } else {
@@ -401,15 +410,16 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
         if (lane == 0 && n_tiles > 0) {
             bool ok = wait(B_QFULL, 0);
             tc::tc_fence_after();
-            int committed_pv = 0;
+            int committed_pv = 0;                   // PVs issued (tiles 0 .. committed_pv-1)
             for (int jj = 0; ok && jj <= n_tiles; ++jj) {
                 if (jj < n_tiles) {
                     const int b = jj & 1;
                     const int kb = KLO ? 0 : b;
+                    const int sb = jj % kSBuf;
                     if (!wait(B_KFULL + kb, KLO ? (jj & 1) : ((jj >> 1) & 1))) break;
-                    if (jj >= 2 && !wait(B_SFREE + b, ((jj >> 1) - 1) & 1)) break;
+                    if (jj >= kSBuf && !wait(B_SFREE + sb, ((jj / kSBuf) - 1) & 1)) break;
                     tc::tc_fence_after();
-                    const uint32_t d_s = tmem + static_cast<uint32_t>(b * kPN);
+                    const uint32_t d_s = tmem + static_cast<uint32_t>(sb * kPN);
                     constexpr int KSTEPS = (KLO ? 2 : 1) * kPD / 16;   // hi then lo
 #pragma unroll
                     for (int ks = 0; ks < KSTEPS; ++ks) {
@@ -420,38 +430,37 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                             sbase + kOffK + (KLO ? (ks / (kPD / 16)) : b) * kTileBytes + off, 16, 1024);
                         tc::mma_f16(d_s, ad, bd, kIdescS, ks > 0);
                     }
-                    tc::mma_commit(bar(B_SFULL + b));
+                    tc::mma_commit(bar(B_SFULL + sb));
                     tc::mma_commit(bar(B_KEMPTY + kb));
                 }
                 if (jj >= 1) {
                     const int j = jj - 1;
                     const int b = j & 1;
-                    if (!wait(B_PFULL + b, (j >> 1) & 1)) break;
+                    const int sb = j % kSBuf;
+                    if (!wait(B_PFULL + sb, (j / kSBuf) & 1)) break;
                     if (!wait(B_VFULL + b, (j >> 1) & 1)) break;
                     tc::tc_fence_after();
-                    const uint32_t d_o = tmem + 2 * kPN;
+                    const uint32_t d_o = tmem + kOCol;
 #pragma unroll
                     for (int kk = 0; kk < kPN / 16; ++kk) {
                         // P of keys 16kk .. 16kk+15: fp16 pairs in columns (kk/4)*64 + (kk%4)*8
                         // of the tile's S buffer
-                        const uint32_t a_t = tmem + static_cast<uint32_t>(b * kPN + (kk >> 2) * 64 + (kk & 3) * 8);
+                        const uint32_t a_t = tmem + static_cast<uint32_t>(sb * kPN + (kk >> 2) * 64 + (kk & 3) * 8);
                         // V tile as B in MN-major layout: 16 keys = 2048 bytes per k-step;
                         // the second 64-wide d block is kHalfTile away (leading offset),
                         // 8-key row groups are 1024 bytes apart (stride offset).
                         const uint64_t bd = tc::smem_desc(sbase + kOffV + b * kTileBytes + kk * 2048, kHalfTile, 1024);
                         tc::mma_f16_ts(d_o, a_t, bd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
                     }
-                    tc::mma_commit(bar(B_PVDONE));
                     tc::mma_commit(bar(B_VEMPTY + b));
-                    tc::mma_commit(bar(B_SFREE + b));
+                    tc::mma_commit(bar(B_SFREE + sb));
                     ++committed_pv;
                 }
             }
             if (*reinterpret_cast<volatile int *>(&s_abort) && committed_pv > 0)
-            {   // drain issued MMAs (the last two PV phases, in order)
-                if (committed_pv >= 2)
-                    tc::mbar_wait(bar(B_PVDONE), (committed_pv - 2) & 1, nullptr, 100000000ull);
-                tc::mbar_wait(bar(B_PVDONE), (committed_pv - 1) & 1, nullptr, 100000000ull);
+            {   // drain issued MMAs: the last PV's commit covers every earlier one
+                const int jl = committed_pv - 1;
+                tc::mbar_wait(bar(B_SFREE + jl % kSBuf), (jl / kSBuf) & 1, nullptr, 100000000ull);
             }
         }
     } else {
@@ -476,7 +485,8 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
         // through to its exit (its outputs are then invalid and the status
         // word says so).
         for (int j = 0; j < n_tiles; ++j) {
-            const int b = j & 1;
+            const int b = j & 1;                        // slot of the row-maximum exchange
+            const int sb = j % kSBuf;                   // S buffer of this tile
             const int64_t key0 = j_lo + static_cast<int64_t>(j) * kPN + hf * NC;   // local index of column 0
             // Padding entries of a row list: one bit per column of this half
             // (entries past the split count as present; lim_end masks them).
@@ -486,11 +496,11 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                 vm0 = __ballot_sync(0xffffffffu, ka >= j_hi || __ldg(lrow + ka) >= 0);
                 vm1 = __ballot_sync(0xffffffffu, kb >= j_hi || __ldg(lrow + kb) >= 0);
             }
-            __all_sync(0xffffffffu, wait(B_SFULL + b, (j >> 1) & 1));
+            __all_sync(0xffffffffu, wait(B_SFULL + sb, (j / kSBuf) & 1));
             tc::tc_fence_after();
             uint32_t sr[NC / 32][32];
 #pragma unroll
-            for (int c = 0; c < NC / 32; ++c) tc::tmem_ld32(lane_base + b * kPN + hf * NC + c * 32, sr[c]);
+            for (int c = 0; c < NC / 32; ++c) tc::tmem_ld32(lane_base + sb * kPN + hf * NC + c * 32, sr[c]);
 #pragma unroll
             for (int c = 0; c < NC / 32; ++c) tc::tmem_wait_ld(sr[c]);
             float x[NC];
@@ -547,40 +557,36 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
             // wait is taken only when this warp rescales (the reference
             // maximum moves rarely).
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                __all_sync(0xffffffffu, wait(B_PVDONE, (j - 1) & 1));
+                __all_sync(0xffffffffu, wait(B_SFREE + (j - 1) % kSBuf, ((j - 1) / kSBuf) & 1));
                 tc::tc_fence_after();
 #pragma unroll
                 for (int c = 0; c < NC / 32; ++c) {
                     uint32_t rr[32];
-                    tc::tmem_ld32(lane_base + 2 * kPN + hf * NC + c * 32, rr);
+                    tc::tmem_ld32(lane_base + kOCol + hf * NC + c * 32, rr);
                     tc::tmem_wait_ld(rr);
                     float v[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(rr[i]) * alpha;
-                    tc::tmem_st32(lane_base + 2 * kPN + hf * NC + c * 32, v);
+                    tc::tmem_st32(lane_base + kOCol + hf * NC + c * 32, v);
                 }
             }
             // P (fp16 pairs) over the first 32 columns of this half's S columns:
             // this thread already read them, and its partner reads only its own
-            tc::tmem_st32u(lane_base + b * kPN + hf * NC, ph);
+            tc::tmem_st32u(lane_base + sb * kPN + hf * NC, ph);
             tc::tmem_wait_st();
             tc::tc_fence_before();
-            tc::mbar_arrive(bar(B_PFULL + b));
+            tc::mbar_arrive(bar(B_PFULL + sb));
         }
         // ---------------- epilogue: O / l, lse -------------------------------
         float ov[NC];
         bool have = n_tiles > 0 && !*reinterpret_cast<volatile int *>(&s_abort);
-        // PV completions are tracked by parity, so wait for the last two in
-        // order: a wait on the last alone could alias a phase two ahead (the
-        // softmax waits for a PV only when it rescales O).
-        if (have && n_tiles >= 2) have = wait(B_PVDONE, (n_tiles - 2) & 1);
-        if (have) have = wait(B_PVDONE, (n_tiles - 1) & 1);
+        if (have) have = wait(B_SFREE + (n_tiles - 1) % kSBuf, ((n_tiles - 1) / kSBuf) & 1);   // the last PV
         have = __all_sync(0xffffffffu, have);
         if (have) {
             tc::tc_fence_after();
             uint32_t orr[NC / 32][32];
 #pragma unroll
-            for (int c = 0; c < NC / 32; ++c) tc::tmem_ld32(lane_base + 2 * kPN + hf * NC + c * 32, orr[c]);
+            for (int c = 0; c < NC / 32; ++c) tc::tmem_ld32(lane_base + kOCol + hf * NC + c * 32, orr[c]);
 #pragma unroll
             for (int c = 0; c < NC / 32; ++c) tc::tmem_wait_ld(orr[c]);
 #pragma unroll
