@@ -82,8 +82,10 @@ struct Cfg {
 // thread is done, so "PV of tile j done" also means every earlier PV is.
 constexpr int kSBuf = 3;
 constexpr int kOCol = kSBuf * kPN;              // first TMEM column of O
+// (M full: row-list mode, a tile's padding mask is in shared memory; 4 slots,
+// tile j in slot j % 4.)
 enum { B_KFULL = 0, B_KEMPTY = 2, B_VFULL = 4, B_VEMPTY = 6, B_QFULL = 8, B_SFULL = 9, B_SFREE = 9 + kSBuf,
-       B_PFULL = 9 + 2 * kSBuf, B_COUNT = 9 + 3 * kSBuf };
+       B_PFULL = 9 + 2 * kSBuf, B_MFULL = 9 + 3 * kSBuf, B_COUNT = 13 + 3 * kSBuf };
 static_assert(B_COUNT * 8 <= 256, "barrier area");
 static_assert(kOCol + kPD <= 512, "tensor memory columns");
 
@@ -251,6 +253,8 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
     // [slot][column half][row]: partial row maxima by tile parity (slots 0, 1),
     // then the halves' row sums (slot 2, so that no partner read is pending)
     __shared__ float s_pair[3][2][kPM];
+    // row-list mode: key-present bits of a tile (word w: keys 32w .. 32w+31), 4 slots
+    __shared__ uint32_t s_vmask[4][kPN / 32];
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -299,6 +303,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
             tc::mbar_init(bar(B_PFULL + i), kSoftmaxThreads);
         }
         tc::mbar_init(bar(B_QFULL), kSoftmaxThreads);
+        for (int i = 0; i < 4; ++i) tc::mbar_init(bar(B_MFULL + i), C::kProducerWarps * 32);
         tc::fence_barrier_init();
         if (MODE == 0) {
             tc::prefetch_tmap(&tmap_k);
@@ -363,37 +368,69 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
             }
         } else {
             // ---------------- software producers: each thread two key rows ------
-            // K_j is published (KFULL) only after V_j's stage was found free, so
-            // the wait order is KEMPTY, VEMPTY; VEMPTY(j) needs PV(j-2), which the
-            // MMA warp issues before it needs K_j: no cycle.
+            // No wait may depend on a tile the producers have not published yet.
             constexpr int NPT = C::kProducerWarps * 32;      // producer threads
             constexpr int RPT = kPN / NPT;                   // rows per thread
             const int r0 = tid - kSoftmaxThreads;
             constexpr int SEGK = KT == SKV_F16 ? 256 : (KT == SKV_Q8_0 ? 136 : 72);
             constexpr int SEGV = VT == SKV_F16 ? 256 : (VT == SKV_Q8_0 ? 136 : 72);
-            for (int j = 0; j < n_tiles; ++j) {
-                const int b = j & 1;
-                const uint8_t *sk[RPT], *sv[RPT];
+            // Cache row of key row r0 + u*NPT of tile j (-1: padding or past the split);
+            // list entries are fetched one tile ahead.
+            auto tile_row = [&](int j, int u) -> int64_t {
+                const int64_t key = j_lo + static_cast<int64_t>(j) * kPN + r0 + u * NPT;
+                if (key >= j_hi) return -1;
+                return lrow ? static_cast<int64_t>(__ldg(lrow + key)) : a.row0 + key;
+            };
+            auto k_src = [&](int64_t row) {
+                return row >= 0 ? a.k + row * a.k_row_bytes + static_cast<int64_t>(kh) * SEGK : nullptr;
+            };
+            auto v_src = [&](int64_t row) {
+                return row >= 0 ? a.v + row * a.v_row_bytes + static_cast<int64_t>(kh) * SEGV : nullptr;
+            };
+            // Row-list mode: tile j's key-present bits (a list row, or past the
+            // split, masked there) to shared memory for the softmax.  Slot j % 4
+            // was last read by the softmax of tile j - 4, which is done once
+            // PV(j - 2) is (the V slot of tile j is free).
+            auto publish_mask = [&](int j, const int64_t (&rw)[RPT]) {
+                if (!lrow) return;
+                uint32_t present[RPT];
 #pragma unroll
                 for (int u = 0; u < RPT; ++u) {
                     const int64_t key = j_lo + static_cast<int64_t>(j) * kPN + r0 + u * NPT;
-                    int64_t row = -1;
-                    if (key < j_hi) row = lrow ? static_cast<int64_t>(__ldg(lrow + key)) : a.row0 + key;
-                    sk[u] = row >= 0 ? a.k + row * a.k_row_bytes + static_cast<int64_t>(kh) * SEGK : nullptr;
-                    sv[u] = row >= 0 ? a.v + row * a.v_row_bytes + static_cast<int64_t>(kh) * SEGV : nullptr;
+                    present[u] = __ballot_sync(0xffffffffu, rw[u] >= 0 || key >= j_hi);
                 }
+                if ((tid & 31) == 0) {
+#pragma unroll
+                    for (int u = 0; u < RPT; ++u) s_vmask[j & 3][(r0 + u * NPT) >> 5] = present[u];
+                }
+                __syncwarp();
+                tc::mbar_arrive(bar(B_MFULL + (j & 3)));
+            };
+            int64_t cur[RPT];
+#pragma unroll
+            for (int u = 0; u < RPT; ++u) cur[u] = n_tiles > 0 ? tile_row(0, u) : -1;
+            // One tile at a time: a tile's K and V copies are in flight together,
+            // and the next tile's list entries load while they land.
+            for (int j = 0; j < n_tiles; ++j) {
+                const int b = j & 1;
                 const int kb = KLO ? 0 : b;                      // K stage of this tile
-                if (KLO ? (j >= 1 && !wait(B_KEMPTY, (j - 1) & 1)) : (j >= 2 && !wait(B_KEMPTY + b, ((j >> 1) - 1) & 1)))
-                    break;
+                int64_t nxt[RPT];
+#pragma unroll
+                for (int u = 0; u < RPT; ++u) nxt[u] = j + 1 < n_tiles ? tile_row(j + 1, u) : -1;
+                // (waits are made warp-uniform: the loop holds warp collectives)
+                const bool k_ok = KLO ? (j < 1 || wait(B_KEMPTY, (j - 1) & 1))
+                                      : (j < 2 || wait(B_KEMPTY + b, ((j >> 1) - 1) & 1));
+                if (!__all_sync(0xffffffffu, k_ok)) break;
 #pragma unroll
                 for (int u = 0; u < RPT; ++u)
-                    produce_row<KT, KLO>(sk[u], a.k, sm + kOffK + kb * kTileBytes, sbase + kOffK + kb * kTileBytes,
-                                         r0 + u * NPT, sm + kOffK + kTileBytes);
+                    produce_row<KT, KLO>(k_src(cur[u]), a.k, sm + kOffK + kb * kTileBytes,
+                                         sbase + kOffK + kb * kTileBytes, r0 + u * NPT, sm + kOffK + kTileBytes);
                 cp_async_commit();
-                if (j >= 2 && !wait(B_VEMPTY + b, ((j >> 1) - 1) & 1)) break;
+                if (!__all_sync(0xffffffffu, j < 2 || wait(B_VEMPTY + b, ((j >> 1) - 1) & 1))) break;
+                publish_mask(j, cur);
 #pragma unroll
                 for (int u = 0; u < RPT; ++u)
-                    produce_row<VT>(sv[u], a.v, sm + kOffV + b * kTileBytes, sbase + kOffV + b * kTileBytes,
+                    produce_row<VT>(v_src(cur[u]), a.v, sm + kOffV + b * kTileBytes, sbase + kOffV + b * kTileBytes,
                                     r0 + u * NPT);
                 cp_async_commit();
                 cp_async_wait<1>();
@@ -402,6 +439,8 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                 cp_async_wait<0>();
                 tc::fence_proxy_async_smem();
                 tc::mbar_arrive(bar(B_VFULL + b));
+#pragma unroll
+                for (int u = 0; u < RPT; ++u) cur[u] = nxt[u];
             }
             cp_async_wait<0>();
         }
@@ -488,15 +527,16 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
             const int b = j & 1;                        // slot of the row-maximum exchange
             const int sb = j % kSBuf;                   // S buffer of this tile
             const int64_t key0 = j_lo + static_cast<int64_t>(j) * kPN + hf * NC;   // local index of column 0
-            // Padding entries of a row list: one bit per column of this half
-            // (entries past the split count as present; lim_end masks them).
+            __all_sync(0xffffffffu, wait(B_SFULL + sb, (j / kSBuf) & 1));
+            // Padding entries of a row list: one bit per column of this half,
+            // published by the producers (entries past the split count as
+            // present; lim_end masks them).
             uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
             if (lrow) {
-                const int64_t ka = key0 + lane, kb = key0 + 32 + lane;
-                vm0 = __ballot_sync(0xffffffffu, ka >= j_hi || __ldg(lrow + ka) >= 0);
-                vm1 = __ballot_sync(0xffffffffu, kb >= j_hi || __ldg(lrow + kb) >= 0);
+                __all_sync(0xffffffffu, wait(B_MFULL + (j & 3), (j >> 2) & 1));
+                vm0 = s_vmask[j & 3][hf * 2];
+                vm1 = s_vmask[j & 3][hf * 2 + 1];
             }
-            __all_sync(0xffffffffu, wait(B_SFULL + sb, (j / kSBuf) & 1));
             tc::tc_fence_after();
             uint32_t sr[NC / 32][32];
 #pragma unroll
