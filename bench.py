@@ -323,7 +323,6 @@ def main():
     step_ms = max_over_ranks(step_ms)
     value = job_throughput(algo_bytes, world, step_ms)
     achieved = algo_bytes / (kern_ms * 1e-3) / 1e9
-    _, n_splits = skv.plan_splits(w.kv_rows.shape[1], w.S * w.Hk, h.sm_count(), 2, 64, 2048)
     launches_per_step = 1          # the split merge runs inside the decode kernel
 
     # ---- end to end through the C ABI with host buffers ---------------------

@@ -45,7 +45,7 @@ struct DecodeCfg {
     static constexpr int kWarps = 4;
     static constexpr int kThreads = 128;
 #ifndef SKV_DECODE_STAGES_F16
-#define SKV_DECODE_STAGES_F16 3
+#define SKV_DECODE_STAGES_F16 2     // 3 CTAs (12 warps) per SM beat a third stage at 2 CTAs
 #endif
 #ifndef SKV_DECODE_STAGES_QUANT
 #define SKV_DECODE_STAGES_QUANT 2   // 3 CTAs per SM: the code conversion needs the warps more than depth
