@@ -438,7 +438,7 @@ int skv_attn_partial(skv_handle *h, const skv_shape *shape, const void *q, const
     if (rows_k)
         rc = plan_splits_cost(n_local, units, h->sm_count, ctas, kRowsTile, 0, 1, &split_len, &n_splits);
     else
-        rc = skv_plan_splits(n_local, units, h->sm_count, ctas, kDecodeTile, kv_rows ? kMaxListSplit : 0, &split_len,
+        rc = skv_plan_splits(n_local, units, h->sm_count, ctas, kDecodeTile, 0, &split_len,
                              &n_splits);
     if (rc) return fail(h, rc, "split planning failed");
 

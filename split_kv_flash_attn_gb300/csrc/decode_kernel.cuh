@@ -8,11 +8,16 @@
 // every K/V byte is read once for all G heads.
 //
 // Per 64-key tile (one pipeline stage):
-//   * cp.async (16 B for fp16 rows, 8/4 B for q8_0/q4_0 segments) stages the
-//     tile's K and V head segments into shared memory, STAGES-1 tiles ahead.
+//   * each of the 4 warps owns 16 keys of the tile and stages their K and V
+//     head segments itself with cp.async (16 B for fp16 rows, 8/4 B for
+//     q8_0/q4_0 segments), STAGES-1 tiles ahead, so a warp waits only for its
+//     own copies and the warps never meet at a block barrier inside the loop.
 //     Rows come from a dense range, from a row list (padding rows read
-//     nothing: zero-filled), or from pages of a block cache.
-//   * each of the 4 warps takes 16 keys: S^T = K Q^T with mma.sync m16n8k16
+//     nothing: zero-filled), or from pages of a block cache.  Row-list
+//     entries stream through a small per-warp ring, fetched in the copy group
+//     that completes before the tile that needs them is issued, so a split
+//     may be any length.
+//   * each warp computes on its 16 keys: S^T = K Q^T with mma.sync m16n8k16
 //     (keys = M, query columns = N, head dim = K), fp16 in / fp32 accumulate.
 //     q8_0 / q4_0 codes are exact in fp16; the per-32-value scale of K is
 //     applied to each block's partial dot product in fp32, the scale of V is
@@ -56,6 +61,11 @@ struct DecodeCfg {
     static constexpr int stage_k = ((kTile * SEGK + 127) / 128) * 128;
     static constexpr int stage_v = ((kTile * SEGV + 127) / 128) * 128;
     static constexpr int stage_bytes = stage_k + stage_v;
+    // Row indices: the page table of a paged split (kMaxListSplit entries at
+    // most), or in list mode each warp's ring of kIdxRing tiles x 16 entries.
+    static constexpr int kIdxRing = 8;
+    static_assert(kIdxRing >= 2 * STAGES - 1, "the index ring must hold 2*STAGES-1 tiles");
+    static_assert(kWarps * kIdxRing * 16 <= kMaxListSplit, "index rings must fit the index buffer");
     static constexpr int idx_off = STAGES * stage_bytes;
     static constexpr int code_off = idx_off + kMaxListSplit * 4;
     static constexpr int code_k = Seg<KT, D>::quant ? 32 * D : 0;   // 16 keys x D halfs per warp
@@ -185,28 +195,36 @@ __global__ void __launch_bounds__(128) splitkv_decode_kernel(const DecodeArgs a)
     const int lg_pr = a.row_mode == ROWS_PAGED ? (31 - __clz(a.page_rows)) : 0;
     const int64_t page_lo = j_lo >> lg_pr;
 
-    // ---- row indices of this split (list / paged modes) -----------------
-    // Asynchronous 4-byte copies: every index request is in flight at once,
-    // so the split starts after one memory round trip, not one per index.
-    if (a.row_mode == ROWS_LIST) {
-        const int32_t *src = a.rows + list * a.rows_ld + a.rows_off + j_lo;
-        const int n = static_cast<int>(j_hi - j_lo);
-        for (int i = tid; i < n; i += C::kThreads) cp_async4(smem_addr(idx_s + i), src + i, 4);
-    } else if (a.row_mode == ROWS_PAGED) {
+    const int wrow = warp * 16;                  // this warp's 16 keys of every tile
+
+    // ---- page table of this split (paged mode) ----------------------------
+    // Asynchronous 4-byte copies: every request is in flight at once, so the
+    // split starts after one memory round trip, not one per entry.
+    if (a.row_mode == ROWS_PAGED) {
         const int32_t *src = a.rows + list * a.rows_ld + page_lo;
         const int n = j_hi > j_lo ? static_cast<int>(((j_hi - 1) >> lg_pr) - page_lo + 1) : 0;
         for (int i = tid; i < n; i += C::kThreads) cp_async4(smem_addr(idx_s + i), src + i, 4);
+        cp_async_commit();
+        cp_async_wait<0>();
+        __syncthreads();
     }
-    cp_async_commit();
-    cp_async_wait<0>();
-    __syncthreads();
+    // List mode: entries of tile t for this warp's keys sit in slot t % kIdxRing.
+    int32_t *ring = idx_s + warp * C::kIdxRing * 16;
+    const int32_t *list_src = a.row_mode == ROWS_LIST ? a.rows + list * a.rows_ld + a.rows_off : nullptr;
+    auto load_idx = [&](int t) {
+        if (a.row_mode != ROWS_LIST || lane >= 16) return;
+        const int64_t j = j_lo + static_cast<int64_t>(t) * kTile + wrow + lane;
+        if (j < j_hi) cp_async4(smem_addr(ring + (t & (C::kIdxRing - 1)) * 16 + lane), list_src + j, 4);
+    };
 
-    // Cache row (dense / list mode) or pool row (paged mode) of key j, or -1
-    // when the key is absent (past the split, or a padding entry).
-    auto key_row = [&](int64_t j) -> int64_t {
+    // Cache row (dense / list mode) or pool row (paged mode) of key wrow + rr
+    // of tile t, or -1 when the key is absent (past the split, or a padding
+    // entry).
+    auto key_row = [&](int t, int rr) -> int64_t {
+        const int64_t j = j_lo + static_cast<int64_t>(t) * kTile + wrow + rr;
         if (j >= j_hi) return -1;
         if (a.row_mode == ROWS_DENSE) return a.row0 + j;
-        if (a.row_mode == ROWS_LIST) return idx_s[j - j_lo];
+        if (a.row_mode == ROWS_LIST) return ring[(t & (C::kIdxRing - 1)) * 16 + rr];
         const int32_t pg = idx_s[(j >> lg_pr) - page_lo];
         return pg < 0 ? -1 : (static_cast<int64_t>(pg) << lg_pr) + (j & (a.page_rows - 1));
     };
@@ -217,21 +235,22 @@ __global__ void __launch_bounds__(128) splitkv_decode_kernel(const DecodeArgs a)
     const int64_t stride_k = paged ? SEGK : a.k_row_bytes;
     const int64_t stride_v = paged ? SEGV : a.v_row_bytes;
 
+    // Stage this warp's 16 keys of tile t into stage st.
     auto load_tile = [&](int t, int st) {
         uint8_t *sk_ = smem + st * C::stage_bytes;
         uint8_t *sv_ = sk_ + C::stage_k;
-        const int64_t jt = j_lo + static_cast<int64_t>(t) * kTile;
         if constexpr (!QK && !QV) {
-            // fp16: each thread owns one 16-byte column chunk of rows r, r+RPI,
-            // ...; one row lookup serves K and V.
+            // fp16: each lane owns one 16-byte column chunk of rows rr,
+            // rr+RPW, ...; one row lookup serves K and V.
             constexpr int CPR = D / 8;
-            constexpr int RPI = C::kThreads / CPR;
-            const int ch = tid % CPR;
+            constexpr int RPW = 32 / CPR;
+            const int ch = lane % CPR;
             const uint32_t dk = smem_addr(sk_), dv = smem_addr(sv_);
 #pragma unroll
-            for (int it = 0; it < kTile / RPI; ++it) {
-                const int r = tid / CPR + RPI * it;
-                const int64_t row = key_row(jt + r);
+            for (int it = 0; it < 16 / RPW; ++it) {
+                const int rr = lane / CPR + RPW * it;
+                const int r = wrow + rr;
+                const int64_t row = key_row(t, rr);
                 const bool ok = row >= 0;
                 const uint8_t *src_k = a.k + (ok ? row * stride_k + head_k + ch * 16 : 0);
                 const uint8_t *src_v = a.v + (ok ? row * stride_v + head_v + ch * 16 : 0);
@@ -241,15 +260,16 @@ __global__ void __launch_bounds__(128) splitkv_decode_kernel(const DecodeArgs a)
         } else {
             {
                 constexpr int CPR = SEGK / CHK;
-                constexpr int TOT = kTile * CPR;
+                constexpr int TOT = 16 * CPR;
                 const uint32_t dk = smem_addr(sk_);
 #pragma unroll
-                for (int it = 0; it < (TOT + C::kThreads - 1) / C::kThreads; ++it) {
-                    const int c = tid + it * C::kThreads;
-                    if (TOT % C::kThreads != 0 && c >= TOT) break;
-                    const int r = c / CPR;
-                    const int ch = c - r * CPR;
-                    const int64_t row = key_row(jt + r);
+                for (int it = 0; it < (TOT + 31) / 32; ++it) {
+                    const int c = lane + it * 32;
+                    if (TOT % 32 != 0 && c >= TOT) break;
+                    const int rr = c / CPR;
+                    const int r = wrow + rr;
+                    const int ch = c - rr * CPR;
+                    const int64_t row = key_row(t, rr);
                     const bool ok = row >= 0;
                     cp_async<CHK>(dk + static_cast<uint32_t>(r * SEGK + ch * CHK),
                                   a.k + (ok ? row * stride_k + head_k + ch * CHK : 0), ok);
@@ -257,15 +277,16 @@ __global__ void __launch_bounds__(128) splitkv_decode_kernel(const DecodeArgs a)
             }
             {
                 constexpr int CPR = SEGV / CHV;
-                constexpr int TOT = kTile * CPR;
+                constexpr int TOT = 16 * CPR;
                 const uint32_t dv = smem_addr(sv_);
 #pragma unroll
-                for (int it = 0; it < (TOT + C::kThreads - 1) / C::kThreads; ++it) {
-                    const int c = tid + it * C::kThreads;
-                    if (TOT % C::kThreads != 0 && c >= TOT) break;
-                    const int r = c / CPR;
-                    const int ch = c - r * CPR;
-                    const int64_t row = key_row(jt + r);
+                for (int it = 0; it < (TOT + 31) / 32; ++it) {
+                    const int c = lane + it * 32;
+                    if (TOT % 32 != 0 && c >= TOT) break;
+                    const int rr = c / CPR;
+                    const int r = wrow + rr;
+                    const int ch = c - rr * CPR;
+                    const int64_t row = key_row(t, rr);
                     const bool ok = row >= 0;
                     cp_async<CHV>(dv + static_cast<uint32_t>(r * SEGV + ch * CHV),
                                   a.v + (ok ? row * stride_v + head_v + ch * CHV : 0), ok);
@@ -319,28 +340,39 @@ __global__ void __launch_bounds__(128) splitkv_decode_kernel(const DecodeArgs a)
     const int n_tiles = static_cast<int>((j_hi - j_lo + kTile - 1) / kTile);
     constexpr float kLog2e = 1.4426950408889634f;
 
-    // ---- pipeline -------------------------------------------------------
+    // ---- pipeline (per warp) ---------------------------------------------
+    // Copy groups, in commit order: the list entries of tiles 0..STAGES-2;
+    // then for p < STAGES-1 tile p with the entries of tile p+STAGES-1; then
+    // at iteration i tile i+STAGES-1 with the entries of tile i+2*STAGES-2.
+    // Waiting at iteration i for all but the STAGES-2 newest groups completes
+    // tile i and the entries of every tile issued at iteration i, and the ring
+    // then holds tiles i .. i+2*STAGES-2 (2*STAGES-1 <= kIdxRing slots).
+    for (int p = 0; p < STAGES - 1; ++p) if (p < n_tiles) load_idx(p);
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncwarp();
 #pragma unroll
     for (int p = 0; p < STAGES - 1; ++p) {
         if (p < n_tiles) load_tile(p, p);
+        if (p + STAGES - 1 < n_tiles) load_idx(p + STAGES - 1);
         cp_async_commit();
     }
     for (int i = 0; i < n_tiles; ++i) {
         cp_async_wait<STAGES - 2>();
-        __syncthreads();
+        __syncwarp();
         {
             const int nt = i + STAGES - 1;
             if (nt < n_tiles) load_tile(nt, nt % STAGES);
+            if (i + 2 * STAGES - 2 < n_tiles) load_idx(i + 2 * STAGES - 2);
             cp_async_commit();
         }
         const int st = i % STAGES;
         const uint8_t *sk_ = smem + st * C::stage_bytes;
         const uint8_t *sv_ = sk_ + C::stage_k;
-        const int wrow = warp * 16;
         const int64_t jw = j_lo + static_cast<int64_t>(i) * kTile + wrow;   // first key of this warp
         const int r0 = lane >> 2;
-        const bool v0 = key_row(jw + r0) >= 0;
-        const bool v1 = key_row(jw + r0 + 8) >= 0;
+        const bool v0 = key_row(i, r0) >= 0;
+        const bool v1 = key_row(i, r0 + 8) >= 0;
         if (!__any_sync(0xffffffffu, v0 || v1)) continue;   // all 16 keys absent: nothing to do
 
         // S^T = K Q^T  (16 keys x 8 columns)

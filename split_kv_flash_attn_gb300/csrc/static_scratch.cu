@@ -118,7 +118,7 @@ extern "C" int skv_attn_partial_static(const skv_shape *shape, const void *q, co
     if (ctas <= 0) return SKV_EUNSUPPORTED;
     int64_t split_len = 0;
     int32_t n_splits = 0;
-    rc = skv_plan_splits(n_local, units, sm_count, ctas, kDecodeTile, kv_rows ? kMaxListSplit : 0, &split_len,
+    rc = skv_plan_splits(n_local, units, sm_count, ctas, kDecodeTile, 0, &split_len,
                          &n_splits);
     if (rc) return rc;
     if (n_splits > kMaxSplits) return SKV_EUNSUPPORTED;
