@@ -15,16 +15,21 @@
 //                   q8_0 / q4_0 rows are loaded, decoded to fp16(d*q) and
 //                   stored in the same layout.
 //   MMA warp      : S_j = Q K_j^T        tcgen05.mma kind::f16, M=N=128, into
-//                                        one of three TMEM S buffers (fp32),
-//                                        so S_j never waits for the PV that
-//                                        read the buffer last (tile j-3);
+//                                        one of two TMEM S buffers (fp32); Q
+//                                        is the A operand in tensor memory
+//                                        (placed there once by the softmax
+//                                        warps), which runs the MMA at twice
+//                                        the rate of an A read from shared
+//                                        memory;
 //                   O  += P_j V_j        into the TMEM O accumulator; V is the
 //                                        B operand in MN-major layout.
 //   softmax (0-7) : two threads per query row (TMEM lane), 64 key columns
 //                   each: tcgen05.ld S_j, causal / padding mask, online
-//                   softmax in log2 units, P_j (fp16) back into tensor memory
-//                   over S_j's columns, where the PV MMA reads it as its A
-//                   operand; S_j's buffer is reused once that PV is done.  O is
+//                   softmax in log2 units, P_j (fp16) into its own tensor-memory
+//                   columns, where the PV MMA reads it as its A operand.  An S
+//                   buffer is released as soon as the softmax warps have loaded
+//                   it, so S_{j+1} and S_{j+2} are computed while P_j is; P_j
+//                   is written once PV_{j-1} has read P_{j-1}.  O is
 //                   rescaled in TMEM only when a row maximum grows by more than
 //                   2^8 (the stale maximum stays the reference otherwise,
 //                   exactly as in the plain online softmax with another shift),
@@ -53,10 +58,9 @@ constexpr int kSoftmaxWarps = 8;   // two warps per query-row group (one per col
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
 constexpr int kTileBytes = kPN * kPD * 2;       // 32 KiB per K or V tile
 constexpr int kHalfTile = kTileBytes / 2;       // one 64-column swizzle block
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTileBytes;       // 2 stages (quantised keys: hi and lo of one stage)
+constexpr int kOffK = 0;                        // 2 stages (quantised keys: hi and lo of one stage)
 constexpr int kOffV = kOffK + 2 * kTileBytes;   // 2 stages
-constexpr int kOffBar = kOffV + 2 * kTileBytes;   // (P lives in tensor memory, over its S buffer)
+constexpr int kOffBar = kOffV + 2 * kTileBytes;   // (Q and P live in tensor memory)
 constexpr int kSmem = kOffBar + 256 + 1024;     // + barriers + alignment slack
 constexpr uint32_t kIdescS = tc::idesc_f16(kPM, kPN, false);
 constexpr uint32_t kIdescPV = tc::idesc_f16(kPM, kPD, true);
@@ -66,26 +70,33 @@ constexpr float kRescaleLog2 = 8.0f;            // rescale O only when the max g
 template <int MODE>
 struct Cfg {
     // 11 warps: at most 3 per SM sub-partition, so the softmax warps keep up
-    // to 168 registers (13 warps would cap them at 128)
-    static constexpr int kProducerWarps = MODE == 0 ? 1 : 2;
+    // to 168 registers (13 warps would cap them at 128).  MODE 0: one warp
+    // streams K tiles and one V tiles, so neither waits behind the other's
+    // ring slot (two lanes of one warp would share its issue).
+    static constexpr int kProducerWarps = 2;
     static constexpr int kMmaWarp = kSoftmaxWarps + kProducerWarps;
     static constexpr int kThreads = (kMmaWarp + 1) * 32;
     static constexpr uint32_t kFullCount = MODE == 0 ? 1 : kProducerWarps * 32;
 };
 
 // barrier slots (8 bytes each) inside the barrier area
-// S buffers: kSBuf in tensor memory (P overlays its S), O after them.  S full,
-// S free (= the PV of the buffer's tile is done) and P full are per S buffer,
-// so that no waiter can be two phases away from the phase it waits for
-// (mbarrier waits are by phase parity): tile j's barriers are buffer j % kSBuf,
-// phase j / kSBuf.  A commit arrives once every earlier MMA of the issuing
-// thread is done, so "PV of tile j done" also means every earlier PV is.
-constexpr int kSBuf = 3;
-constexpr int kOCol = kSBuf * kPN;              // first TMEM column of O
+// Tensor memory: kSBuf S buffers (fp32), then P (fp16 pairs), Q (fp16 pairs:
+// row m in lane m, dims 2c, 2c+1 in column c) and O (fp32).  S full (MMA
+// commit) and S free (the softmax warps have loaded S) are per S buffer: tile
+// j's are buffer j % kSBuf, phase j / kSBuf.  P full (softmax) and P free
+// (commit after PV: P read, O updated) are single barriers, phase j % 2; no
+// waiter can be two phases away from the phase it waits for (mbarrier waits
+// are by phase parity), because each side needs the other's next step before
+// it can complete another phase.  A commit arrives once every earlier MMA of
+// the issuing thread is done, so "PV of tile j done" means every earlier PV is.
+constexpr int kSBuf = 2;
+constexpr int kPCol = kSBuf * kPN;              // P: keys 2c, 2c+1 of the tile in column kPCol + c
+constexpr int kQCol = kPCol + kPN / 2;
+constexpr int kOCol = kQCol + kPD / 2;          // first TMEM column of O
 // (M full: row-list mode, a tile's padding mask is in shared memory; 4 slots,
 // tile j in slot j % 4.)
 enum { B_KFULL = 0, B_KEMPTY = 2, B_VFULL = 4, B_VEMPTY = 6, B_QFULL = 8, B_SFULL = 9, B_SFREE = 9 + kSBuf,
-       B_PFULL = 9 + 2 * kSBuf, B_MFULL = 9 + 3 * kSBuf, B_COUNT = 13 + 3 * kSBuf };
+       B_PFULL = 9 + 2 * kSBuf, B_PFREE = 10 + 2 * kSBuf, B_MFULL = 11 + 2 * kSBuf, B_COUNT = 15 + 2 * kSBuf };
 static_assert(B_COUNT * 8 <= 256, "barrier area");
 static_assert(kOCol + kPD <= 512, "tensor memory columns");
 
@@ -299,9 +310,10 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
         }
         for (int i = 0; i < kSBuf; ++i) {
             tc::mbar_init(bar(B_SFULL + i), 1);
-            tc::mbar_init(bar(B_SFREE + i), 1);     // S buffer free: PV of its tile has read P
-            tc::mbar_init(bar(B_PFULL + i), kSoftmaxThreads);
+            tc::mbar_init(bar(B_SFREE + i), kSoftmaxThreads);   // S buffer free: the softmax warps loaded it
         }
+        tc::mbar_init(bar(B_PFULL), kSoftmaxThreads);
+        tc::mbar_init(bar(B_PFREE), 1);                          // PV of the last P done
         tc::mbar_init(bar(B_QFULL), kSoftmaxThreads);
         for (int i = 0; i < 4; ++i) tc::mbar_init(bar(B_MFULL + i), C::kProducerWarps * 32);
         tc::fence_barrier_init();
@@ -342,10 +354,11 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
     if (warp >= kSoftmaxWarps && warp < C::kMmaWarp) {
         if constexpr (MODE == 0) {
             // ---------------- TMA producer --------------------------------
-            // Lane 0 streams K tiles and lane 1 V tiles, each waiting only for
-            // its own ring slot: a K load never waits for a PV to finish.
-            if (lane < 2) {
-                const bool is_v = lane == 1;
+            // The first producer warp streams K tiles and the second V tiles,
+            // each waiting only for its own ring slot: a K load never waits
+            // for a PV to finish.
+            if (lane == 0) {
+                const bool is_v = warp == kSoftmaxWarps + 1;
                 const int b_empty = is_v ? B_VEMPTY : B_KEMPTY, b_full = is_v ? B_VFULL : B_KFULL;
                 const uint32_t off = is_v ? kOffV : kOffK;
                 const CUtensorMap *map = is_v ? &tmap_v : &tmap_k;
@@ -449,7 +462,8 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
         if (lane == 0 && n_tiles > 0) {
             bool ok = wait(B_QFULL, 0);
             tc::tc_fence_after();
-            int committed_pv = 0;                   // PVs issued (tiles 0 .. committed_pv-1)
+            int last_bar = -1;                      // barrier and phase of the last commit
+            uint32_t last_par = 0;
             for (int jj = 0; ok && jj <= n_tiles; ++jj) {
                 if (jj < n_tiles) {
                     const int b = jj & 1;
@@ -464,27 +478,26 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                     for (int ks = 0; ks < KSTEPS; ++ks) {
                         const int kk = ks % (kPD / 16);
                         const uint32_t off = (kk >> 2) * kHalfTile + (kk & 3) * 32;
-                        const uint64_t ad = tc::smem_desc(sbase + kOffQ + off, 16, 1024);
                         const uint64_t bd = tc::smem_desc(
                             sbase + kOffK + (KLO ? (ks / (kPD / 16)) : b) * kTileBytes + off, 16, 1024);
-                        tc::mma_f16(d_s, ad, bd, kIdescS, ks > 0);
+                        tc::mma_f16_ts(d_s, tmem + static_cast<uint32_t>(kQCol + kk * 8), bd, kIdescS, ks > 0);
                     }
                     tc::mma_commit(bar(B_SFULL + sb));
                     tc::mma_commit(bar(B_KEMPTY + kb));
+                    last_bar = B_SFULL + sb;
+                    last_par = (jj / kSBuf) & 1;
                 }
                 if (jj >= 1) {
                     const int j = jj - 1;
                     const int b = j & 1;
-                    const int sb = j % kSBuf;
-                    if (!wait(B_PFULL + sb, (j / kSBuf) & 1)) break;
+                    if (!wait(B_PFULL, j & 1)) break;
                     if (!wait(B_VFULL + b, (j >> 1) & 1)) break;
                     tc::tc_fence_after();
                     const uint32_t d_o = tmem + kOCol;
 #pragma unroll
                     for (int kk = 0; kk < kPN / 16; ++kk) {
-                        // P of keys 16kk .. 16kk+15: fp16 pairs in columns (kk/4)*64 + (kk%4)*8
-                        // of the tile's S buffer
-                        const uint32_t a_t = tmem + static_cast<uint32_t>(sb * kPN + (kk >> 2) * 64 + (kk & 3) * 8);
+                        // P of keys 16kk .. 16kk+15: fp16 pairs in columns kPCol + 8kk ..
+                        const uint32_t a_t = tmem + static_cast<uint32_t>(kPCol + kk * 8);
                         // V tile as B in MN-major layout: 16 keys = 2048 bytes per k-step;
                         // the second 64-wide d block is kHalfTile away (leading offset),
                         // 8-key row groups are 1024 bytes apart (stride offset).
@@ -492,31 +505,38 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                         tc::mma_f16_ts(d_o, a_t, bd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
                     }
                     tc::mma_commit(bar(B_VEMPTY + b));
-                    tc::mma_commit(bar(B_SFREE + sb));
-                    ++committed_pv;
+                    tc::mma_commit(bar(B_PFREE));
+                    last_bar = B_PFREE;
+                    last_par = j & 1;
                 }
             }
-            if (*reinterpret_cast<volatile int *>(&s_abort) && committed_pv > 0)
-            {   // drain issued MMAs: the last PV's commit covers every earlier one
-                const int jl = committed_pv - 1;
-                tc::mbar_wait(bar(B_SFREE + jl % kSBuf), (jl / kSBuf) & 1, nullptr, 100000000ull);
+            if (*reinterpret_cast<volatile int *>(&s_abort) && last_bar >= 0)
+            {   // drain issued MMAs: the last commit covers every MMA issued before it
+                tc::mbar_wait(bar(last_bar), last_par, nullptr, 100000000ull);
             }
         }
     } else {
         // ---------------- softmax warps (two threads per query row) -----------
-        // Q: this thread's half of its row -> the 128-byte-swizzled K-major layout.
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        // Q: this thread's half of its row (dims hf*64 ..) -> tensor memory
+        // columns kQCol + hf*32 .., two fp16 per column.
         {
             const __half *qp = a.q + ((static_cast<int64_t>(s) * a.nq + (row_ok ? t_row : 0)) * a.H + kh * a.G +
                                       (m % a.G)) * kPD + hf * 64;
+            uint32_t qw[32];
 #pragma unroll
             for (int cc = 0; cc < 8; ++cc) {
-                uint4 v = row_ok ? *reinterpret_cast<const uint4 *>(qp + cc * 8) : make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4 *>(sm + kOffQ + hf * kHalfTile + m * 128 + ((cc ^ (m & 7)) << 4)) = v;
+                const uint4 v = row_ok ? *reinterpret_cast<const uint4 *>(qp + cc * 8) : make_uint4(0, 0, 0, 0);
+                qw[4 * cc] = v.x;
+                qw[4 * cc + 1] = v.y;
+                qw[4 * cc + 2] = v.z;
+                qw[4 * cc + 3] = v.w;
             }
-            tc::fence_proxy_async_smem();
+            tc::tmem_st32u(lane_base + kQCol + hf * 32, qw);
+            tc::tmem_wait_st();
+            tc::tc_fence_before();
             tc::mbar_arrive(bar(B_QFULL));
         }
-        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         constexpr int NC = kPN / 2;                 // columns per thread
         // No early exit from this loop: the two warps of a row pair meet on a
         // named barrier every tile, so both must run every iteration.  After
@@ -543,6 +563,8 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
             for (int c = 0; c < NC / 32; ++c) tc::tmem_ld32(lane_base + sb * kPN + hf * NC + c * 32, sr[c]);
 #pragma unroll
             for (int c = 0; c < NC / 32; ++c) tc::tmem_wait_ld(sr[c]);
+            tc::tc_fence_before();
+            tc::mbar_arrive(bar(B_SFREE + sb));           // the S buffer may take the next tile's S
             float x[NC];
 #pragma unroll
             for (int c = 0; c < NC / 32; ++c)
@@ -593,12 +615,14 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
             }
             l_run = l_run * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));   // this half's columns
             m_ref = ref;
-            // O may be rescaled only once PV of the previous tile is done; the
-            // wait is taken only when this warp rescales (the reference
-            // maximum moves rarely).
-            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                __all_sync(0xffffffffu, wait(B_SFREE + (j - 1) % kSBuf, ((j - 1) / kSBuf) & 1));
+            // P and O are free once PV of the previous tile is done (long
+            // done by now: it was issued when that tile's P was ready).  O is
+            // rescaled only when the reference maximum moved (rarely).
+            if (j > 0) {
+                __all_sync(0xffffffffu, wait(B_PFREE, (j - 1) & 1));
                 tc::tc_fence_after();
+            }
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
                 for (int c = 0; c < NC / 32; ++c) {
                     uint32_t rr[32];
@@ -610,17 +634,16 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                     tc::tmem_st32(lane_base + kOCol + hf * NC + c * 32, v);
                 }
             }
-            // P (fp16 pairs) over the first 32 columns of this half's S columns:
-            // this thread already read them, and its partner reads only its own
-            tc::tmem_st32u(lane_base + sb * kPN + hf * NC, ph);
+            // P (fp16 pairs): keys hf*64 + 2c, +1 in column kPCol + hf*32 + c
+            tc::tmem_st32u(lane_base + kPCol + hf * (NC / 2), ph);
             tc::tmem_wait_st();
             tc::tc_fence_before();
-            tc::mbar_arrive(bar(B_PFULL + sb));
+            tc::mbar_arrive(bar(B_PFULL));
         }
         // ---------------- epilogue: O / l, lse -------------------------------
         float ov[NC];
         bool have = n_tiles > 0 && !*reinterpret_cast<volatile int *>(&s_abort);
-        if (have) have = wait(B_SFREE + (n_tiles - 1) % kSBuf, ((n_tiles - 1) / kSBuf) & 1);   // the last PV
+        if (have) have = wait(B_PFREE, (n_tiles - 1) & 1);   // the last PV
         have = __all_sync(0xffffffffu, have);
         if (have) {
             tc::tc_fence_after();
