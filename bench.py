@@ -113,6 +113,24 @@ def run_profile_case(name: str) -> int:
     return 0
 
 
+def cpu_model() -> str:
+    """The host CPU's model line from /proc/cpuinfo (Arm parts give their
+    implementer and part numbers instead of a name)."""
+    try:
+        info = open("/proc/cpuinfo").read().splitlines()
+    except OSError:
+        return "unknown"
+    for key in ("model name", "Model", "Hardware"):
+        for line in info:
+            if line.split(":")[0].strip() == key and ":" in line:
+                return line.split(":", 1)[1].strip()
+    impl = [ln.split(":", 1)[1].strip() for ln in info if ln.startswith("CPU implementer")]
+    part = [ln.split(":", 1)[1].strip() for ln in info if ln.startswith("CPU part")]
+    if impl and part:
+        return f"arm implementer {impl[0]} part {part[0]}"
+    return "unknown"
+
+
 def dist_env():
     return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
             int(os.environ.get("LOCAL_RANK", 0)))
@@ -247,7 +265,8 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "S": 8, "H": 32, "Hk": 8, "D": 128, "n_cache": 262144,
                    "rows_per_seq": 32768},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample,
+                         "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
     return 0
@@ -375,7 +394,8 @@ def main():
             sec = time.perf_counter() - t0
             sb = int((w.kv_rows[0] >= 0).sum()) * w.Hk * w.D * 4
             cpu = {"value": sb / sec / 1e9, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
-                   "sample": f"sequence 0 of 8 (32 q heads x 32768 gathered rows, {sb} B), {sec:.2f} s"}
+                   "sample": f"sequence 0 of 8 (32 q heads x 32768 gathered rows, {sb} B), {sec:.2f} s",
+                   "cpu_model": cpu_model()}
         except Exception as exc:  # noqa: BLE001
             cpu = {"value": None, "unit": "GB/s", "cores": None, "kind": "oracle", "sample": repr(exc)[:200]}
 
@@ -479,10 +499,14 @@ def run_extras(torch, skv, wl, h, hbm_peak):
         torch.cuda.synchronize()
         h2d_gbs = reps * (tk + tv) / (e0.elapsed_time(e1) * 1e-3) / 1e9
         tail_gbs = tail_bytes / (call_ms * 1e-3) / 1e9
+        # the call can take no less than the longer of the window kernel and
+        # the tail's copy at the pinned H2D rate
+        bound_ms = max(win_ms, tail_bytes / (h2d_gbs * 1e9) * 1e3)
         out["long_context_window_tail"] = {
             "n_kv": w.extra["n_kv"], "wc": w.extra["wc"], "tile_rows": w.tile_rows, "tail_bytes": tail_bytes,
             "call_ms": call_ms, "tail_stream_GBps": tail_gbs, "pinned_h2d_GBps": h2d_gbs,
-            "frac_of_pinned_h2d": tail_gbs / h2d_gbs, "tokens_heads_per_s": w.H / (call_ms * 1e-3)}
+            "frac_of_pinned_h2d": tail_gbs / h2d_gbs, "bound_ms": bound_ms, "frac_of_bound": bound_ms / call_ms,
+            "tokens_heads_per_s": w.H / (call_ms * 1e-3)}
         del kw_, vw_, kt, vt, dst, src, srcv
     except Exception as exc:  # noqa: BLE001
         out["long_context_error"] = repr(exc)[:300]
@@ -491,7 +515,17 @@ def run_extras(torch, skv, wl, h, hbm_peak):
     except Exception as exc:  # noqa: BLE001
         out["prefill_error"] = repr(exc)[:300]
     try:
-        out["block_sparse"] = bench_block_sparse(torch, skv, wl, h, hbm_peak)
+        bs = bench_block_sparse(torch, skv, wl, h, hbm_peak)
+        h2d = out.get("long_context_window_tail", {}).get("pinned_h2d_GBps")
+        if h2d:
+            # hits read from HBM, misses cross the host link: serial and
+            # overlapped lower bounds on a warm call
+            miss_b = bs["warm_miss_pages_per_call"] * bs["page_bytes"]
+            hit_b = bs["call_bytes"] - miss_b
+            t_hit, t_miss = hit_b / (hbm_peak * 1e9) * 1e3, miss_b / (h2d * 1e9) * 1e3
+            bs.update({"bound_ms_serial": t_hit + t_miss, "bound_ms_overlapped": max(t_hit, t_miss),
+                       "frac_of_serial_bound": (t_hit + t_miss) / bs["warm_ms"]})
+        out["block_sparse"] = bs
     except Exception as exc:  # noqa: BLE001
         out["block_sparse_error"] = repr(exc)[:300]
     try:
@@ -780,7 +814,8 @@ def bench_block_sparse(torch, skv, wl, h, hbm_peak):
     warm_calls = st1["calls"] - st0["calls"]
     miss_pages_warm = (st1["misses"] - st0["misses"]) / max(1, warm_calls)
     c.close()
-    return {"call_bytes": call_bytes, "cold_ms": cold_ms, "warm_ms": warm_ms, "drift_ms": drift_ms,
+    return {"call_bytes": call_bytes, "page_bytes": page_bytes, "cold_ms": cold_ms, "warm_ms": warm_ms,
+            "drift_ms": drift_ms,
             "cold_misses": st0["last_misses"], "warm_hit_rate": hit_rate(st0, st1),
             "warm_miss_pages_per_call": miss_pages_warm,
             "warm_miss_GBps": miss_pages_warm * page_bytes / warm_ms / 1e6,
