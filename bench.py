@@ -552,7 +552,29 @@ def run_extras(torch, skv, wl, h, hbm_peak):
         e1.record(stream)
         torch.cuda.synchronize()
         us = e0.elapsed_time(e1) / n * 1e3
-        out["tiny_decode_window_tail"] = {"us_per_call": us, "tokens_heads_per_s": w.H / (us * 1e-6)}
+        # the same call captured once in a CUDA graph and replayed: what the
+        # device needs per call once the host's per-call API work is gone
+        cs = torch.cuda.Stream()
+        o_g = torch.empty((1, 1, w.H, w.D), dtype=torch.float32, device="cuda")
+        l_g = torch.empty((1, 1, w.H), dtype=torch.float32, device="cuda")
+        cs.wait_stream(stream)
+        with torch.cuda.stream(cs):
+            skv.attn_window_tail(h, q, kw_, vw_, kt, vt, Hk=w.Hk, tile_rows=w.tile_rows, o=o_g, lse=l_g, stream=cs)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cs, capture_error_mode="thread_local"):
+            skv.attn_window_tail(h, q, kw_, vw_, kt, vt, Hk=w.Hk, tile_rows=w.tile_rows, o=o_g, lse=l_g, stream=cs)
+        for _ in range(5):
+            g.replay()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(n):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        g_us = e0.elapsed_time(e1) / n * 1e3
+        out["tiny_decode_window_tail"] = {"us_per_call": us, "tokens_heads_per_s": w.H / (us * 1e-6),
+                                          "graph_replay_us_per_call": g_us}
     except Exception as exc:  # noqa: BLE001
         out["tiny_error"] = repr(exc)[:300]
     return out
