@@ -262,6 +262,15 @@ int skv_kv_dequant_q4_0(skv_handle *h, const void *blocks, int64_t n_values, flo
 int skv_gather_rows(skv_handle *h, const void *src, int64_t row_bytes, const int32_t *rows, int64_t n,
                     void *dst, void *stream);
 
+/* Failure-path self-test: one CTA waits, with the same bounded mbarrier wait
+ * the tensor-core kernels use for their pipeline barriers, on a barrier that
+ * nothing arrives on.  After budget_ns of wall-clock time (1e3 .. 1e9) the
+ * wait gives up and sets bit 0 of the handle's device status word, so the
+ * next skv_status returns SKV_ETIMEOUT; the context stays usable.  No fault,
+ * trap or unbounded wait is involved.  SKV_EINVAL for a budget outside the
+ * range. */
+int skv_selftest_wait_timeout(skv_handle *h, int64_t budget_ns, void *stream);
+
 /* ---- appending rows (write routing and quantise-on-append) ------------- */
 
 /* Write n new rows of one tensor (K or V) into a cell-major cache of two

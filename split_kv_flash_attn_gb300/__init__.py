@@ -329,6 +329,12 @@ def gather_rows(h: Handle, src, rows, *, row_bytes=None, out=None, stream=None):
     return out
 
 
+def selftest_wait_timeout(h: Handle, budget_ns: int = 5_000_000, stream=None):
+    """skv_selftest_wait_timeout: a bounded device-side wait that nothing
+    completes gives up after budget_ns and marks the handle's status word."""
+    h.check(_lib.lib().skv_selftest_wait_timeout(h.ptr, int(budget_ns), _stream(stream)))
+
+
 def kv_append(h: Handle, x, positions, dst0, dst1=None, *, type_=F16, n_rows0=None, n_rows1=None, row_bytes=None,
               stream=None):
     """Write x (fp32 [n][Hk][D], device) into a two-region cell-major cache:

@@ -25,7 +25,7 @@ EXPORTS = [
     "skv_attn_paged", "skv_bcache_create", "skv_bcache_destroy", "skv_bcache_reset", "skv_bcache_resolve",
     "skv_bcache_append", "skv_bcache_attn", "skv_bcache_stats", "skv_bcache_check", "skv_bcache_pool",
     "skv_bcache_create_ring", "skv_bcache_ring_restore", "skv_bcache_ring_attn",
-    "skv_attn_partial_static", "skv_plan_window", "skv_plan_tail_tile",
+    "skv_attn_partial_static", "skv_plan_window", "skv_plan_tail_tile", "skv_selftest_wait_timeout",
 ]
 
 
@@ -61,6 +61,7 @@ def _declare(lib):
         "skv_kv_dequant_q8_0": ([P, P, I64, P, P], ctypes.c_int),
         "skv_kv_dequant_q4_0": ([P, P, I64, P, P], ctypes.c_int),
         "skv_gather_rows": ([P, P, I64, P, I64, P, P], ctypes.c_int),
+        "skv_selftest_wait_timeout": ([P, I64, P], ctypes.c_int),
         "skv_kv_append": ([P, I32, I32, I32, I64, P, P, I32, P, I64, P, I64, P], ctypes.c_int),
         "skv_bcache_append": ([P, P, P, P, I32, P], ctypes.c_int),
         "skv_bcache_create_ring": ([P, I64, I32, I32, I32, I32, I32, P, P, ctypes.POINTER(P)], ctypes.c_int),
