@@ -11,8 +11,9 @@
 //                   thread issues TMA loads over a dense fp16 region.  MODE 1:
 //                   two warps, two key rows per thread, fetch the rows through
 //                   a row list (padding entries read nothing) or a dense range;
-//                   fp16 rows go straight to the swizzled tile by cp.async,
-//                   q8_0 / q4_0 rows are loaded, decoded to fp16(d*q) and
+//                   fp16 rows go straight to the swizzled tile by cp.async;
+//                   q8_0 / q4_0 segments are staged raw in shared memory by
+//                   cp.async one tile ahead, then decoded to fp16(d*q) and
 //                   stored in the same layout.
 //   MMA warp      : S_j = Q K_j^T        tcgen05.mma kind::f16, M=N=128, into
 //                                        one of two TMEM S buffers (fp32); Q
@@ -62,6 +63,17 @@ constexpr int kOffK = 0;                        // 2 stages (quantised keys: hi 
 constexpr int kOffV = kOffK + 2 * kTileBytes;   // 2 stages
 constexpr int kOffBar = kOffV + 2 * kTileBytes;   // (Q and P live in tensor memory)
 constexpr int kSmem = kOffBar + 256 + 1024;     // + barriers + alignment slack
+// Quantised instances also stage raw row segments (two tiles of K and V
+// segments) after the barriers, so that a tile's global loads are in flight
+// while the previous tile is decoded.
+constexpr int kOffRaw = kOffBar + 256;
+__host__ __device__ constexpr int seg_bytes_of(int t) { return t == SKV_F16 ? 256 : (t == SKV_Q8_0 ? 136 : 72); }
+template <int KT, int VT>
+__host__ __device__ constexpr int smem_bytes()
+{
+    return KT == SKV_F16 ? kSmem : kSmem + 2 * kPN * (seg_bytes_of(KT) + seg_bytes_of(VT));
+}
+static_assert(kSmem + 2 * kPN * (136 + 136) <= 227 * 1024, "shared memory per CTA");
 constexpr uint32_t kIdescS = tc::idesc_f16(kPM, kPN, false);
 constexpr uint32_t kIdescPV = tc::idesc_f16(kPM, kPD, true);
 constexpr float kRescaleLog2 = 8.0f;            // rescale O only when the max grows by > 2^8
@@ -146,100 +158,99 @@ __device__ __forceinline__ __half2 code_pair(uint32_t w)
     return *reinterpret_cast<const __half2 *>(&h);
 }
 
-// One key row of a tile from a row segment (nullptr: a padding key, zeros).
-// T = SKV_F16: sixteen 16-byte cp.async (the caller commits and waits).
-// q8_0 / q4_0: the segment's bytes are loaded with 8-byte loads and every
-// value d*q is written as fp16, 16 swizzled 16-byte chunks per row.  With
-// LO (keys), the value is split exactly into hi = fp16(d*q) in `tile` and
-// lo = fp16(d*q - hi) in `tile_lo` (one fused multiply-add: d*q has at most
-// 18 significant bits, so hi + lo is d*q whenever lo is a normal fp16);
+// Raw bytes of a q8_0 / q4_0 head segment as 32-bit words.
+template <int T>
+struct QSeg {
+    static constexpr int SEG = T == SKV_Q8_0 ? 136 : 72;   // 4 blocks of 34 or 18 bytes
+    static constexpr int NW = SEG / 4;
+};
+
+// Write one key row of a tile from its loaded segment words: every value d*q
+// as fp16, 16 swizzled 16-byte chunks per row (zeros for a padding row).
+// With LO (keys), the value is split exactly into hi = fp16(d*q) in `tile`
+// and lo = fp16(d*q - hi) in `tile_lo` (one fused multiply-add: d*q has at
+// most 18 significant bits, so hi + lo is d*q whenever lo is a normal fp16);
 // without LO (values) only fp16(d*q) is written, rounded once.
 template <int T, bool LO = false>
-__device__ __forceinline__ void produce_row(const uint8_t *seg, const uint8_t *any_valid, uint8_t *tile,
-                                            uint32_t tile_s, int r, uint8_t *tile_lo = nullptr)
+__device__ __forceinline__ void store_row(const uint32_t (&w)[QSeg<T>::NW], bool valid, uint8_t *tile, int r,
+                                          uint8_t *tile_lo = nullptr)
 {
-    if constexpr (T == SKV_F16) {
-        // a padding row copies nothing (source size 0 zero-fills) from a
-        // valid address
+    constexpr int SEG = QSeg<T>::SEG;
+    if (!valid) {
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-            cp_async16(tile_s + tile_off(r, c), seg ? seg + 16 * c : any_valid, seg ? 16 : 0);
-    } else {
-        constexpr int SEG = T == SKV_Q8_0 ? 136 : 72;   // 4 blocks of 34 or 18 bytes
-        constexpr int NW = SEG / 4;
-        if (!seg) {
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                *reinterpret_cast<uint4 *>(tile + tile_off(r, c)) = make_uint4(0, 0, 0, 0);
-                if (LO) *reinterpret_cast<uint4 *>(tile_lo + tile_off(r, c)) = make_uint4(0, 0, 0, 0);
-            }
-            return;
+        for (int c = 0; c < 16; ++c) {
+            *reinterpret_cast<uint4 *>(tile + tile_off(r, c)) = make_uint4(0, 0, 0, 0);
+            if (LO) *reinterpret_cast<uint4 *>(tile_lo + tile_off(r, c)) = make_uint4(0, 0, 0, 0);
         }
-        uint32_t w[NW];
-#pragma unroll
-        for (int i = 0; i < NW / 2; ++i) {
-            const uint2 x = __ldg(reinterpret_cast<const uint2 *>(seg) + i);
-            w[2 * i] = x.x;
-            w[2 * i + 1] = x.y;
-        }
-        // a byte pair at even offset o lives in word o/4, half (o/2)&1
+        return;
+    }
+    // a byte pair at even offset o lives in word o/4, half (o/2)&1
 #define SKV_PAIR_WORD(o) w[(o) >> 2]
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            constexpr int BLK = SEG / 4;
-            const int o_d = b * BLK;
-            const uint32_t dw = SKV_PAIR_WORD(o_d);
-            const __half d = __ushort_as_half(static_cast<unsigned short>((o_d & 2) ? (dw >> 16) : (dw & 0xffff)));
-            const __half2 dd = __half2half2(d);
-            if constexpr (T == SKV_Q8_0) {
-                const __half2 bias = __half2half2(__ushort_as_half(0x6480));   // 1152 = 1024 + 128
+    for (int b = 0; b < 4; ++b) {
+        constexpr int BLK = SEG / 4;
+        const int o_d = b * BLK;
+        const uint32_t dw = SKV_PAIR_WORD(o_d);
+        const __half d = __ushort_as_half(static_cast<unsigned short>((o_d & 2) ? (dw >> 16) : (dw & 0xffff)));
+        const __half2 dd = __half2half2(d);
+        if constexpr (T == SKV_Q8_0) {
+            const __half2 bias = __half2half2(__ushort_as_half(0x6480));   // 1152 = 1024 + 128
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {            // values 8c .. 8c+7 of the block
-                    uint32_t out[4], out_lo[4];
+            for (int c = 0; c < 4; ++c) {            // values 8c .. 8c+7 of the block
+                uint32_t out[4], out_lo[4];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int o = o_d + 2 + 8 * c + 2 * i;
-                        const uint32_t x = SKV_PAIR_WORD(o) ^ 0x80808080u;   // int8 q -> byte q + 128
-                        const __half2 qv = __hsub2((o & 2) ? code_pair<1>(x) : code_pair<0>(x), bias);
-                        const __half2 val = __hmul2(qv, dd);
-                        out[i] = *reinterpret_cast<const uint32_t *>(&val);
-                        if (LO) {
-                            const __half2 lo = __hfma2(qv, dd, __hneg2(val));
-                            out_lo[i] = *reinterpret_cast<const uint32_t *>(&lo);
-                        }
+                for (int i = 0; i < 4; ++i) {
+                    const int o = o_d + 2 + 8 * c + 2 * i;
+                    const uint32_t x = SKV_PAIR_WORD(o) ^ 0x80808080u;   // int8 q -> byte q + 128
+                    const __half2 qv = __hsub2((o & 2) ? code_pair<1>(x) : code_pair<0>(x), bias);
+                    const __half2 val = __hmul2(qv, dd);
+                    out[i] = *reinterpret_cast<const uint32_t *>(&val);
+                    if (LO) {
+                        const __half2 lo = __hfma2(qv, dd, __hneg2(val));
+                        out_lo[i] = *reinterpret_cast<const uint32_t *>(&lo);
                     }
-                    *reinterpret_cast<uint4 *>(tile + tile_off(r, 4 * b + c)) = make_uint4(out[0], out[1], out[2], out[3]);
-                    if (LO)
-                        *reinterpret_cast<uint4 *>(tile_lo + tile_off(r, 4 * b + c)) =
-                            make_uint4(out_lo[0], out_lo[1], out_lo[2], out_lo[3]);
                 }
-            } else {
-                const __half2 bias = __half2half2(__ushort_as_half(0x6408));   // 1032 = 1024 + 8
+                *reinterpret_cast<uint4 *>(tile + tile_off(r, 4 * b + c)) = make_uint4(out[0], out[1], out[2], out[3]);
+                if (LO)
+                    *reinterpret_cast<uint4 *>(tile_lo + tile_off(r, 4 * b + c)) =
+                        make_uint4(out_lo[0], out_lo[1], out_lo[2], out_lo[3]);
+            }
+        } else {
+            const __half2 bias = __half2half2(__ushort_as_half(0x6408));   // 1032 = 1024 + 8
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {            // c 0,1: low nibbles of bytes 0-7, 8-15; c 2,3: high
-                    uint32_t out[4], out_lo[4];
+            for (int c = 0; c < 4; ++c) {            // c 0,1: low nibbles of bytes 0-7, 8-15; c 2,3: high
+                uint32_t out[4], out_lo[4];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int o = o_d + 2 + 8 * (c & 1) + 2 * i;
-                        const uint32_t raw = SKV_PAIR_WORD(o);
-                        const uint32_t x = (c & 2) ? ((raw >> 4) & 0x0F0F0F0Fu) : (raw & 0x0F0F0F0Fu);
-                        const __half2 qv = __hsub2((o & 2) ? code_pair<1>(x) : code_pair<0>(x), bias);
-                        const __half2 val = __hmul2(qv, dd);
-                        out[i] = *reinterpret_cast<const uint32_t *>(&val);
-                        if (LO) {
-                            const __half2 lo = __hfma2(qv, dd, __hneg2(val));
-                            out_lo[i] = *reinterpret_cast<const uint32_t *>(&lo);
-                        }
+                for (int i = 0; i < 4; ++i) {
+                    const int o = o_d + 2 + 8 * (c & 1) + 2 * i;
+                    const uint32_t raw = SKV_PAIR_WORD(o);
+                    const uint32_t x = (c & 2) ? ((raw >> 4) & 0x0F0F0F0Fu) : (raw & 0x0F0F0F0Fu);
+                    const __half2 qv = __hsub2((o & 2) ? code_pair<1>(x) : code_pair<0>(x), bias);
+                    const __half2 val = __hmul2(qv, dd);
+                    out[i] = *reinterpret_cast<const uint32_t *>(&val);
+                    if (LO) {
+                        const __half2 lo = __hfma2(qv, dd, __hneg2(val));
+                        out_lo[i] = *reinterpret_cast<const uint32_t *>(&lo);
                     }
-                    *reinterpret_cast<uint4 *>(tile + tile_off(r, 4 * b + c)) = make_uint4(out[0], out[1], out[2], out[3]);
-                    if (LO)
-                        *reinterpret_cast<uint4 *>(tile_lo + tile_off(r, 4 * b + c)) =
-                            make_uint4(out_lo[0], out_lo[1], out_lo[2], out_lo[3]);
                 }
+                *reinterpret_cast<uint4 *>(tile + tile_off(r, 4 * b + c)) = make_uint4(out[0], out[1], out[2], out[3]);
+                if (LO)
+                    *reinterpret_cast<uint4 *>(tile_lo + tile_off(r, 4 * b + c)) =
+                        make_uint4(out_lo[0], out_lo[1], out_lo[2], out_lo[3]);
             }
         }
-#undef SKV_PAIR_WORD
     }
+#undef SKV_PAIR_WORD
+}
+
+// One fp16 key row of a tile: sixteen 16-byte cp.async (the caller commits
+// and waits); a padding row copies nothing (source size 0 zero-fills) from a
+// valid address.
+__device__ __forceinline__ void copy_row_f16(const uint8_t *seg, const uint8_t *any_valid, uint32_t tile_s, int r)
+{
+#pragma unroll
+    for (int c = 0; c < 16; ++c)
+        cp_async16(tile_s + tile_off(r, c), seg ? seg + 16 * c : any_valid, seg ? 16 : 0);
 }
 
 template <int MODE, int KT, int VT>
@@ -419,11 +430,86 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                 __syncwarp();
                 tc::mbar_arrive(bar(B_MFULL + (j & 3)));
             };
+            if constexpr (KT != SKV_F16) {
+            // Quantised rows: each thread's raw segments of tile j+1 are copied
+            // (cp.async, 8-byte pieces) into a staging slot while tile j is
+            // decoded from the other slot into the fp16 operand tiles.  A
+            // thread decodes exactly the rows it staged, so its own copy
+            // groups order everything; list entries run two tiles ahead.
+            uint8_t *raw = sm + kOffRaw;
+            constexpr int RAWK = kPN * SEGK, RAWV = kPN * SEGV;
+            auto raw_k = [&](int slot, int r) { return raw + slot * (RAWK + RAWV) + r * SEGK; };
+            auto raw_v = [&](int slot, int r) { return raw + slot * (RAWK + RAWV) + RAWK + r * SEGV; };
+            auto issue_raw = [&](int slot, const int64_t (&rw)[RPT]) {
+#pragma unroll
+                for (int u = 0; u < RPT; ++u) {
+                    const int r = r0 + u * NPT;
+                    const uint8_t *ks = k_src(rw[u]);
+                    const uint8_t *vs = v_src(rw[u]);
+#pragma unroll
+                    for (int i = 0; i < SEGK / 8; ++i)
+                        cp_async8(smem_addr(raw_k(slot, r) + 8 * i), ks ? ks + 8 * i : a.k, ks ? 8 : 0);
+#pragma unroll
+                    for (int i = 0; i < SEGV / 8; ++i)
+                        cp_async8(smem_addr(raw_v(slot, r) + 8 * i), vs ? vs + 8 * i : a.v, vs ? 8 : 0);
+                }
+                cp_async_commit();
+            };
+            int64_t e0[RPT], e1[RPT];
+#pragma unroll
+            for (int u = 0; u < RPT; ++u) {
+                e0[u] = n_tiles > 0 ? tile_row(0, u) : -1;
+                e1[u] = n_tiles > 1 ? tile_row(1, u) : -1;
+            }
+            if (n_tiles > 0) issue_raw(0, e0);
+            for (int j = 0; j < n_tiles; ++j) {
+                const int b = j & 1;
+                const int kb = KLO ? 0 : b;                      // K stage of this tile
+                const int slot = j & 1;
+                if (j + 1 < n_tiles) issue_raw(slot ^ 1, e1);
+                int64_t e2[RPT];
+#pragma unroll
+                for (int u = 0; u < RPT; ++u) e2[u] = j + 2 < n_tiles ? tile_row(j + 2, u) : -1;
+                if (j + 1 < n_tiles) cp_async_wait<1>();        // this thread's segments of tile j landed
+                else cp_async_wait<0>();
+                const bool k_ok = KLO ? (j < 1 || wait(B_KEMPTY, (j - 1) & 1))
+                                      : (j < 2 || wait(B_KEMPTY + b, ((j >> 1) - 1) & 1));
+                if (!__all_sync(0xffffffffu, k_ok)) break;
+#pragma unroll
+                for (int u = 0; u < RPT; ++u) {
+                    const int r = r0 + u * NPT;
+                    uint32_t w[QSeg<KT>::NW];
+#pragma unroll
+                    for (int i = 0; i < QSeg<KT>::NW; ++i) w[i] = *reinterpret_cast<const uint32_t *>(raw_k(slot, r) + 4 * i);
+                    store_row<KT, KLO>(w, e0[u] >= 0, sm + kOffK + kb * kTileBytes, r, sm + kOffK + kTileBytes);
+                }
+                if (!__all_sync(0xffffffffu, j < 2 || wait(B_VEMPTY + b, ((j >> 1) - 1) & 1))) break;
+                publish_mask(j, e0);
+#pragma unroll
+                for (int u = 0; u < RPT; ++u) {
+                    const int r = r0 + u * NPT;
+                    uint32_t w[QSeg<VT>::NW];
+#pragma unroll
+                    for (int i = 0; i < QSeg<VT>::NW; ++i) w[i] = *reinterpret_cast<const uint32_t *>(raw_v(slot, r) + 4 * i);
+                    store_row<VT>(w, e0[u] >= 0, sm + kOffV + b * kTileBytes, r);
+                }
+                tc::fence_proxy_async_smem();
+                tc::mbar_arrive(bar(B_KFULL + kb));
+                tc::mbar_arrive(bar(B_VFULL + b));
+#pragma unroll
+                for (int u = 0; u < RPT; ++u) {
+                    e0[u] = e1[u];
+                    e1[u] = e2[u];
+                }
+            }
+            cp_async_wait<0>();
+            } else {
+            // fp16 rows (row lists), one tile at a time: a tile's K and V copies
+            // are in flight together, and the next tile's list entries load
+            // while they land.
             int64_t cur[RPT];
 #pragma unroll
             for (int u = 0; u < RPT; ++u) cur[u] = n_tiles > 0 ? tile_row(0, u) : -1;
-            // One tile at a time: a tile's K and V copies are in flight together,
-            // and the next tile's list entries load while they land.
             for (int j = 0; j < n_tiles; ++j) {
                 const int b = j & 1;
                 const int kb = KLO ? 0 : b;                      // K stage of this tile
@@ -436,15 +522,13 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                 if (!__all_sync(0xffffffffu, k_ok)) break;
 #pragma unroll
                 for (int u = 0; u < RPT; ++u)
-                    produce_row<KT, KLO>(k_src(cur[u]), a.k, sm + kOffK + kb * kTileBytes,
-                                         sbase + kOffK + kb * kTileBytes, r0 + u * NPT, sm + kOffK + kTileBytes);
+                    copy_row_f16(k_src(cur[u]), a.k, sbase + kOffK + kb * kTileBytes, r0 + u * NPT);
                 cp_async_commit();
                 if (!__all_sync(0xffffffffu, j < 2 || wait(B_VEMPTY + b, ((j >> 1) - 1) & 1))) break;
                 publish_mask(j, cur);
 #pragma unroll
                 for (int u = 0; u < RPT; ++u)
-                    produce_row<VT>(v_src(cur[u]), a.v, sm + kOffV + b * kTileBytes, sbase + kOffV + b * kTileBytes,
-                                    r0 + u * NPT);
+                    copy_row_f16(v_src(cur[u]), a.v, sbase + kOffV + b * kTileBytes, r0 + u * NPT);
                 cp_async_commit();
                 cp_async_wait<1>();
                 tc::fence_proxy_async_smem();
@@ -456,6 +540,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                 for (int u = 0; u < RPT; ++u) cur[u] = nxt[u];
             }
             cp_async_wait<0>();
+            }
         }
     } else if (warp == C::kMmaWarp) {
         // ---------------- MMA issuer ----------------------------------------
@@ -744,12 +829,12 @@ int launch_prefill_t(skv_handle *h, const CUtensorMap &mk, const CUtensorMap &mv
     static bool attr_done = false;
     if (!attr_done) {
         cudaError_t e = cudaFuncSetAttribute(splitkv_prefill_kernel<MODE, KT, VT>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<KT, VT>());
         if (e != cudaSuccess) return cuda_fail(h, e, "cudaFuncSetAttribute(prefill)");
         attr_done = true;
     }
     if (h->prof_before) cudaEventRecord(h->prof_before, st);
-    splitkv_prefill_kernel<MODE, KT, VT><<<grid, Cfg<MODE>::kThreads, kSmem, st>>>(mk, mv, a);
+    splitkv_prefill_kernel<MODE, KT, VT><<<grid, Cfg<MODE>::kThreads, smem_bytes<KT, VT>(), st>>>(mk, mv, a);
     if (h->prof_after) cudaEventRecord(h->prof_after, st);
     return cuda_fail(h, cudaGetLastError(), "prefill kernel launch");
 }
