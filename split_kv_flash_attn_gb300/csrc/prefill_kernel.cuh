@@ -431,115 +431,115 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                 tc::mbar_arrive(bar(B_MFULL + (j & 3)));
             };
             if constexpr (KT != SKV_F16) {
-            // Quantised rows: each thread's raw segments of tile j+1 are copied
-            // (cp.async, 8-byte pieces) into a staging slot while tile j is
-            // decoded from the other slot into the fp16 operand tiles.  A
-            // thread decodes exactly the rows it staged, so its own copy
-            // groups order everything; list entries run two tiles ahead.
-            uint8_t *raw = sm + kOffRaw;
-            constexpr int RAWK = kPN * SEGK, RAWV = kPN * SEGV;
-            auto raw_k = [&](int slot, int r) { return raw + slot * (RAWK + RAWV) + r * SEGK; };
-            auto raw_v = [&](int slot, int r) { return raw + slot * (RAWK + RAWV) + RAWK + r * SEGV; };
-            auto issue_raw = [&](int slot, const int64_t (&rw)[RPT]) {
+                // Quantised rows: each thread's raw segments of tile j+1 are copied
+                // (cp.async, 8-byte pieces) into a staging slot while tile j is
+                // decoded from the other slot into the fp16 operand tiles.  A
+                // thread decodes exactly the rows it staged, so its own copy
+                // groups order everything; list entries run two tiles ahead.
+                uint8_t *raw = sm + kOffRaw;
+                constexpr int RAWK = kPN * SEGK, RAWV = kPN * SEGV;
+                auto raw_k = [&](int slot, int r) { return raw + slot * (RAWK + RAWV) + r * SEGK; };
+                auto raw_v = [&](int slot, int r) { return raw + slot * (RAWK + RAWV) + RAWK + r * SEGV; };
+                auto issue_raw = [&](int slot, const int64_t (&rw)[RPT]) {
+#pragma unroll
+                    for (int u = 0; u < RPT; ++u) {
+                        const int r = r0 + u * NPT;
+                        const uint8_t *ks = k_src(rw[u]);
+                        const uint8_t *vs = v_src(rw[u]);
+#pragma unroll
+                        for (int i = 0; i < SEGK / 8; ++i)
+                            cp_async8(smem_addr(raw_k(slot, r) + 8 * i), ks ? ks + 8 * i : a.k, ks ? 8 : 0);
+#pragma unroll
+                        for (int i = 0; i < SEGV / 8; ++i)
+                            cp_async8(smem_addr(raw_v(slot, r) + 8 * i), vs ? vs + 8 * i : a.v, vs ? 8 : 0);
+                    }
+                    cp_async_commit();
+                };
+                int64_t e0[RPT], e1[RPT];
 #pragma unroll
                 for (int u = 0; u < RPT; ++u) {
-                    const int r = r0 + u * NPT;
-                    const uint8_t *ks = k_src(rw[u]);
-                    const uint8_t *vs = v_src(rw[u]);
-#pragma unroll
-                    for (int i = 0; i < SEGK / 8; ++i)
-                        cp_async8(smem_addr(raw_k(slot, r) + 8 * i), ks ? ks + 8 * i : a.k, ks ? 8 : 0);
-#pragma unroll
-                    for (int i = 0; i < SEGV / 8; ++i)
-                        cp_async8(smem_addr(raw_v(slot, r) + 8 * i), vs ? vs + 8 * i : a.v, vs ? 8 : 0);
+                    e0[u] = n_tiles > 0 ? tile_row(0, u) : -1;
+                    e1[u] = n_tiles > 1 ? tile_row(1, u) : -1;
                 }
-                cp_async_commit();
-            };
-            int64_t e0[RPT], e1[RPT];
+                if (n_tiles > 0) issue_raw(0, e0);
+                for (int j = 0; j < n_tiles; ++j) {
+                    const int b = j & 1;
+                    const int kb = KLO ? 0 : b;                      // K stage of this tile
+                    const int slot = j & 1;
+                    if (j + 1 < n_tiles) issue_raw(slot ^ 1, e1);
+                    int64_t e2[RPT];
 #pragma unroll
-            for (int u = 0; u < RPT; ++u) {
-                e0[u] = n_tiles > 0 ? tile_row(0, u) : -1;
-                e1[u] = n_tiles > 1 ? tile_row(1, u) : -1;
-            }
-            if (n_tiles > 0) issue_raw(0, e0);
-            for (int j = 0; j < n_tiles; ++j) {
-                const int b = j & 1;
-                const int kb = KLO ? 0 : b;                      // K stage of this tile
-                const int slot = j & 1;
-                if (j + 1 < n_tiles) issue_raw(slot ^ 1, e1);
-                int64_t e2[RPT];
+                    for (int u = 0; u < RPT; ++u) e2[u] = j + 2 < n_tiles ? tile_row(j + 2, u) : -1;
+                    if (j + 1 < n_tiles) cp_async_wait<1>();        // this thread's segments of tile j landed
+                    else cp_async_wait<0>();
+                    const bool k_ok = KLO ? (j < 1 || wait(B_KEMPTY, (j - 1) & 1))
+                                          : (j < 2 || wait(B_KEMPTY + b, ((j >> 1) - 1) & 1));
+                    if (!__all_sync(0xffffffffu, k_ok)) break;
 #pragma unroll
-                for (int u = 0; u < RPT; ++u) e2[u] = j + 2 < n_tiles ? tile_row(j + 2, u) : -1;
-                if (j + 1 < n_tiles) cp_async_wait<1>();        // this thread's segments of tile j landed
-                else cp_async_wait<0>();
-                const bool k_ok = KLO ? (j < 1 || wait(B_KEMPTY, (j - 1) & 1))
-                                      : (j < 2 || wait(B_KEMPTY + b, ((j >> 1) - 1) & 1));
-                if (!__all_sync(0xffffffffu, k_ok)) break;
+                    for (int u = 0; u < RPT; ++u) {
+                        const int r = r0 + u * NPT;
+                        uint32_t w[QSeg<KT>::NW];
 #pragma unroll
-                for (int u = 0; u < RPT; ++u) {
-                    const int r = r0 + u * NPT;
-                    uint32_t w[QSeg<KT>::NW];
+                        for (int i = 0; i < QSeg<KT>::NW; ++i) w[i] = *reinterpret_cast<const uint32_t *>(raw_k(slot, r) + 4 * i);
+                        store_row<KT, KLO>(w, e0[u] >= 0, sm + kOffK + kb * kTileBytes, r, sm + kOffK + kTileBytes);
+                    }
+                    if (!__all_sync(0xffffffffu, j < 2 || wait(B_VEMPTY + b, ((j >> 1) - 1) & 1))) break;
+                    publish_mask(j, e0);
 #pragma unroll
-                    for (int i = 0; i < QSeg<KT>::NW; ++i) w[i] = *reinterpret_cast<const uint32_t *>(raw_k(slot, r) + 4 * i);
-                    store_row<KT, KLO>(w, e0[u] >= 0, sm + kOffK + kb * kTileBytes, r, sm + kOffK + kTileBytes);
+                    for (int u = 0; u < RPT; ++u) {
+                        const int r = r0 + u * NPT;
+                        uint32_t w[QSeg<VT>::NW];
+#pragma unroll
+                        for (int i = 0; i < QSeg<VT>::NW; ++i) w[i] = *reinterpret_cast<const uint32_t *>(raw_v(slot, r) + 4 * i);
+                        store_row<VT>(w, e0[u] >= 0, sm + kOffV + b * kTileBytes, r);
+                    }
+                    tc::fence_proxy_async_smem();
+                    tc::mbar_arrive(bar(B_KFULL + kb));
+                    tc::mbar_arrive(bar(B_VFULL + b));
+#pragma unroll
+                    for (int u = 0; u < RPT; ++u) {
+                        e0[u] = e1[u];
+                        e1[u] = e2[u];
+                    }
                 }
-                if (!__all_sync(0xffffffffu, j < 2 || wait(B_VEMPTY + b, ((j >> 1) - 1) & 1))) break;
-                publish_mask(j, e0);
-#pragma unroll
-                for (int u = 0; u < RPT; ++u) {
-                    const int r = r0 + u * NPT;
-                    uint32_t w[QSeg<VT>::NW];
-#pragma unroll
-                    for (int i = 0; i < QSeg<VT>::NW; ++i) w[i] = *reinterpret_cast<const uint32_t *>(raw_v(slot, r) + 4 * i);
-                    store_row<VT>(w, e0[u] >= 0, sm + kOffV + b * kTileBytes, r);
-                }
-                tc::fence_proxy_async_smem();
-                tc::mbar_arrive(bar(B_KFULL + kb));
-                tc::mbar_arrive(bar(B_VFULL + b));
-#pragma unroll
-                for (int u = 0; u < RPT; ++u) {
-                    e0[u] = e1[u];
-                    e1[u] = e2[u];
-                }
-            }
-            cp_async_wait<0>();
-            } else {
-            // fp16 rows (row lists), one tile at a time: a tile's K and V copies
-            // are in flight together, and the next tile's list entries load
-            // while they land.
-            int64_t cur[RPT];
-#pragma unroll
-            for (int u = 0; u < RPT; ++u) cur[u] = n_tiles > 0 ? tile_row(0, u) : -1;
-            for (int j = 0; j < n_tiles; ++j) {
-                const int b = j & 1;
-                const int kb = KLO ? 0 : b;                      // K stage of this tile
-                int64_t nxt[RPT];
-#pragma unroll
-                for (int u = 0; u < RPT; ++u) nxt[u] = j + 1 < n_tiles ? tile_row(j + 1, u) : -1;
-                // (waits are made warp-uniform: the loop holds warp collectives)
-                const bool k_ok = KLO ? (j < 1 || wait(B_KEMPTY, (j - 1) & 1))
-                                      : (j < 2 || wait(B_KEMPTY + b, ((j >> 1) - 1) & 1));
-                if (!__all_sync(0xffffffffu, k_ok)) break;
-#pragma unroll
-                for (int u = 0; u < RPT; ++u)
-                    copy_row_f16(k_src(cur[u]), a.k, sbase + kOffK + kb * kTileBytes, r0 + u * NPT);
-                cp_async_commit();
-                if (!__all_sync(0xffffffffu, j < 2 || wait(B_VEMPTY + b, ((j >> 1) - 1) & 1))) break;
-                publish_mask(j, cur);
-#pragma unroll
-                for (int u = 0; u < RPT; ++u)
-                    copy_row_f16(v_src(cur[u]), a.v, sbase + kOffV + b * kTileBytes, r0 + u * NPT);
-                cp_async_commit();
-                cp_async_wait<1>();
-                tc::fence_proxy_async_smem();
-                tc::mbar_arrive(bar(B_KFULL + kb));
                 cp_async_wait<0>();
-                tc::fence_proxy_async_smem();
-                tc::mbar_arrive(bar(B_VFULL + b));
+            } else {
+                // fp16 rows (row lists), one tile at a time: a tile's K and V copies
+                // are in flight together, and the next tile's list entries load
+                // while they land.
+                int64_t cur[RPT];
 #pragma unroll
-                for (int u = 0; u < RPT; ++u) cur[u] = nxt[u];
-            }
-            cp_async_wait<0>();
+                for (int u = 0; u < RPT; ++u) cur[u] = n_tiles > 0 ? tile_row(0, u) : -1;
+                for (int j = 0; j < n_tiles; ++j) {
+                    const int b = j & 1;
+                    const int kb = KLO ? 0 : b;                      // K stage of this tile
+                    int64_t nxt[RPT];
+#pragma unroll
+                    for (int u = 0; u < RPT; ++u) nxt[u] = j + 1 < n_tiles ? tile_row(j + 1, u) : -1;
+                    // (waits are made warp-uniform: the loop holds warp collectives)
+                    const bool k_ok = KLO ? (j < 1 || wait(B_KEMPTY, (j - 1) & 1))
+                                          : (j < 2 || wait(B_KEMPTY + b, ((j >> 1) - 1) & 1));
+                    if (!__all_sync(0xffffffffu, k_ok)) break;
+#pragma unroll
+                    for (int u = 0; u < RPT; ++u)
+                        copy_row_f16(k_src(cur[u]), a.k, sbase + kOffK + kb * kTileBytes, r0 + u * NPT);
+                    cp_async_commit();
+                    if (!__all_sync(0xffffffffu, j < 2 || wait(B_VEMPTY + b, ((j >> 1) - 1) & 1))) break;
+                    publish_mask(j, cur);
+#pragma unroll
+                    for (int u = 0; u < RPT; ++u)
+                        copy_row_f16(v_src(cur[u]), a.v, sbase + kOffV + b * kTileBytes, r0 + u * NPT);
+                    cp_async_commit();
+                    cp_async_wait<1>();
+                    tc::fence_proxy_async_smem();
+                    tc::mbar_arrive(bar(B_KFULL + kb));
+                    cp_async_wait<0>();
+                    tc::fence_proxy_async_smem();
+                    tc::mbar_arrive(bar(B_VFULL + b));
+#pragma unroll
+                    for (int u = 0; u < RPT; ++u) cur[u] = nxt[u];
+                }
+                cp_async_wait<0>();
             }
         }
     } else if (warp == C::kMmaWarp) {
