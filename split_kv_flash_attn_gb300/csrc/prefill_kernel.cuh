@@ -81,11 +81,15 @@ constexpr float kRescaleLog2 = 8.0f;            // rescale O only when the max g
 // Producer warps and thread count per mode (MODE 0: TMA, MODE 1: software).
 template <int MODE>
 struct Cfg {
-    // 11 warps: at most 3 per SM sub-partition, so the softmax warps keep up
-    // to 168 registers (13 warps would cap them at 128).  MODE 0: one warp
-    // streams K tiles and one V tiles, so neither waits behind the other's
-    // ring slot (two lanes of one warp would share its issue).
-    static constexpr int kProducerWarps = 2;
+    // MODE 0: 11 warps, at most 3 per SM sub-partition, so the softmax warps
+    // keep up to 168 registers; one warp streams K tiles and one V tiles, so
+    // neither waits behind the other's ring slot (two lanes of one warp would
+    // share its issue).  MODE 1: 13 warps, four of them producers, so each
+    // producer thread fetches and converts one key row of a tile; the
+    // sub-partition holding four warps caps every thread at 128 registers,
+    // and the producers' throughput is worth more than the softmax's spare
+    // registers (two producer warps: 1.6x the kernel time).
+    static constexpr int kProducerWarps = MODE == 0 ? 2 : 4;
     static constexpr int kMmaWarp = kSoftmaxWarps + kProducerWarps;
     static constexpr int kThreads = (kMmaWarp + 1) * 32;
     static constexpr uint32_t kFullCount = MODE == 0 ? 1 : kProducerWarps * 32;
@@ -391,7 +395,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                 }
             }
         } else {
-            // ---------------- software producers: each thread two key rows ------
+            // ---------------- software producers: kPN / NPT key rows a thread --
             // No wait may depend on a tile the producers have not published yet.
             constexpr int NPT = C::kProducerWarps * 32;      // producer threads
             constexpr int RPT = kPN / NPT;                   // rows per thread
