@@ -1,6 +1,6 @@
 // prefill.cu -- host side of the tensor-core prefill kernel
 // (prefill_kernel.cuh): eligibility, tensor maps, split arguments, and the
-// TMA instance over dense fp16 regions.  Row-list and quantised regions use
+// TMA instance over dense fp16 regions.  Row lists and quantised rows use
 // the software-producer instances in prefill_sw.cu.
 #include "prefill_kernel.cuh"
 
@@ -66,7 +66,7 @@ int launch_prefill(skv_handle *h, const PrefillLaunch &L, cudaStream_t st)
 {
     const skv_shape *sh = L.shape;
     const int G = sh->H / sh->Hk;
-    const bool tma = L.rows == nullptr && sh->k_type == SKV_F16 && sh->v_type == SKV_F16;
+    const bool f16 = sh->k_type == SKV_F16 && sh->v_type == SKV_F16;
     PrefillArgs a;
     memset(&a, 0, sizeof(a));
     a.q = static_cast<const __half *>(L.q);
@@ -104,12 +104,9 @@ int launch_prefill(skv_handle *h, const PrefillLaunch &L, cudaStream_t st)
         return fail(h, SKV_EUNSUPPORTED, "prefill grid too large");
     dim3 grid(static_cast<unsigned>(sh->Hk * a.m_tiles), static_cast<unsigned>(a.n_splits),
               static_cast<unsigned>(sh->S));
-    if (!tma) {
-        const int al = sh->k_type == SKV_F16 ? 16 : 8;
-        if ((reinterpret_cast<uintptr_t>(L.k) | reinterpret_cast<uintptr_t>(L.v)) % al)
-            return fail(h, SKV_EUNSUPPORTED, "K/V bases must be %d-byte aligned for the prefill kernel", al);
-        return launch_prefill_sw(h, a, sh->k_type, sh->v_type, grid, st);
-    }
+    if ((reinterpret_cast<uintptr_t>(L.k) | reinterpret_cast<uintptr_t>(L.v)) % (f16 ? 16 : 8))
+        return fail(h, SKV_EUNSUPPORTED, "K/V bases must be %d-byte aligned for the prefill kernel", f16 ? 16 : 8);
+    if (!f16 || L.rows) return launch_prefill_sw(h, a, sh->k_type, sh->v_type, grid, st);
     CUtensorMap mk, mv;
     int rc = make_map(h, &mk, L.k, L.n_rows, sh->Hk, sh->k_row_bytes);
     if (rc == SKV_OK) rc = make_map(h, &mv, L.v, L.n_rows, sh->Hk, sh->v_row_bytes);

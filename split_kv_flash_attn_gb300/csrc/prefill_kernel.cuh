@@ -8,13 +8,16 @@
 //
 //   producer      : K_j, V_j tiles (128 keys x 128 d, fp16, 128-byte swizzle)
 //                   into a 2-deep K ring and a 2-deep V ring.  MODE 0: one
-//                   thread issues TMA loads over a dense fp16 region.  MODE 1:
-//                   two warps, two key rows per thread, fetch the rows through
-//                   a row list (padding entries read nothing) or a dense range;
-//                   fp16 rows go straight to the swizzled tile by cp.async;
-//                   q8_0 / q4_0 segments are staged raw in shared memory by
-//                   cp.async one tile ahead, then decoded to fp16(d*q) and
-//                   stored in the same layout.
+//                   thread of a K warp and one of a V warp issue TMA tile
+//                   loads over a dense fp16 region.  MODE 2: two warps copy
+//                   the K rows and two the V rows of a row list by cp.async,
+//                   each pair through its own ring (padding entries copy
+//                   nothing and zero-fill).  MODE 1:
+//                   four warps, one key row per thread, fetch q8_0 / q4_0
+//                   rows through a row list or a dense range: raw segments
+//                   are staged in shared memory by cp.async one tile ahead,
+//                   then decoded to fp16(d*q) and stored in the same
+//                   layout.
 //   MMA warp      : S_j = Q K_j^T        tcgen05.mma kind::f16, M=N=128, into
 //                                        one of two TMEM S buffers (fp32); Q
 //                                        is the A operand in tensor memory
@@ -78,21 +81,28 @@ constexpr uint32_t kIdescS = tc::idesc_f16(kPM, kPN, false);
 constexpr uint32_t kIdescPV = tc::idesc_f16(kPM, kPD, true);
 constexpr float kRescaleLog2 = 8.0f;            // rescale O only when the max grows by > 2^8
 
-// Producer warps and thread count per mode (MODE 0: TMA, MODE 1: software).
+// Producer warps and thread count per mode (MODE 0: TMA tiles, MODE 1:
+// quantised rows converted by software, MODE 2: fp16 row lists by cp.async).
 template <int MODE>
 struct Cfg {
     // MODE 0: 11 warps, at most 3 per SM sub-partition, so the softmax warps
     // keep up to 168 registers; one warp streams K tiles and one V tiles, so
     // neither waits behind the other's ring slot (two lanes of one warp would
-    // share its issue).  MODE 1: 13 warps, four of them producers, so each
-    // producer thread fetches and converts one key row of a tile; the
-    // sub-partition holding four warps caps every thread at 128 registers,
-    // and the producers' throughput is worth more than the softmax's spare
-    // registers (two producer warps: 1.6x the kernel time).
+    // share its issue).  MODE 1 and 2: 13 warps, four of them producers (MODE
+    // 1: each thread fetches and converts one key row of a tile; MODE 2: two
+    // warps copy K rows and two V rows); the sub-partition holding four warps
+    // caps every thread at 128 registers, and the producers' throughput is
+    // worth more than the softmax's spare registers (two producer warps: 1.6x
+    // the kernel time).
     static constexpr int kProducerWarps = MODE == 0 ? 2 : 4;
     static constexpr int kMmaWarp = kSoftmaxWarps + kProducerWarps;
     static constexpr int kThreads = (kMmaWarp + 1) * 32;
-    static constexpr uint32_t kFullCount = MODE == 0 ? 1 : kProducerWarps * 32;
+    // arrivals that fill a K or V stage: the TMA thread's expect-tx, every
+    // producer thread (MODE 1), or the threads of the operand's two warps
+    static constexpr uint32_t kFullCount = MODE == 0 ? 1 : (MODE == 1 ? kProducerWarps * 32 : 64);
+    // arrivals on a row-list padding mask: the producer threads, or (MODE 2)
+    // the two K warps
+    static constexpr uint32_t kMaskCount = MODE == 2 ? 64 : kProducerWarps * 32;
 };
 
 // barrier slots (8 bytes each) inside the barrier area
@@ -247,15 +257,6 @@ __device__ __forceinline__ void store_row(const uint32_t (&w)[QSeg<T>::NW], bool
 #undef SKV_PAIR_WORD
 }
 
-// One fp16 key row of a tile: sixteen 16-byte cp.async (the caller commits
-// and waits); a padding row copies nothing (source size 0 zero-fills) from a
-// valid address.
-__device__ __forceinline__ void copy_row_f16(const uint8_t *seg, const uint8_t *any_valid, uint32_t tile_s, int r)
-{
-#pragma unroll
-    for (int c = 0; c < 16; ++c)
-        cp_async16(tile_s + tile_off(r, c), seg ? seg + 16 * c : any_valid, seg ? 16 : 0);
-}
 
 template <int MODE, int KT, int VT>
 __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
@@ -330,7 +331,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
         tc::mbar_init(bar(B_PFULL), kSoftmaxThreads);
         tc::mbar_init(bar(B_PFREE), 1);                          // PV of the last P done
         tc::mbar_init(bar(B_QFULL), kSoftmaxThreads);
-        for (int i = 0; i < 4; ++i) tc::mbar_init(bar(B_MFULL + i), C::kProducerWarps * 32);
+        for (int i = 0; i < 4; ++i) tc::mbar_init(bar(B_MFULL + i), C::kMaskCount);
         tc::fence_barrier_init();
         if (MODE == 0) {
             tc::prefetch_tmap(&tmap_k);
@@ -394,6 +395,74 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                         tc::mbar_wait(bar(b_full + (j & 1)), (j >> 1) & 1, nullptr, 100000000ull);
                 }
             }
+        } else if constexpr (MODE == 2) {
+            // ---------------- fp16 row lists: two K warps, two V warps -------
+            // Each pair streams its own operand through its 2-slot ring, as
+            // the TMA warps do: tile j's copies are issued once its slot is
+            // free, and tile j-1 is published when its copies have landed, so
+            // up to two tiles of each operand are in flight and a K tile never
+            // waits for a PV.  A warp copies 64 rows of a tile, two rows per
+            // cp.async instruction (16 lanes x 16 bytes cover one row's 256
+            // bytes, so an instruction touches four cache lines); lane l holds
+            // the list entries of its rows l and l + 32.  Padding entries copy
+            // nothing (source size 0 zero-fills).  The K warps publish each
+            // tile's padding mask when they issue it: its slot (j % 4) was last
+            // read by the softmax of tile j - 4, before P(j - 4) was published,
+            // and PV(j - 4) is issued before S(j - 2), whose completion freed
+            // the K slot.
+            static_assert(KT == SKV_F16 && VT == SKV_F16, "fp16 rows");
+            const int pw = warp - kSoftmaxWarps;          // 0, 1: K; 2, 3: V
+            const bool is_v = pw >= 2;
+            const int rbase = (pw & 1) * 64;              // first tile row of this warp
+            const uint8_t *base = is_v ? a.v : a.k;
+            const int64_t row_bytes = is_v ? a.v_row_bytes : a.k_row_bytes;
+            const uint8_t *seg0 = base + static_cast<int64_t>(kh) * (kPD * 2) + 16 * (lane & 15);
+            const uint32_t ring = sbase + (is_v ? kOffV : kOffK);
+            const int b_empty = is_v ? B_VEMPTY : B_KEMPTY, b_full = is_v ? B_VFULL : B_KFULL;
+            auto entry = [&](int j, int half) -> int {
+                const int64_t key = j_lo + static_cast<int64_t>(j) * kPN + rbase + 32 * half + lane;
+                return (j < n_tiles && key < j_hi) ? __ldg(lrow + key) : -1;
+            };
+            int cur0 = entry(0, 0), cur1 = entry(0, 1);
+            int issued = 0;
+            for (int j = 0; j < n_tiles; ++j) {
+                const int b = j & 1;
+                const int nx0 = entry(j + 1, 0), nx1 = entry(j + 1, 1);
+                if (!__all_sync(0xffffffffu, j < 2 || wait(b_empty + b, ((j >> 1) - 1) & 1))) break;
+                if (!is_v) {
+                    const int64_t key = j_lo + static_cast<int64_t>(j) * kPN + rbase + lane;
+                    const uint32_t w0 = __ballot_sync(0xffffffffu, cur0 >= 0 || key >= j_hi);
+                    const uint32_t w1 = __ballot_sync(0xffffffffu, cur1 >= 0 || key + 32 >= j_hi);
+                    if (lane == 0) {
+                        s_vmask[j & 3][rbase / 32] = w0;
+                        s_vmask[j & 3][rbase / 32 + 1] = w1;
+                    }
+                    __syncwarp();
+                    tc::mbar_arrive(bar(B_MFULL + (j & 3)));
+                }
+                const uint32_t tile_s = ring + static_cast<uint32_t>(b * kTileBytes);
+#pragma unroll
+                for (int it = 0; it < 32; ++it) {
+                    const int rr = 2 * it + (lane >> 4);      // row of this warp's 64
+                    const int row = __shfl_sync(0xffffffffu, it < 16 ? cur0 : cur1, rr & 31);
+                    cp_async16(tile_s + tile_off(rbase + rr, lane & 15),
+                               row >= 0 ? seg0 + static_cast<int64_t>(row) * row_bytes : base, row >= 0 ? 16 : 0);
+                }
+                cp_async_commit();
+                if (j >= 1) {
+                    cp_async_wait<1>();                       // this thread's copies of tile j-1
+                    tc::fence_proxy_async_smem();
+                    tc::mbar_arrive(bar(b_full + ((j - 1) & 1)));
+                }
+                ++issued;
+                cur0 = nx0;
+                cur1 = nx1;
+            }
+            cp_async_wait<0>();
+            if (issued == n_tiles && issued > 0) {
+                tc::fence_proxy_async_smem();
+                tc::mbar_arrive(bar(b_full + ((issued - 1) & 1)));
+            }
         } else {
             // ---------------- software producers: kPN / NPT key rows a thread --
             // No wait may depend on a tile the producers have not published yet.
@@ -434,7 +503,8 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                 __syncwarp();
                 tc::mbar_arrive(bar(B_MFULL + (j & 3)));
             };
-            if constexpr (KT != SKV_F16) {
+            static_assert(KT != SKV_F16 && VT != SKV_F16, "quantised rows");
+            {
                 // Quantised rows: each thread's raw segments of tile j+1 are copied
                 // (cp.async, 8-byte pieces) into a staging slot while tile j is
                 // decoded from the other slot into the fp16 operand tiles.  A
@@ -505,43 +575,6 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                         e0[u] = e1[u];
                         e1[u] = e2[u];
                     }
-                }
-                cp_async_wait<0>();
-            } else {
-                // fp16 rows (row lists), one tile at a time: a tile's K and V copies
-                // are in flight together, and the next tile's list entries load
-                // while they land.
-                int64_t cur[RPT];
-#pragma unroll
-                for (int u = 0; u < RPT; ++u) cur[u] = n_tiles > 0 ? tile_row(0, u) : -1;
-                for (int j = 0; j < n_tiles; ++j) {
-                    const int b = j & 1;
-                    const int kb = KLO ? 0 : b;                      // K stage of this tile
-                    int64_t nxt[RPT];
-#pragma unroll
-                    for (int u = 0; u < RPT; ++u) nxt[u] = j + 1 < n_tiles ? tile_row(j + 1, u) : -1;
-                    // (waits are made warp-uniform: the loop holds warp collectives)
-                    const bool k_ok = KLO ? (j < 1 || wait(B_KEMPTY, (j - 1) & 1))
-                                          : (j < 2 || wait(B_KEMPTY + b, ((j >> 1) - 1) & 1));
-                    if (!__all_sync(0xffffffffu, k_ok)) break;
-#pragma unroll
-                    for (int u = 0; u < RPT; ++u)
-                        copy_row_f16(k_src(cur[u]), a.k, sbase + kOffK + kb * kTileBytes, r0 + u * NPT);
-                    cp_async_commit();
-                    if (!__all_sync(0xffffffffu, j < 2 || wait(B_VEMPTY + b, ((j >> 1) - 1) & 1))) break;
-                    publish_mask(j, cur);
-#pragma unroll
-                    for (int u = 0; u < RPT; ++u)
-                        copy_row_f16(v_src(cur[u]), a.v, sbase + kOffV + b * kTileBytes, r0 + u * NPT);
-                    cp_async_commit();
-                    cp_async_wait<1>();
-                    tc::fence_proxy_async_smem();
-                    tc::mbar_arrive(bar(B_KFULL + kb));
-                    cp_async_wait<0>();
-                    tc::fence_proxy_async_smem();
-                    tc::mbar_arrive(bar(B_VFULL + b));
-#pragma unroll
-                    for (int u = 0; u < RPT; ++u) cur[u] = nxt[u];
                 }
                 cp_async_wait<0>();
             }
