@@ -81,6 +81,14 @@ constexpr uint32_t kIdescS = tc::idesc_f16(kPM, kPN, false);
 constexpr uint32_t kIdescPV = tc::idesc_f16(kPM, kPD, true);
 constexpr float kRescaleLog2 = 8.0f;            // rescale O only when the max grows by > 2^8
 
+// fp16 row lists (MODE 2): warps per operand, and how many of a lane's copy
+// instructions for tile j go out before tile j-1 is published (the rest
+// follow).  Measured on 8 x 64 tokens over 32768 listed rows: one warp per
+// operand 0.59 ms, two 0.50 ms with all 32 copies first; then 16 first 0.41
+// ms, 8 first 0.41 ms, none first (one tile in flight) 0.46 ms.  Four warps
+// per operand would cap every thread at 96 registers.
+constexpr int kRowWarps = 2;
+constexpr int kPubAfter = 16;
 // Producer warps and thread count per mode (MODE 0: TMA tiles, MODE 1:
 // quantised rows converted by software, MODE 2: fp16 row lists by cp.async).
 template <int MODE>
@@ -94,15 +102,15 @@ struct Cfg {
     // caps every thread at 128 registers, and the producers' throughput is
     // worth more than the softmax's spare registers (two producer warps: 1.6x
     // the kernel time).
-    static constexpr int kProducerWarps = MODE == 0 ? 2 : 4;
+    static constexpr int kProducerWarps = MODE == 0 ? 2 : (MODE == 1 ? 4 : 2 * kRowWarps);
     static constexpr int kMmaWarp = kSoftmaxWarps + kProducerWarps;
     static constexpr int kThreads = (kMmaWarp + 1) * 32;
     // arrivals that fill a K or V stage: the TMA thread's expect-tx, every
     // producer thread (MODE 1), or the threads of the operand's two warps
-    static constexpr uint32_t kFullCount = MODE == 0 ? 1 : (MODE == 1 ? kProducerWarps * 32 : 64);
+    static constexpr uint32_t kFullCount = MODE == 0 ? 1 : (MODE == 1 ? kProducerWarps * 32 : kRowWarps * 32);
     // arrivals on a row-list padding mask: the producer threads, or (MODE 2)
     // the two K warps
-    static constexpr uint32_t kMaskCount = MODE == 2 ? 64 : kProducerWarps * 32;
+    static constexpr uint32_t kMaskCount = MODE == 2 ? kRowWarps * 32 : kProducerWarps * 32;
 };
 
 // barrier slots (8 bytes each) inside the barrier area
@@ -411,52 +419,68 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
             // and PV(j - 4) is issued before S(j - 2), whose completion freed
             // the K slot.
             static_assert(KT == SKV_F16 && VT == SKV_F16, "fp16 rows");
-            const int pw = warp - kSoftmaxWarps;          // 0, 1: K; 2, 3: V
-            const bool is_v = pw >= 2;
-            const int rbase = (pw & 1) * 64;              // first tile row of this warp
+            constexpr int W = kRowWarps;               // warps per operand
+            constexpr int RW = kPN / W;                   // rows a warp copies
+            constexpr int NH = RW / 32;                   // list entries a lane holds
+            const int pw = warp - kSoftmaxWarps;          // 0 .. W-1: K; W .. 2W-1: V
+            const bool is_v = pw >= W;
+            const int rbase = (pw % W) * RW;              // first tile row of this warp
             const uint8_t *base = is_v ? a.v : a.k;
             const int64_t row_bytes = is_v ? a.v_row_bytes : a.k_row_bytes;
             const uint8_t *seg0 = base + static_cast<int64_t>(kh) * (kPD * 2) + 16 * (lane & 15);
             const uint32_t ring = sbase + (is_v ? kOffV : kOffK);
             const int b_empty = is_v ? B_VEMPTY : B_KEMPTY, b_full = is_v ? B_VFULL : B_KFULL;
-            auto entry = [&](int j, int half) -> int {
-                const int64_t key = j_lo + static_cast<int64_t>(j) * kPN + rbase + 32 * half + lane;
+            auto entry = [&](int j, int h) -> int {
+                const int64_t key = j_lo + static_cast<int64_t>(j) * kPN + rbase + 32 * h + lane;
                 return (j < n_tiles && key < j_hi) ? __ldg(lrow + key) : -1;
             };
-            int cur0 = entry(0, 0), cur1 = entry(0, 1);
+            int cur[NH], nxt[NH];
+#pragma unroll
+            for (int h = 0; h < NH; ++h) cur[h] = entry(0, h);
             int issued = 0;
             for (int j = 0; j < n_tiles; ++j) {
                 const int b = j & 1;
-                const int nx0 = entry(j + 1, 0), nx1 = entry(j + 1, 1);
+#pragma unroll
+                for (int h = 0; h < NH; ++h) nxt[h] = entry(j + 1, h);
                 if (!__all_sync(0xffffffffu, j < 2 || wait(b_empty + b, ((j >> 1) - 1) & 1))) break;
                 if (!is_v) {
                     const int64_t key = j_lo + static_cast<int64_t>(j) * kPN + rbase + lane;
-                    const uint32_t w0 = __ballot_sync(0xffffffffu, cur0 >= 0 || key >= j_hi);
-                    const uint32_t w1 = __ballot_sync(0xffffffffu, cur1 >= 0 || key + 32 >= j_hi);
-                    if (lane == 0) {
-                        s_vmask[j & 3][rbase / 32] = w0;
-                        s_vmask[j & 3][rbase / 32 + 1] = w1;
+#pragma unroll
+                    for (int h = 0; h < NH; ++h) {
+                        const uint32_t w = __ballot_sync(0xffffffffu, cur[h] >= 0 || key + 32 * h >= j_hi);
+                        if (lane == 0) s_vmask[j & 3][rbase / 32 + h] = w;
                     }
                     __syncwarp();
                     tc::mbar_arrive(bar(B_MFULL + (j & 3)));
                 }
                 const uint32_t tile_s = ring + static_cast<uint32_t>(b * kTileBytes);
-#pragma unroll
-                for (int it = 0; it < 32; ++it) {
-                    const int rr = 2 * it + (lane >> 4);      // row of this warp's 64
-                    const int row = __shfl_sync(0xffffffffu, it < 16 ? cur0 : cur1, rr & 31);
+                auto copy = [&](int it) {
+                    const int rr = 2 * it + (lane >> 4);      // row of this warp's RW
+                    const int row = __shfl_sync(0xffffffffu, cur[it / 16], rr & 31);
                     cp_async16(tile_s + tile_off(rbase + rr, lane & 15),
                                row >= 0 ? seg0 + static_cast<int64_t>(row) * row_bytes : base, row >= 0 ? 16 : 0);
+                };
+                // The first PUB copy instructions of tile j go out before tile
+                // j-1 is published (so that the S MMA of tile j-1 does not wait
+                // for all of them), the rest after.
+                constexpr int PUB = kPubAfter;
+                if (PUB > 0) {
+#pragma unroll
+                    for (int it = 0; it < PUB; ++it) copy(it);
+                    cp_async_commit();
                 }
-                cp_async_commit();
                 if (j >= 1) {
-                    cp_async_wait<1>();                       // this thread's copies of tile j-1
+                    if (PUB > 0) cp_async_wait<1>();          // this thread's copies of tile j-1
+                    else cp_async_wait<0>();
                     tc::fence_proxy_async_smem();
                     tc::mbar_arrive(bar(b_full + ((j - 1) & 1)));
                 }
+#pragma unroll
+                for (int it = PUB; it < RW / 2; ++it) copy(it);
+                cp_async_commit();
                 ++issued;
-                cur0 = nx0;
-                cur1 = nx1;
+#pragma unroll
+                for (int h = 0; h < NH; ++h) cur[h] = nxt[h];
             }
             cp_async_wait<0>();
             if (issued == n_tiles && issued > 0) {
