@@ -509,9 +509,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                 return row >= 0 ? a.v + row * a.v_row_bytes + static_cast<int64_t>(kh) * SEGV : nullptr;
             };
             // Row-list mode: tile j's key-present bits (a list row, or past the
-            // split, masked there) to shared memory for the softmax.  Slot j % 4
-            // was last read by the softmax of tile j - 4, which is done once
-            // PV(j - 2) is (the V slot of tile j is free).
+            // split, masked there) to shared memory for the softmax.
             auto publish_mask = [&](int j, const int64_t (&rw)[RPT]) {
                 if (!lrow) return;
                 uint32_t present[RPT];
@@ -573,6 +571,11 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                     const bool k_ok = KLO ? (j < 1 || wait(B_KEMPTY, (j - 1) & 1))
                                           : (j < 2 || wait(B_KEMPTY + b, ((j >> 1) - 1) & 1));
                     if (!__all_sync(0xffffffffu, k_ok)) break;
+                    // The mask slot of tile j is free here: S(j-1) is issued
+                    // after PV(j-3), and so after the softmax of tile j-3 (and
+                    // of j-4) has read its mask.  K is published as soon as it
+                    // is stored, so S(j) never waits for the V slot.
+                    publish_mask(j, e0);
 #pragma unroll
                     for (int u = 0; u < RPT; ++u) {
                         const int r = r0 + u * NPT;
@@ -581,8 +584,9 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                         for (int i = 0; i < QSeg<KT>::NW; ++i) w[i] = *reinterpret_cast<const uint32_t *>(raw_k(slot, r) + 4 * i);
                         store_row<KT, KLO>(w, e0[u] >= 0, sm + kOffK + kb * kTileBytes, r, sm + kOffK + kTileBytes);
                     }
+                    tc::fence_proxy_async_smem();
+                    tc::mbar_arrive(bar(B_KFULL + kb));
                     if (!__all_sync(0xffffffffu, j < 2 || wait(B_VEMPTY + b, ((j >> 1) - 1) & 1))) break;
-                    publish_mask(j, e0);
 #pragma unroll
                     for (int u = 0; u < RPT; ++u) {
                         const int r = r0 + u * NPT;
@@ -592,7 +596,6 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                         store_row<VT>(w, e0[u] >= 0, sm + kOffV + b * kTileBytes, r);
                     }
                     tc::fence_proxy_async_smem();
-                    tc::mbar_arrive(bar(B_KFULL + kb));
                     tc::mbar_arrive(bar(B_VFULL + b));
 #pragma unroll
                     for (int u = 0; u < RPT; ++u) {
