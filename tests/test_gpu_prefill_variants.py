@@ -4,7 +4,8 @@
   causal positions and sub-ranges, and window + pinned quantised tail;
 * fp16 rows through per-sequence row lists with -1 padding (whole padding
   tiles included) for several sequences, and through per-KV-head lists;
-* quantised rows through row lists;
+* quantised rows through row lists; rows outside every list hold NaN bytes
+  and must never be read; a sub-range [kv_begin, kv_end) of longer lists;
 * the software producer writes the same operand tiles as the TMA producer: an
   identity row list reproduces the dense TMA result bit for bit.
 All against the oracle at the attention tolerance; the status word stays clear.
@@ -115,6 +116,56 @@ def test_prefill_row_lists(skv, h, oracle_mod, kt, vt):
                             q_pos=dev(q_pos))
     want_o, want_l = _oracle(oracle_mod, q, H, Hk, kt, vt, K, V, n_cache, n_keys=ld, kv_rows=rows, q_pos=q_pos)
     check_attention(o, l, want_o, want_l, vmax_of(oracle_mod, vt, V, D), "row-list prefill")
+    assert h.status() == 0
+
+
+@pytest.mark.parametrize("kt,vt", [(wl.F16, wl.F16), (wl.Q8_0, wl.Q4_0)])
+def test_prefill_row_lists_read_only_listed_rows(skv, h, oracle_mod, kt, vt):
+    """Every cache row that no list names is all 0xFF bytes (an fp16 NaN, a
+    NaN block scale): the result stays finite and equal to the oracle's, so
+    neither padding entries (-1, inside a list and at its end) nor tile or
+    split edges make the producers read a row outside the lists."""
+    rng = wl.generator(4, salt=600 + kt)
+    S, nq, H, Hk, n_cache = 2, 64, 32, 8, 5000
+    lens, ld = [1400, 1100], 1536
+    q = wl.normal_f16(rng, (S, nq, H, D))
+    K = wl.cache_rows(rng, kt, n_cache, Hk, D)
+    V = wl.cache_rows(rng, vt, n_cache, Hk, D)
+    rows = _lists(rng, n_cache, lens, ld)
+    rows[0, 300:420] = -1
+    listed = np.zeros(n_cache, dtype=bool)
+    listed[rows[rows >= 0]] = True
+    Kp, Vp = K.copy(), V.copy()
+    Kp[~listed] = 0xFF
+    Vp[~listed] = 0xFF
+    q_pos = np.stack([np.arange(nq, dtype=np.int32) + (n - nq) for n in lens]).astype(np.int32)
+    o, l = skv.attn_partial(h, dev(q), dev(Kp), dev(Vp), Hk=Hk, k_type=kt, v_type=vt, kv_rows=dev(rows),
+                            q_pos=dev(q_pos))
+    want_o, want_l = _oracle(oracle_mod, q, H, Hk, kt, vt, K, V, n_cache, n_keys=ld, kv_rows=rows, q_pos=q_pos)
+    check_attention(o, l, want_o, want_l, vmax_of(oracle_mod, vt, V, D), "row lists, NaN outside them")
+    assert h.status() == 0
+
+
+@pytest.mark.parametrize("kt,vt", [(wl.F16, wl.F16), (wl.Q4_0, wl.Q8_0)])
+def test_prefill_row_list_subrange(skv, h, oracle_mod, kt, vt):
+    """Entries [kv_begin, kv_end) of longer lists (both ends ragged against
+    the 128-key tiles, sequence 1's end in its padding), a ragged last query
+    tile (80 tokens x 4 heads), causal positions: the oracle takes the
+    sliced lists with the positions shifted by kv_begin."""
+    rng = wl.generator(4, salt=650 + kt)
+    S, nq, H, Hk, n_cache = 2, 80, 16, 4, 6000
+    lens, ld = [2900, 2500], 3000
+    b, e = 333, 2777
+    q = wl.normal_f16(rng, (S, nq, H, D))
+    K = wl.cache_rows(rng, kt, n_cache, Hk, D)
+    V = wl.cache_rows(rng, vt, n_cache, Hk, D)
+    rows = _lists(rng, n_cache, lens, ld)
+    q_pos = np.stack([np.arange(nq, dtype=np.int32) + (e - nq - 7 * s) for s in range(S)]).astype(np.int32)
+    o, l = skv.attn_partial(h, dev(q), dev(K), dev(V), Hk=Hk, k_type=kt, v_type=vt, kv_rows=dev(rows),
+                            kv_begin=b, kv_end=e, q_pos=dev(q_pos))
+    want_o, want_l = _oracle(oracle_mod, q, H, Hk, kt, vt, K, V, n_cache, n_keys=e - b,
+                             kv_rows=np.ascontiguousarray(rows[:, b:e]), q_pos=q_pos, key_pos0=b)
+    check_attention(o, l, want_o, want_l, vmax_of(oracle_mod, vt, V, D), "row-list sub-range")
     assert h.status() == 0
 
 
