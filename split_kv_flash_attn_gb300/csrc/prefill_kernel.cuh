@@ -488,15 +488,15 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                 tc::mbar_arrive(bar(b_full + ((issued - 1) & 1)));
             }
         } else {
-            // ---------------- software producers: kPN / NPT key rows a thread --
+            // ---------------- quantised rows: kPN / NPT key rows a thread -----
             // No wait may depend on a tile the producers have not published yet.
+            static_assert(KT != SKV_F16 && VT != SKV_F16, "quantised rows");
             constexpr int NPT = C::kProducerWarps * 32;      // producer threads
             constexpr int RPT = kPN / NPT;                   // rows per thread
             const int r0 = tid - kSoftmaxThreads;
-            constexpr int SEGK = KT == SKV_F16 ? 256 : (KT == SKV_Q8_0 ? 136 : 72);
-            constexpr int SEGV = VT == SKV_F16 ? 256 : (VT == SKV_Q8_0 ? 136 : 72);
-            // Cache row of key row r0 + u*NPT of tile j (-1: padding or past the split);
-            // list entries are fetched one tile ahead.
+            constexpr int SEGK = seg_bytes_of(KT), SEGV = seg_bytes_of(VT);
+            // Cache row of key row r0 + u*NPT of tile j (-1: padding or past
+            // the split).
             auto tile_row = [&](int j, int u) -> int64_t {
                 const int64_t key = j_lo + static_cast<int64_t>(j) * kPN + r0 + u * NPT;
                 if (key >= j_hi) return -1;
@@ -525,86 +525,83 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                 __syncwarp();
                 tc::mbar_arrive(bar(B_MFULL + (j & 3)));
             };
-            static_assert(KT != SKV_F16 && VT != SKV_F16, "quantised rows");
-            {
-                // Quantised rows: each thread's raw segments of tile j+1 are copied
-                // (cp.async, 8-byte pieces) into a staging slot while tile j is
-                // decoded from the other slot into the fp16 operand tiles.  A
-                // thread decodes exactly the rows it staged, so its own copy
-                // groups order everything; list entries run two tiles ahead.
-                uint8_t *raw = sm + kOffRaw;
-                constexpr int RAWK = kPN * SEGK, RAWV = kPN * SEGV;
-                auto raw_k = [&](int slot, int r) { return raw + slot * (RAWK + RAWV) + r * SEGK; };
-                auto raw_v = [&](int slot, int r) { return raw + slot * (RAWK + RAWV) + RAWK + r * SEGV; };
-                auto issue_raw = [&](int slot, const int64_t (&rw)[RPT]) {
-#pragma unroll
-                    for (int u = 0; u < RPT; ++u) {
-                        const int r = r0 + u * NPT;
-                        const uint8_t *ks = k_src(rw[u]);
-                        const uint8_t *vs = v_src(rw[u]);
-#pragma unroll
-                        for (int i = 0; i < SEGK / 8; ++i)
-                            cp_async8(smem_addr(raw_k(slot, r) + 8 * i), ks ? ks + 8 * i : a.k, ks ? 8 : 0);
-#pragma unroll
-                        for (int i = 0; i < SEGV / 8; ++i)
-                            cp_async8(smem_addr(raw_v(slot, r) + 8 * i), vs ? vs + 8 * i : a.v, vs ? 8 : 0);
-                    }
-                    cp_async_commit();
-                };
-                int64_t e0[RPT], e1[RPT];
+            // Each thread's raw segments of tile j+1 are copied
+            // (cp.async, 8-byte pieces) into a staging slot while tile j is
+            // decoded from the other slot into the fp16 operand tiles.  A
+            // thread decodes exactly the rows it staged, so its own copy
+            // groups order everything; list entries run two tiles ahead.
+            uint8_t *raw = sm + kOffRaw;
+            constexpr int RAWK = kPN * SEGK, RAWV = kPN * SEGV;
+            auto raw_k = [&](int slot, int r) { return raw + slot * (RAWK + RAWV) + r * SEGK; };
+            auto raw_v = [&](int slot, int r) { return raw + slot * (RAWK + RAWV) + RAWK + r * SEGV; };
+            auto issue_raw = [&](int slot, const int64_t (&rw)[RPT]) {
 #pragma unroll
                 for (int u = 0; u < RPT; ++u) {
-                    e0[u] = n_tiles > 0 ? tile_row(0, u) : -1;
-                    e1[u] = n_tiles > 1 ? tile_row(1, u) : -1;
+                    const int r = r0 + u * NPT;
+                    const uint8_t *ks = k_src(rw[u]);
+                    const uint8_t *vs = v_src(rw[u]);
+#pragma unroll
+                    for (int i = 0; i < SEGK / 8; ++i)
+                        cp_async8(smem_addr(raw_k(slot, r) + 8 * i), ks ? ks + 8 * i : a.k, ks ? 8 : 0);
+#pragma unroll
+                    for (int i = 0; i < SEGV / 8; ++i)
+                        cp_async8(smem_addr(raw_v(slot, r) + 8 * i), vs ? vs + 8 * i : a.v, vs ? 8 : 0);
                 }
-                if (n_tiles > 0) issue_raw(0, e0);
-                for (int j = 0; j < n_tiles; ++j) {
-                    const int b = j & 1;
-                    const int kb = KLO ? 0 : b;                      // K stage of this tile
-                    const int slot = j & 1;
-                    if (j + 1 < n_tiles) issue_raw(slot ^ 1, e1);
-                    int64_t e2[RPT];
+                cp_async_commit();
+            };
+            int64_t e0[RPT], e1[RPT];
 #pragma unroll
-                    for (int u = 0; u < RPT; ++u) e2[u] = j + 2 < n_tiles ? tile_row(j + 2, u) : -1;
-                    if (j + 1 < n_tiles) cp_async_wait<1>();        // this thread's segments of tile j landed
-                    else cp_async_wait<0>();
-                    const bool k_ok = KLO ? (j < 1 || wait(B_KEMPTY, (j - 1) & 1))
-                                          : (j < 2 || wait(B_KEMPTY + b, ((j >> 1) - 1) & 1));
-                    if (!__all_sync(0xffffffffu, k_ok)) break;
-                    // The mask slot of tile j is free here: S(j-1) is issued
-                    // after PV(j-3), and so after the softmax of tile j-3 (and
-                    // of j-4) has read its mask.  K is published as soon as it
-                    // is stored, so S(j) never waits for the V slot.
-                    publish_mask(j, e0);
-#pragma unroll
-                    for (int u = 0; u < RPT; ++u) {
-                        const int r = r0 + u * NPT;
-                        uint32_t w[QSeg<KT>::NW];
-#pragma unroll
-                        for (int i = 0; i < QSeg<KT>::NW; ++i) w[i] = *reinterpret_cast<const uint32_t *>(raw_k(slot, r) + 4 * i);
-                        store_row<KT, KLO>(w, e0[u] >= 0, sm + kOffK + kb * kTileBytes, r, sm + kOffK + kTileBytes);
-                    }
-                    tc::fence_proxy_async_smem();
-                    tc::mbar_arrive(bar(B_KFULL + kb));
-                    if (!__all_sync(0xffffffffu, j < 2 || wait(B_VEMPTY + b, ((j >> 1) - 1) & 1))) break;
-#pragma unroll
-                    for (int u = 0; u < RPT; ++u) {
-                        const int r = r0 + u * NPT;
-                        uint32_t w[QSeg<VT>::NW];
-#pragma unroll
-                        for (int i = 0; i < QSeg<VT>::NW; ++i) w[i] = *reinterpret_cast<const uint32_t *>(raw_v(slot, r) + 4 * i);
-                        store_row<VT>(w, e0[u] >= 0, sm + kOffV + b * kTileBytes, r);
-                    }
-                    tc::fence_proxy_async_smem();
-                    tc::mbar_arrive(bar(B_VFULL + b));
-#pragma unroll
-                    for (int u = 0; u < RPT; ++u) {
-                        e0[u] = e1[u];
-                        e1[u] = e2[u];
-                    }
-                }
-                cp_async_wait<0>();
+            for (int u = 0; u < RPT; ++u) {
+                e0[u] = n_tiles > 0 ? tile_row(0, u) : -1;
+                e1[u] = n_tiles > 1 ? tile_row(1, u) : -1;
             }
+            if (n_tiles > 0) issue_raw(0, e0);
+            for (int j = 0; j < n_tiles; ++j) {
+                const int b = j & 1;
+                const int kb = KLO ? 0 : b;                      // K stage of this tile
+                const int slot = j & 1;
+                if (j + 1 < n_tiles) issue_raw(slot ^ 1, e1);
+                int64_t e2[RPT];
+#pragma unroll
+                for (int u = 0; u < RPT; ++u) e2[u] = j + 2 < n_tiles ? tile_row(j + 2, u) : -1;
+                if (j + 1 < n_tiles) cp_async_wait<1>();        // this thread's segments of tile j landed
+                else cp_async_wait<0>();
+                const bool k_ok = KLO ? (j < 1 || wait(B_KEMPTY, (j - 1) & 1))
+                                      : (j < 2 || wait(B_KEMPTY + b, ((j >> 1) - 1) & 1));
+                if (!__all_sync(0xffffffffu, k_ok)) break;
+                // The mask slot of tile j is free here: S(j-1) is issued
+                // after PV(j-3), and so after the softmax of tile j-3 (and
+                // of j-4) has read its mask.  K is published as soon as it
+                // is stored, so S(j) never waits for the V slot.
+                publish_mask(j, e0);
+#pragma unroll
+                for (int u = 0; u < RPT; ++u) {
+                    const int r = r0 + u * NPT;
+                    uint32_t w[QSeg<KT>::NW];
+#pragma unroll
+                    for (int i = 0; i < QSeg<KT>::NW; ++i) w[i] = *reinterpret_cast<const uint32_t *>(raw_k(slot, r) + 4 * i);
+                    store_row<KT, KLO>(w, e0[u] >= 0, sm + kOffK + kb * kTileBytes, r, sm + kOffK + kTileBytes);
+                }
+                tc::fence_proxy_async_smem();
+                tc::mbar_arrive(bar(B_KFULL + kb));
+                if (!__all_sync(0xffffffffu, j < 2 || wait(B_VEMPTY + b, ((j >> 1) - 1) & 1))) break;
+#pragma unroll
+                for (int u = 0; u < RPT; ++u) {
+                    const int r = r0 + u * NPT;
+                    uint32_t w[QSeg<VT>::NW];
+#pragma unroll
+                    for (int i = 0; i < QSeg<VT>::NW; ++i) w[i] = *reinterpret_cast<const uint32_t *>(raw_v(slot, r) + 4 * i);
+                    store_row<VT>(w, e0[u] >= 0, sm + kOffV + b * kTileBytes, r);
+                }
+                tc::fence_proxy_async_smem();
+                tc::mbar_arrive(bar(B_VFULL + b));
+#pragma unroll
+                for (int u = 0; u < RPT; ++u) {
+                    e0[u] = e1[u];
+                    e1[u] = e2[u];
+                }
+            }
+            cp_async_wait<0>();
         }
     } else if (warp == C::kMmaWarp) {
         // ---------------- MMA issuer ----------------------------------------
