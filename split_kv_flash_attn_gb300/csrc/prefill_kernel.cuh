@@ -85,8 +85,9 @@ constexpr float kRescaleLog2 = 8.0f;            // rescale O only when the max g
 // instructions for tile j go out before tile j-1 is published (the rest
 // follow).  Measured on 8 x 64 tokens over 32768 listed rows: one warp per
 // operand 0.59 ms, two 0.50 ms with all 32 copies first; then 16 first 0.41
-// ms, 8 first 0.41 ms, none first (one tile in flight) 0.46 ms.  Four warps
-// per operand would cap every thread at 96 registers.
+// ms, 8 first 0.41 ms, none first (one tile in flight) 0.46 ms.  Three warps
+// per operand (rows 44/44/40) measured 0.41 ms too; four would cap every
+// thread at 96 registers.
 constexpr int kRowWarps = 2;
 constexpr int kPubAfter = 16;
 // Producer warps and thread count per mode (MODE 0: TMA tiles, MODE 1:
