@@ -235,12 +235,13 @@ int skv_attn_combine(skv_handle *h, int32_t n_parts, const float *o_parts, const
  * [n_win, n_win + n_tail) are rows of k_tail_host/v_tail_host, which must be
  * page-locked host memory (SKV_ENOTPINNED otherwise).  The tail is cut into
  * tiles of tile_rows rows (<= 0: skv_plan_tail_tile with 32768 target keys,
- * 2 ring slots within 512 MiB, 256-key blocks); each tile's raw bytes (any of the
+ * 4 ring slots within 512 MiB, 256-key blocks); each tile's raw bytes (any of the
  * three types) are copied in one cudaMemcpyAsync per K/V into a ring slot on
  * the handle's copy stream, while the window and earlier tiles compute on
- * `stream`; copy_done/compute_done events order slot reuse.  All partials
- * merge in one combine into o/lse.  Ring slots hold tile_rows rows and grow
- * only outside capture. */
+ * `stream`; copy_done/compute_done events order slot reuse.  The ring takes
+ * one slot per tile, at most 4 (during graph capture: the slots it already
+ * has).  All partials merge in one combine into o/lse.  Ring slots hold
+ * tile_rows rows and grow only outside capture. */
 int skv_attn_window_tail(skv_handle *h, const skv_shape *shape, const void *q,
                          const void *k_win, const void *v_win, int64_t n_win,
                          const void *k_tail_host, const void *v_tail_host, int64_t n_tail,

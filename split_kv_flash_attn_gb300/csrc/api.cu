@@ -502,8 +502,8 @@ int skv_attn_window_tail(skv_handle *h, const skv_shape *shape, const void *q, c
         // default: the tail-tile planner (32768-key tiles, the ring's slots
         // within 512 MiB, whole 256-key blocks)
         int32_t nt = 0;
-        if ((rc = skv_plan_tail_tile(n_tail, shape->k_row_bytes + shape->v_row_bytes, 2, int64_t(512) << 20, 32768,
-                                     256, &tile_rows, &nt)))
+        if ((rc = skv_plan_tail_tile(n_tail, shape->k_row_bytes + shape->v_row_bytes, SKV_MAX_SLOTS,
+                                     int64_t(512) << 20, 32768, 256, &tile_rows, &nt)))
             return fail(h, rc, "tail-tile planning failed");
     }
     if (tile_rows <= 0) tile_rows = 32768;
@@ -566,7 +566,13 @@ int skv_attn_window_tail(skv_handle *h, const skv_shape *shape, const void *q, c
     const size_t k_tile_bytes = static_cast<size_t>(tile_rows) * shape->k_row_bytes;
     const size_t v_off = round_up(k_tile_bytes, 256);
     const size_t slot_bytes = v_off + static_cast<size_t>(tile_rows) * shape->v_row_bytes;
-    const int n_slots = static_cast<int>(std::min<int64_t>(2, n_tt));
+    // One slot per tile, up to SKV_MAX_SLOTS (the Rolling KV patch's slot pool
+    // holds at most four; two is its default): with compute on `stream`
+    // held back by the window, two slots would leave the copy engine idle
+    // until the first tile's compute frees its slot.  During graph capture
+    // the ring's present slots serve (growth is refused there).
+    int n_slots = static_cast<int>(std::min<int64_t>(SKV_MAX_SLOTS, n_tt));
+    if (capturing(st) && h->n_ring > 0) n_slots = std::min(n_slots, h->n_ring);
     if (n_tt > 0 && (rc = ensure_ring(h, slot_bytes, n_slots, st))) return rc;
 
     DecodeArgs a = base_args(shape, G, n_cg, q, mask, mask_ld, q_pos, 0);
