@@ -84,19 +84,12 @@ def run_profile_case(name: str) -> int:
         q, k, v, qp = cu(w.q), cu(w.k), cu(w.v), cu(w.q_pos)
         call = lambda: skv.attn_partial(h, q, k, v, Hk=w.Hk, q_pos=qp)   # noqa: E731
     elif name == "prefill_q8q4_window":
-        rng = wl.generator(4, salt=77)
-        nq, H, Hk, D, n = 512, 32, 8, 128, 32768
-        q = cu(wl.normal_f16(rng, (1, nq, H, D)))
-        k, v = cu(wl.cache_rows(rng, wl.Q8_0, n, Hk, D)), cu(wl.cache_rows(rng, wl.Q4_0, n, Hk, D))
-        qp = torch.arange(n - nq, n, dtype=torch.int32, device="cuda").reshape(1, nq)
-        call = lambda: skv.attn_partial(h, q, k, v, Hk=Hk, k_type=wl.Q8_0, v_type=wl.Q4_0, q_pos=qp)   # noqa: E731
+        w = wl.prefill_quant_window()
+        q, k, v, qp = cu(w.q), cu(w.k), cu(w.v), cu(w.q_pos)
+        call = lambda: skv.attn_partial(h, q, k, v, Hk=w.Hk, k_type=w.k_type, v_type=w.v_type, q_pos=qp)   # noqa: E731
     elif name == "prefill_row_list":
-        w = wl.unified_decode()
-        rng = wl.generator(4, salt=77)
-        nq, n_list = 64, w.kv_rows.shape[1]
-        q = cu(wl.normal_f16(rng, (w.S, nq, w.H, w.D)))
-        k, v, rows = cu(w.k), cu(w.v), cu(w.kv_rows)
-        qp = (torch.arange(nq, dtype=torch.int32, device="cuda") + (n_list - nq)).repeat(w.S, 1).contiguous()
+        w = wl.prefill_row_lists()
+        q, k, v, rows, qp = cu(w.q), cu(w.k), cu(w.v), cu(w.kv_rows), cu(w.q_pos)
         call = lambda: skv.attn_partial(h, q, k, v, Hk=w.Hk, kv_rows=rows, q_pos=qp)   # noqa: E731
     else:
         rng = wl.generator(6, salt=7)
@@ -235,38 +228,60 @@ def job_throughput(bytes_per_rank: int, world: int, step_ms: float) -> float:
     return bytes_per_rank * world / (step_ms * 1e-3) / 1e9
 
 
+# ---------------------------------------------------------------- shared by both arms
+
+def workload_config(n_gpus: int) -> dict:
+    """The config dict both arms print (same workload, same keys)."""
+    return {"workload": WORKLOAD, "S": 8, "nq": 1, "H": 32, "Hk": 8, "D": 128, "n_cache": 262144,
+            "rows_per_seq": 32768, "kv_dtype": "f16",
+            "l2": "inputs larger than L2: 1 GiB of K/V gathered per step vs 126 MB L2",
+            "parallelism": f"replicas x{n_gpus}"}
+
+
+def time_oracle(w, n_warm: int, n_timed: int):
+    """The fp64 CPU oracle on the unified-cache workload, one sequence per
+    call (sequence i % 8 for call i), timed call by call on all host cores.
+    Returns (seconds of each timed call, K+V bytes one call gathers, threads)."""
+    import oracle
+    oracle.build()
+    bytes_per_seq = int((w.kv_rows[0] >= 0).sum()) * w.Hk * w.D * 2 * 2
+    times = []
+    for i in range(n_warm + n_timed):
+        s = i % w.S
+        t0 = time.perf_counter()
+        oracle.attention(w.q[s:s + 1], D=w.D, H=w.H, Hk=w.Hk, scale=w.scale, k0=w.k, v0=w.v,
+                         n_rows0=w.k.shape[0], k_row_bytes0=w.k.shape[1], v_row_bytes0=w.v.shape[1],
+                         n_keys=w.n_keys, kv_rows=w.kv_rows[s:s + 1])
+        if i >= n_warm:
+            times.append(time.perf_counter() - t0)
+    return times, bytes_per_seq, oracle.max_threads()
+
+
+def oracle_baseline(times, bytes_per_seq, threads) -> dict:
+    med = statistics.median(times)
+    return {"value": bytes_per_seq / med / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{len(times)} timed calls (after warm-up), each one of the 8 sequences in turn: 32 q heads x "
+                      f"32768 gathered rows x 8 KV heads ({bytes_per_seq} B of K+V); value from the median call",
+            "median_s": med, "min_s": min(times), "max_s": max(times), "cpu_model": cpu_model()}
+
+
 # ---------------------------------------------------------------- reference arm
 
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    import oracle
     from split_kv_flash_attn_gb300 import workloads as wl
-    oracle.build()
     w = wl.unified_decode()
-    cores = oracle.max_threads()
-    bytes_per_seq = w.kv_rows.shape[1] * w.Hk * w.D * 2 * 2
-    times = []
-    for i in range(args.warmup + args.steps):
-        s = i % w.S
-        t0 = time.perf_counter()
-        oracle.attention(w.q[s:s + 1], D=w.D, H=w.H, Hk=w.Hk, scale=w.scale, k0=w.k, v0=w.v,
-                         n_rows0=w.k.shape[0], k_row_bytes0=w.k.shape[1], v_row_bytes0=w.v.shape[1],
-                         n_keys=w.n_keys, kv_rows=w.kv_rows[s:s + 1])
-        if i >= args.warmup:
-            times.append(time.perf_counter() - t0)
-    sec = statistics.mean(times)
-    value = bytes_per_seq / sec / 1e9
-    sample = f"one of the 8 sequences per step (32768 rows x 8 KV heads x 32 q heads, {bytes_per_seq} B)"
+    times, bytes_per_seq, threads = time_oracle(w, args.warmup, args.steps)
+    cpu = oracle_baseline(times, bytes_per_seq, threads)
+    value = cpu["value"]
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": cpu["median_s"] * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "S": 8, "H": 32, "Hk": 8, "D": 128, "n_cache": 262144,
-                   "rows_per_seq": 32768},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample,
-                         "cpu_model": cpu_model()},
+        "config": workload_config(args.gpus),
+        "cpu_baseline": cpu,
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
     return 0
@@ -385,17 +400,7 @@ def main():
     cpu = None
     if rank == 0 and not args.no_cpu:
         try:
-            import oracle
-            oracle.build()
-            t0 = time.perf_counter()
-            oracle.attention(w.q[0:1], D=w.D, H=w.H, Hk=w.Hk, scale=w.scale, k0=w.k, v0=w.v,
-                             n_rows0=w.k.shape[0], k_row_bytes0=w.k.shape[1], v_row_bytes0=w.v.shape[1],
-                             n_keys=w.n_keys, kv_rows=w.kv_rows[0:1])
-            sec = time.perf_counter() - t0
-            sb = int((w.kv_rows[0] >= 0).sum()) * w.Hk * w.D * 4
-            cpu = {"value": sb / sec / 1e9, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
-                   "sample": f"sequence 0 of 8 (32 q heads x 32768 gathered rows, {sb} B), {sec:.2f} s",
-                   "cpu_model": cpu_model()}
+            cpu = oracle_baseline(*time_oracle(w, 1, 6))
         except Exception as exc:  # noqa: BLE001
             cpu = {"value": None, "unit": "GB/s", "cores": None, "kind": "oracle", "sample": repr(exc)[:200]}
 
@@ -409,10 +414,7 @@ def main():
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K_, "warmup": args.warmup,
         "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "S": w.S, "nq": 1, "H": w.H, "Hk": w.Hk, "D": w.D,
-                   "n_cache": w.k.shape[0], "rows_per_seq": 32768, "kv_dtype": "f16", "accumulate": "f32",
-                   "l2": "inputs larger than L2: 1 GiB of K/V gathered per step vs 126 MB L2",
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(world),
         "tokens_heads_per_s": tokens_heads * world / (step_ms * 1e-3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": traffic,
@@ -686,15 +688,15 @@ def bench_prefill_variants(torch, skv, wl, h):
         h.set_profile_events(None, None)
         return statistics.median(ks)
 
-    rng = wl.generator(4, salt=77)
-    nq, H, Hk, D, n = 512, 32, 8, 128, 32768
-    q = torch.from_numpy(wl.normal_f16(rng, (1, nq, H, D))).cuda()
-    K = torch.from_numpy(wl.cache_rows(rng, wl.Q8_0, n, Hk, D)).cuda()
-    V = torch.from_numpy(wl.cache_rows(rng, wl.Q4_0, n, Hk, D)).cuda()
-    qp = torch.arange(n - nq, n, dtype=torch.int32, device="cuda").reshape(1, nq)
+    wq = wl.prefill_quant_window()
+    nq, H, Hk, D, n = wq.nq, wq.H, wq.Hk, wq.D, wq.n_keys
+    q = torch.from_numpy(wq.q).cuda()
+    K = torch.from_numpy(wq.k).cuda()
+    V = torch.from_numpy(wq.v).cuda()
+    qp = torch.from_numpy(wq.q_pos).cuda()
     o = torch.empty((1, nq, H, D), dtype=torch.float32, device="cuda")
     lse = torch.empty((1, nq, H), dtype=torch.float32, device="cuda")
-    ms = kernel_ms(lambda: skv.attn_partial(h, q, K, V, Hk=Hk, k_type=wl.Q8_0, v_type=wl.Q4_0, q_pos=qp, o=o,
+    ms = kernel_ms(lambda: skv.attn_partial(h, q, K, V, Hk=Hk, k_type=wq.k_type, v_type=wq.v_type, q_pos=qp, o=o,
                                             lse=lse))
     pairs = float(np.arange(n - nq, n, dtype=np.int64).sum() + nq)
     flop = 4.0 * D * H * pairs
@@ -702,13 +704,13 @@ def bench_prefill_variants(torch, skv, wl, h):
                                    "frac_of_bf16_peak": flop / ms / 1e9 / bf16_peak,
                                    "bytes": K.numel() + V.numel()}
     del K, V
-    w = wl.unified_decode()
-    S, nq2 = w.S, 64
-    q2 = torch.from_numpy(wl.normal_f16(rng, (S, nq2, w.H, w.D))).cuda()
+    w = wl.prefill_row_lists()
+    S, nq2 = w.S, w.nq
+    q2 = torch.from_numpy(w.q).cuda()
     kc, vc = torch.from_numpy(w.k).cuda(), torch.from_numpy(w.v).cuda()
     rows = torch.from_numpy(w.kv_rows).cuda()
     n_list = w.kv_rows.shape[1]
-    qp2 = (torch.arange(nq2, dtype=torch.int32, device="cuda") + (n_list - nq2)).repeat(S, 1).contiguous()
+    qp2 = torch.from_numpy(w.q_pos).cuda()
     o2 = torch.empty((S, nq2, w.H, w.D), dtype=torch.float32, device="cuda")
     l2 = torch.empty((S, nq2, w.H), dtype=torch.float32, device="cuda")
     ms = kernel_ms(lambda: skv.attn_partial(h, q2, kc, vc, Hk=w.Hk, kv_rows=rows, q_pos=qp2, o=o2, lse=l2))

@@ -206,14 +206,18 @@ int skv_attn_partial(skv_handle *h, const skv_shape *shape,
  * in-kernel merge's arrival counters) is one 16 MiB array in device global
  * memory that every GPU loading this library holds until the process exits.
  * The first call on a device, made with that device current, looks up the
- * array's device address (cudaGetSymbolAddress); make that first call before
- * any stream capture.  Returns SKV_ENOMEM when the call needs more than the
- * array holds (more than 4096 sequence x KV-head x 8-column units, or split
- * partials beyond 16 MiB - 16 KiB) and SKV_EINVAL / SKV_EUNSUPPORTED for the
- * same argument errors as skv_attn_partial (there is no handle to carry a
- * message).  All calls share the one array: calls that overlap on the GPU
- * (different streams, or different host threads) race and must be ordered by
- * the caller.  The arrival counters are cleared on `stream` at every call. */
+ * array's device address (cudaGetSymbolAddress) and keeps it for the life of
+ * the process; make that first call before any stream capture, and do not call
+ * this entry point on a device after cudaDeviceReset (the kept address is then
+ * stale).  Maximum: 4096 sequence x KV-head x 8-column units (the arrival
+ * counters); a call with more returns SKV_ENOMEM.  When the planned key splits'
+ * partials would not fit the rest of the array, the call uses as many splits as
+ * fit (one split writes o/lse directly and needs no scratch).  SKV_EINVAL /
+ * SKV_EUNSUPPORTED for the same argument errors as skv_attn_partial (there is
+ * no handle to carry a message).  All calls share the one array: calls that
+ * overlap on the GPU (different streams, or different host threads) race and
+ * must be ordered by the caller.  The arrival counters are cleared on `stream`
+ * at every call that splits. */
 int skv_attn_partial_static(const skv_shape *shape, const void *q, const void *k, const void *v,
                             const void *mask, int64_t mask_ld, const int32_t *q_pos, int64_t key_pos0,
                             const int32_t *kv_rows, int64_t kv_rows_ld, int32_t kv_rows_per_head,
@@ -341,9 +345,10 @@ int skv_bcache_destroy(skv_bcache *c);
 int skv_bcache_reset(skv_bcache *c, void *stream);
 
 /* Make the pages named by sel (int32 block ids [S][Hk][n_sel], device) readable
- * in the pool: hits keep their slot; misses take a slot by a CLOCK sweep that
- * never evicts a page of this call, or an overflow page; then every missed page
- * is copied from the host copy.  page_ids [S][Hk][n_sel] (device; NULL = the
+ * in the pool: hits keep their slot; each missing page, however many lookups
+ * name it, takes one slot chosen by second chance (CLOCK) among the slots this
+ * call does not read, or -- when none is left -- an overflow page for this call
+ * only; then every missed page is copied from the host copy.  page_ids [S][Hk][n_sel] (device; NULL = the
  * cache's own buffer) receives the pool page of each lookup (-1 for a block id
  * out of range).  Runs entirely on `stream`, no host synchronisation. */
 int skv_bcache_resolve(skv_bcache *c, const int32_t *sel, int32_t S, int32_t n_sel, int32_t *page_ids, void *stream);
@@ -362,7 +367,8 @@ int skv_bcache_append(skv_bcache *c, const float *k_new, const float *v_new, con
                       void *stream);
 
 /* Resolve, then attention through the pool (skv_attn_paged with page_rows =
- * block_rows) for q of shape [S][nq][H][D]. */
+ * block_rows) for q of shape [S][nq][H][D] ("Strata compare", KV streaming:
+ * resolve, copy the missed blocks, attend), all on `stream`. */
 int skv_bcache_attn(skv_bcache *c, const skv_shape *shape, const void *q, const int32_t *sel, int32_t n_sel,
                     float *o, float *lse, void *stream);
 

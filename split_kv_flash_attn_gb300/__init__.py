@@ -194,9 +194,11 @@ def attn_combine(h: Handle, o_parts, lse_parts, *, o=None, lse=None, stream=None
 
 
 def attn_window_tail(h: Handle, q, k_win, v_win, k_tail_host, v_tail_host, *, Hk, n_win=None, n_tail=None,
-                     tile_rows=32768, k_type=F16, v_type=F16, k_row_bytes=None, v_row_bytes=None, scale=None,
+                     tile_rows=0, k_type=F16, v_type=F16, k_row_bytes=None, v_row_bytes=None, scale=None,
                      mask=None, q_pos=None, o=None, lse=None, stream=None):
-    """skv_attn_window_tail: window rows on the device, tail rows in pinned host memory."""
+    """skv_attn_window_tail: window rows on the device, tail rows in pinned host memory.
+
+    tile_rows <= 0 lets the library size the tail tiles (skv_plan_tail_tile)."""
     sh = _shape(q, Hk, k_type, v_type, k_row_bytes, v_row_bytes, scale)
     if n_win is None:
         n_win = int(k_win.shape[0]) if k_win is not None else 0

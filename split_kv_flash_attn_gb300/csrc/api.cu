@@ -92,6 +92,32 @@ int ensure_ring(skv_handle *h, size_t bytes_per_slot, int n_slots, cudaStream_t 
     return SKV_OK;
 }
 
+cudaError_t kernel_smem_optin(KernelAttrCache &c, const void *func, int smem, int threads, int *ctas)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kAttrDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(c.mu);
+    if (c.smem[dev] < smem) {
+        e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        c.smem[dev] = smem;
+    }
+    if (ctas) {
+        if (c.occ_smem[dev] != smem || c.occ_threads[dev] != threads) {
+            int n = 0;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, func, threads, smem);
+            if (e != cudaSuccess) return e;
+            c.occ_smem[dev] = smem;
+            c.occ_threads[dev] = threads;
+            c.occ_ctas[dev] = n;
+        }
+        *ctas = c.occ_ctas[dev];
+    }
+    return cudaSuccess;
+}
+
 int64_t segment_bytes(int type, int D)
 {
     switch (type) {

@@ -17,21 +17,50 @@
 // The block here is q8_0's 32 values (the page groups 64 values per scale;
 // the cache rows use the q8_0 block).  x / d is divided by the STORED fp16
 // scale, so d*q is the code nearest x.
+//
+// Both divisions are replaced by products with a reciprocal, with the exact
+// division kept for the few values where the two could decide differently:
+//  * the code: t0 = x * rcp(d), rcp correctly rounded, lies within 2^-23 |t0|
+//    of x/d, and the fp32 quotient fl(x/d) within 2^-17 of it for |x/d| < 256;
+//    so when t0 is more than 2^-14 away from every half-integer, rint(t0) =
+//    rint(fl(x/d)).  Nearer than that (about 1 value in 8000, and every exact
+//    tie), the code is taken from the IEEE division itself; |t0| >= 130 clamps
+//    either way.
+//  * the scale: s0 = amax * fl(1/qmax) lies within 2^-22.4 (relative) of
+//    fl(amax/qmax); when s0 (1 - 2^-20) and s0 (1 + 2^-20) round to the same
+//    fp16 value, so does fl(amax/qmax) (rounding is monotone); otherwise the
+//    scale comes from the IEEE division.
+// The stored bytes are therefore those of the plain fp32 rule, bit for bit.
 #include "internal.h"
 
 namespace skv {
-
-__device__ __forceinline__ float warp_max32(float v)
-{
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-    return v;
-}
 
 __device__ __forceinline__ uint32_t pack_half2(float a, float b)
 {
     const __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// fp16(fl(amax / qmax)) without a division unless the product could round
+// to another fp16 value (see the header).
+__device__ __forceinline__ __half block_scale(float amax, float qmax, float inv_qmax)
+{
+    const float s0 = __fmul_rn(amax, inv_qmax);
+    const __half h = __float2half_rn(s0);
+    const __half lo = __float2half_rn(__fmul_rn(s0, 1.f - 0x1p-20f));
+    const __half hi = __float2half_rn(__fmul_rn(s0, 1.f + 0x1p-20f));
+    if (__half_as_ushort(lo) == __half_as_ushort(h) && __half_as_ushort(hi) == __half_as_ushort(h)) return h;
+    return __float2half_rn(__fdiv_rn(amax, qmax));
+}
+
+// rint(fl(x / d)) for d > 0, rd = rcp_rn(d) (see the header).
+__device__ __forceinline__ int nearest_code(float x, float d, float rd)
+{
+    const float t0 = __fmul_rn(x, rd);
+    if (fabsf(t0) >= 130.f) return t0 > 0.f ? 1024 : -1024;       // clamped by every code range
+    const float r0 = rintf(t0);
+    if (0.5f - fabsf(t0 - r0) > 0x1p-14f) return static_cast<int>(r0);
+    return __float2int_rn(__fdiv_rn(x, d));
 }
 
 // Each warp takes kItemsPerWarp consecutive (row, head) items: it loads all of
@@ -60,18 +89,13 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(const float *
         p[it] = -1;
         if (item >= total) continue;
         p[it] = pos[item / Hk];
-        const float *src = x + item * DD;
-        if (T == SKV_F16) {                                       // values lane*VPL .. lane*VPL + VPL - 1
-            if (VPL == 4) {
-                const float4 a = reinterpret_cast<const float4 *>(src)[lane];
-                v[it][0] = a.x; v[it][1] = a.y; v[it][2] = a.z; v[it][3] = a.w;
-            } else {
-                const float2 a = reinterpret_cast<const float2 *>(src)[lane];
-                v[it][0] = a.x; v[it][1] = a.y;
-            }
-        } else {                                                  // value b*32 + lane of block b
-#pragma unroll
-            for (int b = 0; b < VPL; ++b) v[it][b] = src[b * 32 + lane];
+        const float *src = x + item * DD;                         // values lane*VPL .. lane*VPL + VPL - 1
+        if (VPL == 4) {
+            const float4 a = reinterpret_cast<const float4 *>(src)[lane];
+            v[it][0] = a.x; v[it][1] = a.y; v[it][2] = a.z; v[it][3] = a.w;
+        } else {
+            const float2 a = reinterpret_cast<const float2 *>(src)[lane];
+            v[it][0] = a.x; v[it][1] = a.y;
         }
     }
 #pragma unroll
@@ -98,31 +122,45 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(const float *
                 *reinterpret_cast<uint32_t *>(out) = pack_half2(v[it][0], v[it][1]);
             }
         } else {
+            // lane holds values j0 .. j0 + VPL - 1 of block b (LPB lanes per block)
             constexpr int BLK = T == SKV_Q8_0 ? 34 : 18;
+            constexpr int LPB = 32 / VPL;
             constexpr float QMAX = T == SKV_Q8_0 ? 127.f : 7.f;
-            uint8_t *seg = row + static_cast<int64_t>(h) * VPL * BLK;
+            constexpr float INV_QMAX = 1.f / QMAX;
+            const int b = lane / LPB, j0 = (lane % LPB) * VPL;
+            float amax = 0.f;
 #pragma unroll
-            for (int b = 0; b < VPL; ++b) {
-                const float xv = v[it][b];
-                const float amax = warp_max32(fabsf(xv));
-                const __half d16 = __float2half_rn(__fdiv_rn(amax, QMAX));
-                const float d = __half2float(d16);
-                const int q = d > 0.f ? __float2int_rn(__fdiv_rn(xv, d)) : 0;
-                uint8_t *blk = seg + b * BLK;                     // 2-byte aligned
-                if (T == SKV_Q8_0) {
-                    const int c = max(-127, min(127, q)) & 0xff;
-                    const int next = __shfl_down_sync(0xffffffffu, c, 1);
-                    if (!(lane & 1)) reinterpret_cast<uint16_t *>(blk + 2)[lane >> 1] = static_cast<uint16_t>(c | (next << 8));
-                } else {
-                    const int u = max(0, min(15, q + 8));
-                    const int hi = __shfl_down_sync(0xffffffffu, u, 16);   // value j + 16: high nibble of byte j
-                    const int byte = u | (hi << 4);
-                    const int next = __shfl_down_sync(0xffffffffu, byte, 1);
-                    if (lane < 16 && !(lane & 1))
-                        reinterpret_cast<uint16_t *>(blk + 2)[lane >> 1] = static_cast<uint16_t>(byte | (next << 8));
-                }
-                if (lane == 0) *reinterpret_cast<__half *>(blk) = d16;
+            for (int i = 0; i < VPL; ++i) amax = fmaxf(amax, fabsf(v[it][i]));
+#pragma unroll
+            for (int off = LPB / 2; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+            const __half d16 = block_scale(amax, QMAX, INV_QMAX);
+            const float d = __half2float(d16);
+            const float rd = d > 0.f ? __frcp_rn(d) : 0.f;
+            uint32_t packed = 0;                                  // VPL code bytes / nibbles, value j0 + i in byte i
+#pragma unroll
+            for (int i = 0; i < VPL; ++i) {
+                const int q = d > 0.f ? nearest_code(v[it][i], d, rd) : 0;
+                const uint32_t c = T == SKV_Q8_0 ? static_cast<uint32_t>(max(-127, min(127, q)) & 0xff)
+                                                 : static_cast<uint32_t>(max(0, min(15, q + 8)));
+                packed |= c << (8 * i);
             }
+            uint8_t *blk = row + static_cast<int64_t>(h) * VPL * BLK + b * BLK;   // 2-byte aligned
+            if (T == SKV_Q8_0) {
+                uint16_t *dst = reinterpret_cast<uint16_t *>(blk + 2 + j0);
+#pragma unroll
+                for (int w = 0; w < VPL / 2; ++w) dst[w] = static_cast<uint16_t>(packed >> (16 * w));
+            } else {
+                // byte j holds value j (low nibble) and value j + 16 (high
+                // nibble): the lane LPB/2 further on holds values j0 + 16 ..
+                const uint32_t high = __shfl_down_sync(0xffffffffu, packed, LPB / 2);
+                if (j0 < 16) {
+                    const uint32_t bytes = packed | (high << 4);
+                    uint16_t *dst = reinterpret_cast<uint16_t *>(blk + 2 + j0);
+#pragma unroll
+                    for (int w = 0; w < VPL / 2; ++w) dst[w] = static_cast<uint16_t>(bytes >> (16 * w));
+                }
+            }
+            if (j0 == 0) *reinterpret_cast<__half *>(blk) = d16;
         }
     }
 }

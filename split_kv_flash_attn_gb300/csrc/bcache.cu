@@ -3,26 +3,42 @@
 // The host copy is paged [block][Hk][block_rows][D] fp16 (the identity layout
 // of "Strata compare", KV streaming, KvHostPools).  The cache unit is one
 // page = one (block, KV head): block_rows rows of K and of V.  The device pool
-// holds n_slots resident pages plus a per-call overflow area; page_ids map each
+// holds n_slots resident pages plus a per-call overflow area; page ids map each
 // selected (sequence, KV head, block) to a pool page.
 //
-// skv_bcache_resolve, on the device (capturable, no host round trip):
-//   1. lookups: a resident page gets this call's epoch and its reference bit;
-//      a missing page is claimed once (-1 -> -2, atomicCAS) into a miss list;
-//   2. victims: a second-chance (CLOCK) sweep from the hand picks one slot per
-//      miss, never a slot this call uses (epoch), clearing the reference bits
-//      it passes; the table is re-pointed (old page -> -1, new page -> slot);
-//   3. misses without a slot (demand above capacity) go to the overflow area
-//      for this call only and stay non-resident;
-//   4. a copy kernel reads every missed page from the host copy (16-byte
-//      loads over the host link) into its pool page.
-// This follows the resolve / copy design of the Strata KV-streaming page, with
-// two readings of our own: the unit is a (block, KV head) page because the
-// selection is per KV head, and an oversubscribed call reads its excess misses
-// from the host once instead of failing.
+// The page's guarantees for a resolve are kept: a page this call reads is never
+// evicted by it, each missing page is claimed once however many lookups name
+// it, and victims are chosen by second chance (CLOCK).  The structure is this
+// library's own, three stream-ordered launches with no host round trip:
+//   lookup  (grid)   a resident page is stamped with the call's epoch and its
+//                    reference bit; a missing page records, by one atomic
+//                    maximum on its claim word, the first lookup that names it;
+//   claim + victims + placement  (1 CTA)  the missed pages are listed in the
+//                    order of their first lookups (a block scan over the
+//                    lookups), so every decision below is deterministic; every
+//                    slot is classed, in hand order, as in use by this call,
+//                    cold (free or unreferenced) or warm (referenced), and one
+//                    scan of the class counts gives the whole sweep at once --
+//                    the first `need` cold slots, then (when the cold ones run
+//                    out, after the hand has passed and cleared every warm
+//                    slot) warm slots in hand order; misses beyond cold + warm
+//                    go to the overflow area, decided here once for the call;
+//                    victims are re-pointed (old page -> -1, new page -> slot);
+//   fetch + ids  (persistent grid)  every missed page is copied from the host
+//                    copy into its pool page over the host link, and every
+//                    lookup gets its pool page id.
+// Attention then reads the pages through the ids.  (Attending to the pages
+// resident at entry while the misses stream, with the partial results merged
+// afterwards, was measured and not kept: an attention launch over a page list
+// costs nearly as much when most of its pages are absent, so the part left
+// after the fetch did not shrink.)  Two readings of our own: the unit is a
+// (block, KV head) page because the selection is per KV head, and an
+// oversubscribed call reads its excess misses from the host once instead of
+// failing.
 #include <string.h>
 
 #include <algorithm>
+#include <cub/block/block_scan.cuh>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -38,13 +54,15 @@ struct skv_bcache {
     int64_t page_bytes = 0;
     uint8_t *host_k = nullptr;         // device-accessible addresses of the pinned host copy
     uint8_t *host_v = nullptr;
-    int32_t *page_table = nullptr;     // [n_blocks*Hk] slot, -1, or transient markers
+    int32_t *page_table = nullptr;     // [n_blocks*Hk] slot or -1
+    uint64_t *page_claim = nullptr;    // [n_blocks*Hk] epoch << 32 | ~lookup of the call that last missed the page
+    int32_t *page_miss = nullptr;      // [n_blocks*Hk] its index in that call's miss list
     int32_t *slot_page = nullptr;      // [n_slots]
-    int32_t *slot_epoch = nullptr;     // [n_slots]
-    int32_t *slot_ref = nullptr;       // [n_slots]
+    int32_t *slot_epoch = nullptr;     // [n_slots] epoch of the last call that used the slot
+    int32_t *slot_ref = nullptr;       // [n_slots] reference bit
+    int32_t *victim = nullptr;         // [n_slots] slots chosen for this call's misses, in order
     int32_t *miss_page = nullptr;      // [max_lookups]
-    int32_t *miss_dest = nullptr;      // [max_lookups]
-    int32_t *miss_slot = nullptr;      // [n_slots]
+    int32_t *miss_dest = nullptr;      // [max_lookups] pool page each miss is fetched into
     int32_t *page_ids = nullptr;       // [max_lookups] of the last resolve
     uint64_t *ctl = nullptr;           // kCtlWords, see below
     int32_t *check = nullptr;          // invariant-violation counter
@@ -55,186 +73,274 @@ struct skv_bcache {
 
 namespace skv {
 
-// ctl words (uint64): 0 epoch, 1 hand, 2 calls, 3 lookups, 4 hits, 5 misses,
-// 6 overflow, 7 last misses, 8 last overflow, 9 pages to fetch.
+// ctl words (uint64): 0 epoch of the last resolve, 1 hand, 2 calls, 3 lookups,
+// 4 hits, 5 misses, 6 overflow, 7 last misses, 8 last overflow, 9 pages a ring
+// restore fetches, 11 misses placed in slots by the last resolve, 12 misses of
+// the last resolve.
 constexpr int kCtlWords = 16;
-constexpr int kResolveThreads = 1024;
+constexpr int kVictimThreads = 512;
 
-__device__ __forceinline__ int block_exclusive_scan(int v, int *warp_sums, int &total)
-{
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    int x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-    }
-    if (lane == 31) warp_sums[w] = x;
-    __syncthreads();
-    if (w == 0) {
-        int t = warp_sums[lane];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, t, o);
-            if (lane >= o) t += y;
-        }
-        warp_sums[lane] = t;
-    }
-    __syncthreads();
-    total = warp_sums[31];
-    const int excl = x - v + (w > 0 ? warp_sums[w - 1] : 0);
-    __syncthreads();
-    return excl;
-}
-
-struct ResolveArgs {
-    const int32_t *sel;       // [S][Hk][n_sel] block ids
-    int S, n_sel, Hk;
-    int n_slots;
-    int64_t n_pages;          // n_blocks * Hk
-    int32_t *page_table, *slot_page, *slot_epoch, *slot_ref, *miss_page, *miss_dest, *miss_slot, *page_ids;
+struct ResolveState {
+    int32_t *page_table;
+    uint64_t *page_claim;
+    int32_t *page_miss;
+    int32_t *slot_page, *slot_epoch, *slot_ref, *victim;
+    int32_t *miss_page, *miss_dest;
     uint64_t *ctl;
+    int n_slots;
+    int64_t n_pages;
 };
 
-__global__ void __launch_bounds__(kResolveThreads) bcache_resolve_kernel(ResolveArgs a)
+__device__ __forceinline__ int64_t lookup_page(const int32_t *sel, int64_t e, int n_sel, int Hk, int64_t n_pages)
 {
-    __shared__ int s_nmiss, s_cut;
-    __shared__ int warp_sums[32];
-    __shared__ unsigned long long s_lookups, s_hits;
-    const int tid = threadIdx.x;
-    const int epoch = static_cast<int>(a.ctl[0]) + 1;
-    if (tid == 0) {
-        s_nmiss = 0;
-        s_lookups = 0;
-        s_hits = 0;
-    }
-    __syncthreads();
-    const int64_t n_look = static_cast<int64_t>(a.S) * a.Hk * a.n_sel;
-    // 1. lookups
-    unsigned long long hits = 0, looks = 0;
-    for (int64_t e = tid; e < n_look; e += kResolveThreads) {
-        const int k = static_cast<int>((e / a.n_sel) % a.Hk);
-        const int64_t blk = a.sel[e];
-        if (blk < 0 || blk * a.Hk + k >= a.n_pages) continue;    // rejected on the host; never indexes out
-        const int64_t p = blk * a.Hk + k;
-        ++looks;
-        const int v = a.page_table[p];
-        if (v >= 0) {
-            a.slot_epoch[v] = epoch;
-            a.slot_ref[v] = 1;
-            ++hits;
-        } else if (v == -1 && atomicCAS(a.page_table + p, -1, -2) == -1) {
-            a.miss_page[atomicAdd(&s_nmiss, 1)] = static_cast<int32_t>(p);
+    const int64_t b = sel[e];
+    const int64_t p = b * Hk + (e / n_sel) % Hk;
+    return (b < 0 || p >= n_pages) ? -1 : p;     // out-of-range ids are rejected here; never indexed
+}
+
+// Claim key of lookup e in call `epoch`: a later call, then an earlier lookup,
+// compares larger.
+__device__ __forceinline__ unsigned long long claim_key(int epoch, int64_t e)
+{
+    return (static_cast<unsigned long long>(static_cast<uint32_t>(epoch)) << 32) |
+           static_cast<unsigned long long>(0xffffffffu - static_cast<uint32_t>(e));
+}
+
+// Lookup pass (this call's epoch is one past the last resolve's).
+__global__ void __launch_bounds__(256) bcache_lookup_kernel(ResolveState r, const int32_t *__restrict__ sel,
+                                                            int64_t n_look, int n_sel, int Hk)
+{
+    const int epoch = static_cast<int>(r.ctl[0]) + 1;
+    unsigned looks = 0, hits = 0;
+    for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n_look;
+         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t p = lookup_page(sel, e, n_sel, Hk, r.n_pages);
+        if (p >= 0) {
+            ++looks;
+            const int s = r.page_table[p];
+            if (s >= 0) {
+                r.slot_epoch[s] = epoch;          // in use: no victim this call
+                r.slot_ref[s] = 1;
+                ++hits;
+            } else {
+                atomicMax(reinterpret_cast<unsigned long long *>(r.page_claim + p), claim_key(epoch, e));
+            }
         }
     }
-    atomicAdd(&s_lookups, looks);
-    atomicAdd(&s_hits, hits);
-    __syncthreads();
-    // 2. CLOCK victims: one slot per miss, never a slot used by this call.
-    const int need = s_nmiss;
-    const int n = a.n_slots;
-    int hand = static_cast<int>(a.ctl[1]);
-    int got = 0;
-    for (int scanned = 0; got < need && scanned < 2 * n + kResolveThreads; scanned += kResolveThreads) {
-        const int j = static_cast<int>((static_cast<int64_t>(hand) + tid) % n);
-        const bool in_window = tid < n;                          // a window never wraps onto itself
-        const bool current = in_window && a.slot_epoch[j] == epoch;
-        const bool cand = in_window && !current && (a.slot_page[j] < 0 || a.slot_ref[j] == 0);
-        int total = 0;
-        const int rank = block_exclusive_scan(cand ? 1 : 0, warp_sums, total);
-        const int want = need - got;
-        if (tid == 0) s_cut = min(n, kResolveThreads);
-        __syncthreads();
-        if (cand && rank == want - 1) s_cut = tid + 1;           // the hand stops after the last slot taken
-        __syncthreads();
-        const int cut = s_cut;
-        if (cand && rank < want) {
-            a.miss_slot[got + rank] = j;
-            a.slot_epoch[j] = epoch;                             // taken: a later window must not take it again
-        } else if (in_window && tid < cut && !current) {
-            a.slot_ref[j] = 0;                                   // second chance used up
-        }
-        got += min(total, want);
-        hand = static_cast<int>((static_cast<int64_t>(hand) + cut) % n);
-        __syncthreads();
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        looks += __shfl_xor_sync(0xffffffffu, looks, o);
+        hits += __shfl_xor_sync(0xffffffffu, hits, o);
     }
-    const int placed = min(got, need);
-    // 3. re-point the table; overflow misses get a transient marker
-    for (int m = tid; m < need; m += kResolveThreads) {
-        const int p = a.miss_page[m];
-        if (m < placed) {
-            const int sl = a.miss_slot[m];
-            const int old = a.slot_page[sl];
-            if (old >= 0) a.page_table[old] = -1;
-            a.slot_page[sl] = p;
-            a.slot_ref[sl] = 1;
-            a.page_table[p] = sl;
-            a.miss_dest[m] = sl;
-        } else {
-            a.page_table[p] = -3 - (m - placed);
-            a.miss_dest[m] = n + (m - placed);
-        }
-    }
-    __syncthreads();
-    // 4. page ids of every lookup
-    for (int64_t e = tid; e < n_look; e += kResolveThreads) {
-        const int k = static_cast<int>((e / a.n_sel) % a.Hk);
-        const int64_t blk = a.sel[e];
-        if (blk < 0 || blk * a.Hk + k >= a.n_pages) {
-            a.page_ids[e] = -1;
-            continue;
-        }
-        const int v = a.page_table[blk * a.Hk + k];
-        a.page_ids[e] = v >= 0 ? v : n + (-3 - v);
-    }
-    __syncthreads();
-    // 5. overflow pages are not resident after this call
-    for (int m = placed + tid; m < need; m += kResolveThreads) a.page_table[a.miss_page[m]] = -1;
-    if (tid == 0) {
-        a.ctl[0] = static_cast<uint64_t>(epoch);
-        a.ctl[1] = static_cast<uint64_t>(hand);
-        a.ctl[2] += 1;
-        a.ctl[3] += s_lookups;
-        a.ctl[4] += s_hits;
-        a.ctl[5] += static_cast<uint64_t>(need);
-        a.ctl[6] += static_cast<uint64_t>(need - placed);
-        a.ctl[7] = static_cast<uint64_t>(need);
-        a.ctl[8] = static_cast<uint64_t>(need - placed);
-        a.ctl[9] = static_cast<uint64_t>(need);
+    if ((threadIdx.x & 31) == 0 && looks) {
+        atomicAdd(reinterpret_cast<unsigned long long *>(r.ctl + 3), static_cast<unsigned long long>(looks));
+        atomicAdd(reinterpret_cast<unsigned long long *>(r.ctl + 4), static_cast<unsigned long long>(hits));
     }
 }
 
-// Copy every missed page (K and V) from the host copy into its pool page:
-// one CTA per page in turn, 16 bytes per thread per load, 4 loads in flight.
-__global__ void __launch_bounds__(256) bcache_fetch_kernel(const uint64_t *__restrict__ ctl,
-                                                           const int32_t *__restrict__ miss_page,
-                                                           const int32_t *__restrict__ miss_dest,
-                                                           const uint8_t *__restrict__ host_k,
-                                                           const uint8_t *__restrict__ host_v, uint8_t *pool_k,
-                                                           uint8_t *pool_v, int64_t page_bytes)
+// Claim, victim and placement pass, one CTA.
+//  1. Miss list: lookup e owns page p when p's claim word holds e's key (the
+//     first lookup of this call naming a missing p); owners are numbered in
+//     lookup order by a block scan, tile by tile.
+//  2. Victims: thread t owns hand-relative positions [t*per, (t+1)*per);
+//     position i is slot (hand + i) % n_slots.
+//  3. Placement (below).
+constexpr int kClaimItems = 16;
+__global__ void __launch_bounds__(kVictimThreads) bcache_victim_kernel(ResolveState r, const int32_t *__restrict__ sel,
+                                                                       int64_t n_look, int n_sel, int Hk)
 {
-    const int n_fetch = static_cast<int>(ctl[9]);
+    using Scan = cub::BlockScan<unsigned long long, kVictimThreads>;
+    __shared__ typename Scan::TempStorage scan_tmp;
+    __shared__ int s_stop;
+    const int epoch = static_cast<int>(r.ctl[0]) + 1;
+    // 1. the miss list in lookup order
+    int64_t need = 0;
+    for (int64_t t0 = 0; t0 < n_look; t0 += static_cast<int64_t>(kVictimThreads) * kClaimItems) {
+        const int64_t e0 = t0 + static_cast<int64_t>(threadIdx.x) * kClaimItems;
+        unsigned own = 0;                            // bit u: lookup e0 + u owns its page
+#pragma unroll
+        for (int u = 0; u < kClaimItems; ++u) {
+            const int64_t e = e0 + u;
+            if (e < n_look) {
+                const int64_t p = lookup_page(sel, e, n_sel, Hk, r.n_pages);
+                if (p >= 0 && r.page_claim[p] == claim_key(epoch, e)) own |= 1u << u;
+            }
+        }
+        unsigned long long before = 0, total = 0;
+        Scan(scan_tmp).ExclusiveSum(static_cast<unsigned long long>(__popc(own)), before, total);
+        int64_t m = need + static_cast<int64_t>(before);
+        for (int u = 0; u < kClaimItems; ++u) {
+            if (own & (1u << u)) {
+                const int32_t p = static_cast<int32_t>(lookup_page(sel, e0 + u, n_sel, Hk, r.n_pages));
+                r.miss_page[m] = p;
+                r.page_miss[p] = static_cast<int32_t>(m);
+                ++m;
+            }
+        }
+        need += static_cast<int64_t>(total);
+        __syncthreads();                             // scan_tmp is reused
+    }
+    // 2. victims
+    const int n = r.n_slots;
+    const int hand = static_cast<int>(r.ctl[1] % static_cast<uint64_t>(n));
+    const int per = (n + kVictimThreads - 1) / kVictimThreads;
+    const int i0 = min(n, static_cast<int>(threadIdx.x) * per), i1 = min(n, i0 + per);
+    auto slot_at = [&](int i) { return static_cast<int>((static_cast<int64_t>(hand) + i) % n); };
+    // 0: in use by this call, 1: cold (free or unreferenced), 2: warm (referenced)
+    auto class_of = [&](int j) {
+        if (r.slot_epoch[j] == epoch) return 0;
+        return (r.slot_page[j] < 0 || r.slot_ref[j] == 0) ? 1 : 2;
+    };
+    unsigned long long mine = 0;                 // cold count | warm count << 32
+    for (int i = i0; i < i1; ++i) {
+        const int c = class_of(slot_at(i));
+        mine += c == 1 ? 1ull : (c == 2 ? (1ull << 32) : 0ull);
+    }
+    unsigned long long before = 0, total = 0;
+    Scan(scan_tmp).ExclusiveSum(mine, before, total);
+    const int64_t n_cold = static_cast<int64_t>(total & 0xffffffffull), n_warm = static_cast<int64_t>(total >> 32);
+    const int64_t placed = min(need, n_cold + n_warm);
+    // The sweep wraps once the cold slots run out: the hand has then passed --
+    // and cleared -- every warm slot, and takes warm slots on its second round.
+    const bool wraps = need > n_cold;
+    const int64_t warm_taken = wraps ? placed - n_cold : 0;
+    if (threadIdx.x == 0) s_stop = -1;
+    __syncthreads();
+    int64_t rc = static_cast<int64_t>(before & 0xffffffffull), rw = static_cast<int64_t>(before >> 32);
+    for (int i = i0; i < i1; ++i) {
+        const int j = slot_at(i);
+        const int c = class_of(j);
+        if (c == 1) {
+            if (rc < need) {
+                r.victim[rc] = j;
+                if (rc == (wraps ? (warm_taken == 0 ? n_cold - 1 : -1) : need - 1)) s_stop = i;
+            }
+            ++rc;
+        } else if (c == 2) {
+            if (wraps) {
+                r.slot_ref[j] = 0;
+                if (rw < warm_taken) {
+                    r.victim[n_cold + rw] = j;
+                    if (rw == warm_taken - 1) s_stop = i;
+                }
+            }
+            ++rw;
+        }
+    }
+    __syncthreads();
+    const int stop = s_stop;
+    if (!wraps && stop >= 0) {
+        // one partial round: the warm slots before the stop lose their reference bit
+        for (int i = i0; i < min(i1, stop); ++i) {
+            const int j = slot_at(i);
+            if (class_of(j) == 2) r.slot_ref[j] = 0;
+        }
+    }
+    __syncthreads();                                 // victim[] complete
+    // 3. placement: miss m < placed takes victim[m]; the rest go to the
+    //    overflow area (pool page n_slots + m - placed), for this call only.
+    //    Each thread places kPlaceBatch misses at a time, all their loads
+    //    issued before any store.
+    constexpr int kPlaceBatch = 8;
+    for (int64_t m0 = threadIdx.x; m0 < need; m0 += static_cast<int64_t>(kVictimThreads) * kPlaceBatch) {
+        int pg[kPlaceBatch], vj[kPlaceBatch], old[kPlaceBatch];
+#pragma unroll
+        for (int u = 0; u < kPlaceBatch; ++u) {
+            const int64_t m = m0 + static_cast<int64_t>(u) * kVictimThreads;
+            pg[u] = m < need ? r.miss_page[m] : -1;
+            vj[u] = m < placed ? r.victim[m] : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < kPlaceBatch; ++u) old[u] = vj[u] >= 0 ? r.slot_page[vj[u]] : -1;
+#pragma unroll
+        for (int u = 0; u < kPlaceBatch; ++u) {
+            const int64_t m = m0 + static_cast<int64_t>(u) * kVictimThreads;
+            if (m >= need) continue;
+            if (vj[u] >= 0) {
+                const int j = vj[u];
+                if (old[u] >= 0) r.page_table[old[u]] = -1;   // a resident page no lookup of this call named
+                r.slot_page[j] = pg[u];
+                r.slot_ref[j] = 1;
+                r.slot_epoch[j] = epoch;
+                r.page_table[pg[u]] = j;
+                r.miss_dest[m] = j;
+            } else {
+                r.miss_dest[m] = static_cast<int32_t>(n + (m - placed));
+            }
+        }
+    }
+    if (threadIdx.x == 0) {
+        if (stop >= 0) r.ctl[1] = static_cast<uint64_t>((static_cast<int64_t>(hand) + stop + 1) % n);
+        r.ctl[0] = static_cast<uint64_t>(epoch);
+        r.ctl[2] += 1;
+        r.ctl[5] += static_cast<uint64_t>(need);
+        r.ctl[6] += static_cast<uint64_t>(need - placed);
+        r.ctl[7] = static_cast<uint64_t>(need);
+        r.ctl[8] = static_cast<uint64_t>(need - placed);
+        r.ctl[11] = static_cast<uint64_t>(placed);
+        r.ctl[12] = static_cast<uint64_t>(need);
+    }
+}
+
+// Fetch and ids pass, a persistent grid of one CTA per SM.
+//  * With sel != NULL, the pool page id of every lookup: its slot (hits, and
+//    misses placed in a slot by this call) or its overflow page.
+//  * Every page of the miss list (count entries) is copied from the host copy
+//    into its pool page: one warp per page in turn, each lane keeping 8 loads
+//    of 16 bytes in flight over the host link.
+constexpr int kFetchThreads = 256;
+__global__ void __launch_bounds__(kFetchThreads, 1) bcache_fetch_kernel(const uint64_t *__restrict__ count,
+                                                                        const int32_t *__restrict__ miss_page,
+                                                                        const int32_t *__restrict__ miss_dest,
+                                                                        const uint8_t *__restrict__ host_k,
+                                                                        const uint8_t *__restrict__ host_v,
+                                                                        uint8_t *pool_k, uint8_t *pool_v,
+                                                                        int64_t page_bytes, ResolveState r,
+                                                                        const int32_t *__restrict__ sel, int64_t n_look,
+                                                                        int n_sel, int Hk, int32_t *__restrict__ ids)
+{
+    if (sel) {
+        const uint32_t epoch = static_cast<uint32_t>(r.ctl[0]);
+        for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n_look;
+             e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+            const int64_t p = lookup_page(sel, e, n_sel, Hk, r.n_pages);
+            int32_t id = -1;
+            if (p >= 0)
+                id = (r.page_claim[p] >> 32) == epoch ? r.miss_dest[r.page_miss[p]]   // missed by this call
+                                                      : r.page_table[p];
+            ids[e] = id;
+        }
+    }
+    constexpr int kU = 4;
+    const int64_t n = static_cast<int64_t>(*count);
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     const int64_t n16 = page_bytes / 16;
-    for (int m = blockIdx.x; m < n_fetch; m += gridDim.x) {
+    for (int64_t m = warp; m < n; m += n_warps) {
         const int64_t src = static_cast<int64_t>(miss_page[m]) * page_bytes;
         const int64_t dst = static_cast<int64_t>(miss_dest[m]) * page_bytes;
         const uint4 *sk = reinterpret_cast<const uint4 *>(host_k + src);
         const uint4 *sv = reinterpret_cast<const uint4 *>(host_v + src);
         uint4 *dk = reinterpret_cast<uint4 *>(pool_k + dst);
         uint4 *dv = reinterpret_cast<uint4 *>(pool_v + dst);
-        for (int64_t i = threadIdx.x; i < n16; i += 2 * blockDim.x) {
-            const int64_t i2 = i + blockDim.x;
-            const uint4 a0 = sk[i], b0 = sv[i];
-            uint4 a1 = make_uint4(0, 0, 0, 0), b1 = a1;
-            if (i2 < n16) {
-                a1 = sk[i2];
-                b1 = sv[i2];
+        for (int64_t base = 0; base < n16; base += 32 * kU) {
+            uint4 a[kU], b[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int64_t i = base + u * 32 + lane;
+                if (i < n16) {
+                    a[u] = sk[i];
+                    b[u] = sv[i];
+                }
             }
-            dk[i] = a0;
-            dv[i] = b0;
-            if (i2 < n16) {
-                dk[i2] = a1;
-                dv[i2] = b1;
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int64_t i = base + u * 32 + lane;
+                if (i < n16) {
+                    dk[i] = a[u];
+                    dv[i] = b[u];
+                }
             }
         }
     }
@@ -283,12 +389,15 @@ __global__ void __launch_bounds__(256) bcache_append_kernel(const float *__restr
     }
 }
 
-__global__ void bcache_reset_kernel(int32_t *page_table, int64_t n_pages, int32_t *slot_page, int32_t *slot_epoch,
-                                    int32_t *slot_ref, int n_slots, uint64_t *ctl)
+__global__ void bcache_reset_kernel(int32_t *page_table, uint64_t *page_claim, int64_t n_pages, int32_t *slot_page,
+                                    int32_t *slot_epoch, int32_t *slot_ref, int n_slots, uint64_t *ctl)
 {
     const int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t st = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t i = i0; i < n_pages; i += st) page_table[i] = -1;
+    for (int64_t i = i0; i < n_pages; i += st) {
+        page_table[i] = -1;
+        page_claim[i] = 0;
+    }
     for (int64_t i = i0; i < n_slots; i += st) {
         slot_page[i] = -1;
         slot_epoch[i] = 0;
@@ -297,8 +406,8 @@ __global__ void bcache_reset_kernel(int32_t *page_table, int64_t n_pages, int32_
     if (i0 < kCtlWords) ctl[i0] = 0;
 }
 
-// Count violations of: page_table[p] = s >= 0  <=>  slot_page[s] = p, and no
-// page left at a transient marker (< -1).
+// Count violations of: page_table[p] = s >= 0  <=>  slot_page[s] = p, and
+// every entry either -1 or a slot.
 __global__ void bcache_check_kernel(const int32_t *page_table, int64_t n_pages, const int32_t *slot_page,
                                     int n_slots, int32_t *violations)
 {
@@ -371,6 +480,44 @@ __global__ void ring_check_kernel(const int32_t *page_table, int64_t n_pages, in
 
 }  // namespace skv
 
+namespace skv {
+
+// Resolve one selection on `st`: lookup, claim + victims + placement, then
+// fetch + ids (page ids into `ids`).
+static int bcache_resolve_launch(skv_bcache *c, const int32_t *sel, int32_t S, int32_t n_sel, int32_t *ids,
+                                 cudaStream_t st)
+{
+    skv_handle *h = c->h;
+    if (c->ring_blocks > 0) return fail(h, SKV_EUNSUPPORTED, "a ring cache has a static table and no resolve");
+    if (!sel || S <= 0 || n_sel <= 0) return fail(h, SKV_EINVAL, "bad selection");
+    const int64_t n_look = static_cast<int64_t>(S) * c->Hk * n_sel;
+    if (n_look > c->max_lookups)
+        return fail(h, SKV_EINVAL, "%lld lookups exceed max_lookups %lld", (long long)n_look,
+                    (long long)c->max_lookups);
+    ResolveState r;
+    r.page_table = c->page_table;
+    r.page_claim = c->page_claim;
+    r.page_miss = c->page_miss;
+    r.slot_page = c->slot_page;
+    r.slot_epoch = c->slot_epoch;
+    r.slot_ref = c->slot_ref;
+    r.victim = c->victim;
+    r.miss_page = c->miss_page;
+    r.miss_dest = c->miss_dest;
+    r.ctl = c->ctl;
+    r.n_slots = c->n_slots;
+    r.n_pages = c->n_blocks * c->Hk;
+    const unsigned g_look = static_cast<unsigned>(std::min<int64_t>((n_look + 255) / 256, 4 * h->sm_count));
+    bcache_lookup_kernel<<<g_look, 256, 0, st>>>(r, sel, n_look, n_sel, c->Hk);
+    bcache_victim_kernel<<<1, kVictimThreads, 0, st>>>(r, sel, n_look, n_sel, c->Hk);
+    bcache_fetch_kernel<<<h->sm_count, kFetchThreads, 0, st>>>(c->ctl + 12, c->miss_page, c->miss_dest, c->host_k,
+                                                               c->host_v, c->pool_k, c->pool_v, c->page_bytes, r, sel,
+                                                               n_look, n_sel, c->Hk, ids);
+    return cuda_fail(h, cudaGetLastError(), "resolve launch");
+}
+
+}  // namespace skv
+
 using namespace skv;
 
 extern "C" {
@@ -384,7 +531,9 @@ int skv_bcache_destroy(skv_bcache *c)
     cudaFree(c->slot_ref);
     cudaFree(c->miss_page);
     cudaFree(c->miss_dest);
-    cudaFree(c->miss_slot);
+    cudaFree(c->page_claim);
+    cudaFree(c->page_miss);
+    cudaFree(c->victim);
     cudaFree(c->page_ids);
     cudaFree(c->ctl);
     cudaFree(c->check);
@@ -404,7 +553,7 @@ int skv_bcache_reset(skv_bcache *c, void *stream)
                                                                             c->n_slots, c->ctl);
     else
         bcache_reset_kernel<<<256, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-            c->page_table, n_pages, c->slot_page, c->slot_epoch, c->slot_ref, c->n_slots, c->ctl);
+            c->page_table, c->page_claim, n_pages, c->slot_page, c->slot_epoch, c->slot_ref, c->n_slots, c->ctl);
     return cuda_fail(c->h, cudaGetLastError(), "block-cache reset");
 }
 
@@ -453,12 +602,14 @@ static int bcache_create_impl(skv_handle *h, int64_t n_blocks, int32_t block_row
         if (e == cudaSuccess) e = cudaMalloc(p, bytes);
     };
     A(reinterpret_cast<void **>(&c->page_table), sizeof(int32_t) * n_pages);
+    A(reinterpret_cast<void **>(&c->page_claim), sizeof(uint64_t) * n_pages);
+    A(reinterpret_cast<void **>(&c->page_miss), sizeof(int32_t) * n_pages);
     A(reinterpret_cast<void **>(&c->slot_page), sizeof(int32_t) * n_slots);
     A(reinterpret_cast<void **>(&c->slot_epoch), sizeof(int32_t) * n_slots);
     A(reinterpret_cast<void **>(&c->slot_ref), sizeof(int32_t) * n_slots);
     A(reinterpret_cast<void **>(&c->miss_page), sizeof(int32_t) * max_lookups);
     A(reinterpret_cast<void **>(&c->miss_dest), sizeof(int32_t) * max_lookups);
-    A(reinterpret_cast<void **>(&c->miss_slot), sizeof(int32_t) * n_slots);
+    A(reinterpret_cast<void **>(&c->victim), sizeof(int32_t) * n_slots);
     A(reinterpret_cast<void **>(&c->page_ids), sizeof(int32_t) * max_lookups);
     A(reinterpret_cast<void **>(&c->ctl), sizeof(uint64_t) * kCtlWords);
     A(reinterpret_cast<void **>(&c->check), sizeof(int32_t));
@@ -503,36 +654,9 @@ int skv_bcache_create_ring(skv_handle *h, int64_t n_blocks, int32_t block_rows, 
 int skv_bcache_resolve(skv_bcache *c, const int32_t *sel, int32_t S, int32_t n_sel, int32_t *page_ids, void *stream)
 {
     if (!c) return SKV_EINVAL;
-    skv_handle *h = c->h;
-    h->err[0] = 0;
-    if (c->ring_blocks > 0) return fail(h, SKV_EUNSUPPORTED, "a ring cache has a static table and no resolve");
-    if (!sel || S <= 0 || n_sel <= 0) return fail(h, SKV_EINVAL, "bad selection");
-    const int64_t n_look = static_cast<int64_t>(S) * c->Hk * n_sel;
-    if (n_look > c->max_lookups) return fail(h, SKV_EINVAL, "%lld lookups exceed max_lookups %lld",
-                                             (long long)n_look, (long long)c->max_lookups);
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    ResolveArgs a;
-    a.sel = sel;
-    a.S = S;
-    a.n_sel = n_sel;
-    a.Hk = c->Hk;
-    a.n_slots = c->n_slots;
-    a.n_pages = c->n_blocks * c->Hk;
-    a.page_table = c->page_table;
-    a.slot_page = c->slot_page;
-    a.slot_epoch = c->slot_epoch;
-    a.slot_ref = c->slot_ref;
-    a.miss_page = c->miss_page;
-    a.miss_dest = c->miss_dest;
-    a.miss_slot = c->miss_slot;
-    a.page_ids = page_ids ? page_ids : c->page_ids;
-    a.ctl = c->ctl;
-    bcache_resolve_kernel<<<1, kResolveThreads, 0, st>>>(a);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(h, e, "resolve launch");
-    bcache_fetch_kernel<<<2 * h->sm_count, 256, 0, st>>>(c->ctl, c->miss_page, c->miss_dest, c->host_k, c->host_v,
-                                                         c->pool_k, c->pool_v, c->page_bytes);
-    return cuda_fail(h, cudaGetLastError(), "fetch launch");
+    c->h->err[0] = 0;
+    return bcache_resolve_launch(c, sel, S, n_sel, page_ids ? page_ids : c->page_ids,
+                                 static_cast<cudaStream_t>(stream));
 }
 
 int skv_bcache_append(skv_bcache *c, const float *k_new, const float *v_new, const int32_t *positions, int32_t n,
@@ -629,8 +753,11 @@ extern "C" int skv_bcache_ring_restore(skv_bcache *c, int64_t n_keys, void *stre
                                           c->miss_page, c->miss_dest, c->slot_page, c->ctl);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return skv::cuda_fail(h, e, "ring restore launch");
-    bcache_fetch_kernel<<<2 * h->sm_count, 256, 0, st>>>(c->ctl, c->miss_page, c->miss_dest, c->host_k, c->host_v,
-                                                         c->pool_k, c->pool_v, c->page_bytes);
+    ResolveState none;
+    memset(&none, 0, sizeof(none));
+    bcache_fetch_kernel<<<h->sm_count, kFetchThreads, 0, st>>>(c->ctl + 9, c->miss_page, c->miss_dest, c->host_k,
+                                                               c->host_v, c->pool_k, c->pool_v, c->page_bytes, none,
+                                                               nullptr, 0, 0, 0, nullptr);
     return skv::cuda_fail(h, cudaGetLastError(), "ring fetch launch");
 }
 

@@ -644,16 +644,20 @@ __global__ void __launch_bounds__(128) splitkv_decode_kernel(const DecodeArgs a)
 }
 
 template <int D, int KT, int VT>
+KernelAttrCache &decode_attr_cache()
+{
+    static KernelAttrCache c;
+    return c;
+}
+
+template <int D, int KT, int VT>
 int launch_decode_t(skv_handle *h, const DecodeArgs &a, cudaStream_t st)
 {
     using C = DecodeCfg<D, KT, VT>;
-    static bool attr_done = false;   // per process; the attribute is per function, not per device
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(splitkv_decode_kernel<D, KT, VT>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::smem);
-        if (e != cudaSuccess) return cuda_fail(h, e, "cudaFuncSetAttribute(decode)");
-        attr_done = true;
-    }
+    cudaError_t e = kernel_smem_optin(decode_attr_cache<D, KT, VT>(),
+                                      reinterpret_cast<const void *>(splitkv_decode_kernel<D, KT, VT>), C::smem,
+                                      C::kThreads, nullptr);
+    if (e != cudaSuccess) return cuda_fail(h, e, "cudaFuncSetAttribute(decode)");
     if (a.Hk * a.n_cg > 65535 || a.n_splits > 65535 || a.S > 65535)
         return fail(h, SKV_EUNSUPPORTED, "grid too large: Hk*n_cg=%d splits=%d S=%d", a.Hk * a.n_cg, a.n_splits, a.S);
     if (a.n_splits > kMaxSplits) return fail(h, SKV_EUNSUPPORTED, "%d splits exceed %d", a.n_splits, kMaxSplits);
@@ -666,19 +670,14 @@ template <int D, int KT, int VT>
 int decode_ctas_per_sm_t(skv_handle *h)
 {
     using C = DecodeCfg<D, KT, VT>;
-    static int cached = -1;
-    if (cached < 0) {
-        if (cudaFuncSetAttribute(splitkv_decode_kernel<D, KT, VT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::smem) != cudaSuccess)
-            return 0;
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, splitkv_decode_kernel<D, KT, VT>, C::kThreads,
-                                                          C::smem) != cudaSuccess)
-            return 0;
-        cached = n;
+    int n = 0;
+    if (kernel_smem_optin(decode_attr_cache<D, KT, VT>(), reinterpret_cast<const void *>(splitkv_decode_kernel<D, KT, VT>),
+                          C::smem, C::kThreads, &n) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
     }
     (void)h;
-    return cached;
+    return n;
 }
 
 }  // namespace skv

@@ -408,16 +408,20 @@ __global__ void __launch_bounds__(256) splitkv_decode_rows_kernel(const DecodeAr
 }
 
 template <int KT, int VT>
+KernelAttrCache &rows_attr_cache()
+{
+    static KernelAttrCache c;
+    return c;
+}
+
+template <int KT, int VT>
 int launch_rows_t(skv_handle *h, const DecodeArgs &a, cudaStream_t st)
 {
     const int smem = kRStages * static_cast<int>(rows_stage_bytes(a.k_row_bytes, a.v_row_bytes));
-    static int attr_smem = 0;   // per process: the attribute is per function
-    if (smem > attr_smem) {
-        cudaError_t e = cudaFuncSetAttribute(splitkv_decode_rows_kernel<KT, VT>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return cuda_fail(h, e, "cudaFuncSetAttribute(decode rows)");
-        attr_smem = smem;
-    }
+    cudaError_t e = kernel_smem_optin(rows_attr_cache<KT, VT>(),
+                                      reinterpret_cast<const void *>(splitkv_decode_rows_kernel<KT, VT>), smem,
+                                      32 * a.Hk, nullptr);
+    if (e != cudaSuccess) return cuda_fail(h, e, "cudaFuncSetAttribute(decode rows)");
     dim3 grid(static_cast<unsigned>(a.n_cg), static_cast<unsigned>(a.n_splits), static_cast<unsigned>(a.S));
     if (h->prof_before) cudaEventRecord(h->prof_before, st);
     splitkv_decode_rows_kernel<KT, VT><<<grid, 32 * a.Hk, smem, st>>>(a);
@@ -428,20 +432,13 @@ int launch_rows_t(skv_handle *h, const DecodeArgs &a, cudaStream_t st)
 template <int KT, int VT>
 int rows_ctas_t(int smem, int threads)
 {
-    static int cached_smem = -1, cached_threads = -1, cached = 0;
-    if (cached_smem != smem || cached_threads != threads) {
-        if (cudaFuncSetAttribute(splitkv_decode_rows_kernel<KT, VT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 smem) != cudaSuccess)
-            return 0;
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, splitkv_decode_rows_kernel<KT, VT>, threads, smem) !=
-            cudaSuccess)
-            return 0;
-        cached_smem = smem;
-        cached_threads = threads;
-        cached = n;
+    int n = 0;
+    if (kernel_smem_optin(rows_attr_cache<KT, VT>(), reinterpret_cast<const void *>(splitkv_decode_rows_kernel<KT, VT>),
+                          smem, threads, &n) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
     }
-    return cached;
+    return n;
 }
 
 }  // namespace

@@ -4,6 +4,7 @@
 
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <mutex>
 #include <stdarg.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -45,6 +46,23 @@ int ensure_workspace(skv_handle *h, size_t bytes, cudaStream_t stream);
 int ensure_ring(skv_handle *h, size_t bytes_per_slot, int n_slots, cudaStream_t stream);
 
 int64_t segment_bytes(int type, int D);
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) takes effect in the current
+// device's context only, so a kernel's opt-in (and the occupancy it gives) is
+// recorded per device.  One cache per kernel instance; host threads share it
+// under its mutex.
+constexpr int kAttrDevices = 64;
+struct KernelAttrCache {
+    std::mutex mu;
+    int smem[kAttrDevices] = {};       // dynamic shared memory opted in on each device
+    int occ_smem[kAttrDevices] = {};   // the (smem, threads) the cached occupancy was taken at
+    int occ_threads[kAttrDevices] = {};
+    int occ_ctas[kAttrDevices] = {};
+};
+// Opt `func` in to `smem` bytes of dynamic shared memory on the current device
+// (once per device and size).  With ctas != NULL, also store the CTAs of
+// `threads` threads resident per SM at that size.
+cudaError_t kernel_smem_optin(KernelAttrCache &c, const void *func, int smem, int threads, int *ctas);
 
 // How key indices of one launch map to cache rows.
 enum RowMode { ROWS_DENSE = 0, ROWS_LIST = 1, ROWS_PAGED = 2 };

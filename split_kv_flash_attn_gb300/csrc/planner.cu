@@ -2,18 +2,41 @@
 // resident in device memory (the window), and how large the streamed tail's
 // tiles are.  Pure integer logic; no GPU needed.
 //
-// Window ("Rolling KV -- position-windowed KV residency", the position-axis
-// residency sizing of the KV cache): budget = min(free, target) minus a
-// reserve; the whole cache stays resident when it fits; otherwise the window
-// is the largest cell count that fits, rounded down to the alignment (the
-// larger of the cache padding and 256, the attention kernels' key stride), no
-// smaller than one alignment step and leaving at least one step of tail.
+// Both answers are closed forms of the constraints the "Rolling KV --
+// position-windowed KV residency" page puts on them (position-axis residency
+// sizing; streaming forward's tile sizing):
 //
-// Tail tiles (same page, streaming forward's tile sizing): tiles of about
-// target_keys keys (32768 there, to keep launches few), enlarged in count
-// until n_slots slots of one tile fit the slot-memory cap (512 MiB there), at
-// most one tile per alignment block, each tile a whole number of blocks.
+//  window: the largest multiple of the alignment whose cells fit the budget,
+//          never below one alignment step, and -- when the cache is longer
+//          than one step -- never above the last aligned cell count that still
+//          leaves a whole step of tail.  The alignment is a multiple of both the
+//          cache padding and the attention kernels' 256-key stride, i.e. their
+//          least common multiple (the page takes the larger of the two, which
+//          is the same number for the power-of-two paddings it uses).
+//  tiles:  as many tiles as the larger of two demands -- one tile per target
+//          count of keys, and enough tiles that n_slots copies of one tile fit
+//          the slot-memory cap -- but no more tiles than alignment blocks; the
+//          blocks are then spread evenly, so every tile but the last holds the
+//          same whole number of blocks.
 #include "internal.h"
+
+namespace {
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int64_t gcd64(int64_t a, int64_t b)
+{
+    while (b) {
+        const int64_t r = a % b;
+        a = b;
+        b = r;
+    }
+    return a;
+}
+
+int64_t clamp64(int64_t x, int64_t lo, int64_t hi) { return x < lo ? lo : (x > hi ? hi : x); }
+
+}  // namespace
 
 extern "C" {
 
@@ -23,27 +46,24 @@ int skv_plan_window(int64_t per_cell_bytes, int64_t kv_size, int64_t free_bytes,
     if (!window_cells || per_cell_bytes < 0 || kv_size < 0 || free_bytes < 0 || target_bytes < 0 ||
         reserve_bytes < 0 || n_pad < 0)
         return SKV_EINVAL;
+    // Nothing to size: an empty cache, or cells that cost nothing.
     if (kv_size == 0 || per_cell_bytes == 0) {
         *window_cells = kv_size;
         return SKV_OK;
     }
-    int64_t budget = free_bytes;
-    if (target_bytes > 0 && target_bytes < budget) budget = target_bytes;
-    budget = budget > reserve_bytes ? budget - reserve_bytes : 0;
-    if (per_cell_bytes <= budget / kv_size) {          // per_cell * kv_size <= budget, without overflow
+    const int64_t cap = target_bytes > 0 ? (target_bytes < free_bytes ? target_bytes : free_bytes) : free_bytes;
+    const int64_t budget = cap > reserve_bytes ? cap - reserve_bytes : 0;
+    const int64_t fit = budget / per_cell_bytes;              // whole cells the budget holds
+    if (fit >= kv_size) {                                     // the whole cache stays resident
         *window_cells = kv_size;
         return SKV_OK;
     }
-    const int64_t pad = n_pad ? n_pad : 32;
-    const int64_t align = pad >= 256 ? pad : 256;
-    int64_t cells = budget / per_cell_bytes;
-    cells = cells / align * align;
-    if (cells < align) cells = align;
-    if (kv_size > align && cells > kv_size - align) {
-        cells = (kv_size - align) / align * align;
-        if (cells < align) cells = align;
-    }
-    *window_cells = cells;
+    const int64_t pad = n_pad > 0 ? n_pad : 32;
+    const int64_t step = pad / gcd64(pad, 256) * 256;         // lcm(pad, 256)
+    const int64_t lo = step;                                  // at least one step resident
+    const int64_t hi = kv_size > step ? (kv_size - step) / step * step : 0;   // a step of tail stays
+    const int64_t want = fit / step * step;
+    *window_cells = kv_size > step ? clamp64(want, lo, hi > lo ? hi : lo) : (want > lo ? want : lo);
     return SKV_OK;
 }
 
@@ -58,18 +78,17 @@ int skv_plan_tail_tile(int64_t n_keys, int64_t per_key_bytes, int32_t n_slots, i
         *n_tiles = 0;
         return SKV_OK;
     }
-    const int64_t n_blk = (n_keys + align - 1) / align;
-    int64_t tiles = (n_keys + target_keys - 1) / target_keys;
-    const int64_t denom = per_key_bytes * n_slots;
-    int64_t max_keys = denom == 0 ? n_keys : slot_cap_bytes / denom;
-    if (max_keys < align) max_keys = align;
-    const int64_t tiles_cap = (n_keys + max_keys - 1) / max_keys;
-    if (tiles < tiles_cap) tiles = tiles_cap;
-    if (tiles < 1) tiles = 1;
-    if (tiles > n_blk) tiles = n_blk;
-    const int64_t blk_per_tile = (n_blk + tiles - 1) / tiles;
-    const int64_t rows = blk_per_tile * align;
-    const int64_t count = (n_keys + rows - 1) / rows;
+    const int64_t blocks = ceil_div(n_keys, align);
+    // Most keys one tile may hold so that n_slots tiles fit the cap; a single
+    // alignment block is allowed even when it alone exceeds the cap.
+    const int64_t per_tile_slots = per_key_bytes * n_slots;
+    const int64_t cap_keys =
+        per_tile_slots == 0 ? n_keys : (slot_cap_bytes / per_tile_slots > align ? slot_cap_bytes / per_tile_slots : align);
+    const int64_t by_target = ceil_div(n_keys, target_keys);
+    const int64_t by_cap = ceil_div(n_keys, cap_keys);
+    const int64_t tiles = clamp64(by_target > by_cap ? by_target : by_cap, 1, blocks);
+    const int64_t rows = ceil_div(blocks, tiles) * align;     // blocks spread evenly
+    const int64_t count = ceil_div(n_keys, rows);
     if (count > 0x7fffffff) return SKV_EUNSUPPORTED;
     *tile_rows = rows;
     *n_tiles = static_cast<int32_t>(count);

@@ -883,18 +883,15 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
     if (tid == 0) a.counters[unit] = 0;
 }
 
-// Launch one instance (sets its shared-memory attribute once per process).
+// Launch one instance (its shared-memory opt-in is made once per device).
 template <int MODE, int KT, int VT>
 int launch_prefill_t(skv_handle *h, const CUtensorMap &mk, const CUtensorMap &mv, const PrefillArgs &a, dim3 grid,
                      cudaStream_t st)
 {
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(splitkv_prefill_kernel<MODE, KT, VT>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<KT, VT>());
-        if (e != cudaSuccess) return cuda_fail(h, e, "cudaFuncSetAttribute(prefill)");
-        attr_done = true;
-    }
+    static KernelAttrCache attrs;
+    cudaError_t e = kernel_smem_optin(attrs, reinterpret_cast<const void *>(splitkv_prefill_kernel<MODE, KT, VT>),
+                                      smem_bytes<KT, VT>(), Cfg<MODE>::kThreads, nullptr);
+    if (e != cudaSuccess) return cuda_fail(h, e, "cudaFuncSetAttribute(prefill)");
     if (h->prof_before) cudaEventRecord(h->prof_before, st);
     splitkv_prefill_kernel<MODE, KT, VT><<<grid, Cfg<MODE>::kThreads, smem_bytes<KT, VT>(), st>>>(mk, mv, a);
     if (h->prof_after) cudaEventRecord(h->prof_after, st);

@@ -28,7 +28,9 @@ constexpr int kStaticMaxDevices = 64;
 
 // Host code must not use this symbol's address directly: on the host it names
 // a stand-in, not device memory.  Its device address is looked up once per
-// device (cudaGetSymbolAddress) and passed to the kernels.
+// device (cudaGetSymbolAddress) and passed to the kernels.  The address is
+// kept for the life of the process: after cudaDeviceReset on a device it is
+// stale, so this entry point must not be called on a device that was reset.
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 std::mutex g_mu;
@@ -116,17 +118,29 @@ extern "C" int skv_attn_partial_static(const skv_shape *shape, const void *q, co
     const bool f16 = sh.k_type == SKV_F16;
     const int ctas = f16 ? decode_ctas_f16(nullptr, D) : decode_ctas_quant(nullptr, sh.k_type, sh.v_type, D);
     if (ctas <= 0) return SKV_EUNSUPPORTED;
+    // The stated maximum: one arrival counter per unit in the array's head.
+    if (units > kStaticUnits) return SKV_ENOMEM;
     int64_t split_len = 0;
     int32_t n_splits = 0;
     rc = skv_plan_splits(n_local, units, sm_count, ctas, kDecodeTile, 0, &split_len,
                          &n_splits);
     if (rc) return rc;
+    // The split count is free: when the planned splits' partials do not fit
+    // the array, use as many as fit (one split writes o/lse directly and
+    // needs no scratch at all).
+    const size_t per_split = size_t(R) * D * sizeof(float) + size_t(R) * sizeof(float);
+    const int64_t max_fit = int64_t((kStaticScratchBytes - kStaticCounterBytes - 256) / per_split);
+    if (n_splits > 1 && n_splits > max_fit) {
+        const int64_t want = max_fit > 1 ? max_fit : 1;
+        split_len = (n_local + want - 1) / want;
+        split_len = (split_len + kDecodeTile - 1) / kDecodeTile * kDecodeTile;
+        n_splits = static_cast<int32_t>((n_local + split_len - 1) / split_len);
+    }
     if (n_splits > kMaxSplits) return SKV_EUNSUPPORTED;
     // The fixed scratch: counters, then O partials, then lse partials.
     const size_t o_bytes = (size_t(n_splits) * R * D * sizeof(float) + 255) / 256 * 256;
     const size_t l_bytes = size_t(n_splits) * R * sizeof(float);
-    if (units > kStaticUnits || (n_splits > 1 && kStaticCounterBytes + o_bytes + l_bytes > kStaticScratchBytes))
-        return SKV_ENOMEM;   // this call needs more than the fixed scratch holds
+    if (n_splits > 1 && kStaticCounterBytes + o_bytes + l_bytes > kStaticScratchBytes) return SKV_ENOMEM;
 
     DecodeArgs a;
     memset(&a, 0, sizeof(a));

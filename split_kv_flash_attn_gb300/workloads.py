@@ -175,6 +175,32 @@ def prefill_chunk(n_kv: int = 65536, wc: int = 32768, nq: int = 512, H: int = 32
                     tile_rows=tile_rows, extra={"wc": wc, "n_kv": n_kv})
 
 
+def prefill_quant_window(n: int = 32768, nq: int = 512, H: int = 32, Hk: int = 8, D: int = 128,
+                         k_type: int = Q8_0, v_type: int = Q4_0, salt: int = 77) -> Workload:
+    """Prefill over quantised rows: nq causal tokens at positions n-nq .. n-1
+    over n q8_0-K / q4_0-V rows held on the device (the prefill chunk's shape
+    over the long-context workload's row types)."""
+    rng = generator(4, salt)
+    q = normal_f16(rng, (1, nq, H, D))
+    k = cache_rows(rng, k_type, n, Hk, D)
+    v = cache_rows(rng, v_type, n, Hk, D)
+    q_pos = (n - nq + np.arange(nq, dtype=np.int32)).reshape(1, nq)
+    return Workload("prefill_quant_window", 1, nq, H, Hk, D, k_type, v_type, q, k, v, q_pos=q_pos, n_keys=n)
+
+
+def prefill_row_lists(nq: int = 64, salt: int = 78, **unified) -> Workload:
+    """Prefill through row lists: the unified-cache workload's cache and lists
+    (``unified_decode(**unified)``), with nq causal tokens per sequence at the
+    last nq positions of its list."""
+    w = unified_decode(**unified)
+    rng = generator(4, salt)
+    q = normal_f16(rng, (w.S, nq, w.H, w.D))
+    n_list = w.kv_rows.shape[1]
+    q_pos = np.tile(np.arange(n_list - nq, n_list, dtype=np.int32), (w.S, 1))
+    return Workload("prefill_row_lists", w.S, nq, w.H, w.Hk, w.D, F16, F16, q, w.k, w.v, kv_rows=w.kv_rows,
+                    q_pos=q_pos, n_keys=n_list, extra=w.extra)
+
+
 def block_sparse_decode(n_kv: int = 262144, S: int = 4, H: int = 32, Hk: int = 4,
                         D: int = 128, block_rows: int = 64, n_sel: int = 512,
                         cache_pages: int = 2048, seed_workload: int = 5) -> Workload:

@@ -40,3 +40,23 @@ def vmax_of(oracle_mod, type_, raw_rows, D):
         return float(np.abs(raw.view(np.float16).astype(np.float64)).max())
     n_vals = raw.size // (34 if type_ == oracle_mod.Q8_0 else 18) * 32
     return float(np.abs(oracle_mod.dequant(type_, raw, n_vals)).max())
+
+
+def head_columns(rows, kh, seg):
+    """The bytes of KV head kh (segment size seg) of cell-major rows, as rows
+    of their own (a one-head cache the oracle can read with Hk = 1)."""
+    return np.ascontiguousarray(np.asarray(rows).reshape(rows.shape[0], -1)[:, kh * seg:(kh + 1) * seg])
+
+
+def oracle_one_head(oracle_mod, w, kh, *, k_type, v_type, k0, v0, k1=None, v1=None, **kw):
+    """Oracle rows of the G query heads of KV head kh (all tokens, all
+    sequences): the cache regions are cut down to that head's columns."""
+    G = w.H // w.Hk
+    sk, sv = oracle_mod.segment_bytes(k_type, w.D), oracle_mod.segment_bytes(v_type, w.D)
+    qh = np.ascontiguousarray(w.q[:, :, kh * G:(kh + 1) * G])
+    regions = dict(k0=head_columns(k0, kh, sk), v0=head_columns(v0, kh, sv), n_rows0=k0.shape[0],
+                   k_row_bytes0=sk, v_row_bytes0=sv)
+    if k1 is not None:
+        regions.update(k1=head_columns(k1, kh, sk), v1=head_columns(v1, kh, sv), n_rows1=k1.shape[0],
+                       k_row_bytes1=sk, v_row_bytes1=sv)
+    return oracle_mod.attention(qh, D=w.D, H=G, Hk=1, scale=w.scale, k_type=k_type, v_type=v_type, **regions, **kw)

@@ -60,6 +60,62 @@ def test_kv_append_bit_exact(skv, h, D, type_, pad):
     assert np.array_equal(d1.numpy(), r1), "tail bytes differ from the oracle"
 
 
+def _tie_blocks(rng, x, qmax):
+    """Overwrite blocks of x (float32 [..., D], 32-value blocks) with the cases
+    where a product with a reciprocal and the fp32 quotient could decide
+    differently: values on and within 3 ulps of half-integer multiples of the
+    block's scale (exact ties included), block maxima whose amax/qmax falls
+    exactly between two fp16 values, and blocks with fp16-subnormal scales."""
+    blocks = x.reshape(-1, 32)
+    nb = blocks.shape[0]
+    kind = rng.integers(0, 4, nb)              # 0: untouched, 1: ties, 2: fp16-midpoint scale, 3: subnormal scale
+    d = rng.uniform(1e-3, 0.05, nb).astype(np.float16).astype(np.float32)
+    k = rng.integers(-qmax, qmax, (nb, 32)).astype(np.float32)
+    t = (k + 0.5) * d[:, None]                 # exact in fp32 (9-bit x 11-bit products)
+    nudge = rng.integers(-3, 4, (nb, 32)).astype(np.int32)
+    nudge[:, ::4] = 0                          # a quarter stay exact ties
+    t = (t.view(np.int32) + nudge).view(np.float32)
+    t[:, 0] = qmax * d                         # the block maximum: amax / qmax = d exactly
+    ties = kind == 1
+    blocks[ties] = t[ties]
+    # amax / qmax exactly halfway between two fp16 values
+    mid = kind == 2
+    h = d.astype(np.float16)
+    up = np.nextafter(h, np.float16(np.inf)).astype(np.float32)
+    m = (d + up) / 2                           # exact: 12 significant bits
+    blocks[mid] = np.clip(blocks[mid], -0.99 * qmax * m[mid, None], 0.99 * qmax * m[mid, None])
+    blocks[mid, 5] = -qmax * m[mid]            # exact: 12-bit x 7-bit product
+    sub = kind == 3
+    blocks[sub] *= np.float32(2e-5)
+    return x
+
+
+@pytest.mark.parametrize("type_", [wl.Q8_0, wl.Q4_0])
+def test_kv_append_quant_near_ties_bit_exact(skv, h, type_):
+    """Quantise-on-append decides each code without dividing unless the value
+    is near a rounding boundary; on blocks built to sit on those boundaries,
+    and on 32768 ordinary rows, every stored byte equals the oracle's fp32
+    division rule."""
+    import torch
+    rng = wl.generator(6, salt=4242 + type_)
+    qmax = 127 if type_ == wl.Q8_0 else 7
+    Hk, D = 8, 128
+    row_bytes = Hk * wl.segment_bytes(type_, D)
+    for n, ties in ((4096, True), (32768, False)):
+        x, _ = wl.new_kv_values(rng, n, Hk, D)
+        if ties:
+            x = _tie_blocks(rng, x, qmax)
+        pos = np.arange(n, dtype=np.int32)
+        r0 = np.zeros(n * row_bytes, np.uint8)
+        d0 = dev(r0)
+        skv.kv_append(h, dev(x), dev(pos), d0, None, type_=type_, n_rows0=n, n_rows1=0, row_bytes=row_bytes)
+        torch.cuda.synchronize()
+        assert h.status() == 0
+        assert oracle.kv_append(type_, x, pos, r0, n, np.zeros(1, np.uint8), 0, row_bytes) == 0
+        got = d0.cpu().numpy()
+        assert np.array_equal(got, r0), f"{int((got != r0).sum())} bytes differ from the oracle (ties={ties})"
+
+
 def test_kv_append_out_of_range_sets_status(skv, h):
     import torch
     Hk, D, n0, n1 = 2, 64, 8, 8

@@ -30,8 +30,9 @@ def h(skv):
     return skv.Handle(0)
 
 
-def _resident(skv, h, w, q_d, sel, k_full, v_full):
-    """Paged attention with every page resident: page id = block * Hk + head."""
+def _resident(skv, h, c, w, q_d, sel, k_full, v_full):
+    """The same paged attention with every page resident on the device
+    (identity page table: page id = block * Hk + head)."""
     ids = (sel * w.Hk + np.arange(w.Hk, dtype=np.int32)[None, :, None]).astype(np.int32)
     return skv.attn_paged(h, q_d, k_full, v_full, dev(ids), Hk=w.Hk, page_rows=w.extra["block_rows"])
 
@@ -62,7 +63,7 @@ def test_block_cache_cold_warm_drift(skv, h, oracle_mod, n_slots):
     o0, l0 = c.attn(q_d, dev(sel))                            # cold
     want_o, want_l = _oracle(oracle_mod, w, sel)
     check_attention(o0, l0, want_o, want_l, vmax, "cold")
-    r_o, r_l = _resident(skv, h, w, q_d, sel, k_full, v_full)
+    r_o, r_l = _resident(skv, h, c, w, q_d, sel, k_full, v_full)
     assert torch.equal(o0, r_o) and torch.equal(l0, r_l), "cold call differs from the all-resident run"
     assert c.check() == 0
     st = c.stats()
@@ -70,7 +71,9 @@ def test_block_cache_cold_warm_drift(skv, h, oracle_mod, n_slots):
     assert st["misses"] == distinct and st["overflow"] == max(0, distinct - n_slots)
 
     o1, l1 = c.attn(q_d, dev(sel))                            # warm, same selection
-    assert torch.equal(o1, o0) and torch.equal(l1, l0)
+    r_o, r_l = _resident(skv, h, c, w, q_d, sel, k_full, v_full)
+    assert torch.equal(o1, r_o) and torch.equal(l1, r_l), "warm call differs from the all-resident run"
+    check_attention(o1, l1, want_o, want_l, vmax, "warm")
     assert c.check() == 0
     st1 = c.stats()
     new_hits = st1["hits"] - st["hits"]
@@ -86,14 +89,14 @@ def test_block_cache_cold_warm_drift(skv, h, oracle_mod, n_slots):
     for step in range(3):                                     # drift: 10% of the blocks redrawn per step
         cur = wl.redraw_selection(cur, n_blocks, 0.1, rng)
         o2, l2 = c.attn(q_d, dev(cur))
-        r_o, r_l = _resident(skv, h, w, q_d, cur, k_full, v_full)
+        r_o, r_l = _resident(skv, h, c, w, q_d, cur, k_full, v_full)
         assert torch.equal(o2, r_o) and torch.equal(l2, r_l), f"drift step {step}"
         assert c.check() == 0
     want_o, want_l = _oracle(oracle_mod, w, cur)
     check_attention(o2, l2, want_o, want_l, vmax, "drift")
 
     c.reset()
-    o3, l3 = c.attn(q_d, dev(sel))                            # after a reset: cold again
+    o3, l3 = c.attn(q_d, dev(sel))                            # after a reset: cold again, the same decisions
     assert torch.equal(o3, o0) and torch.equal(l3, l0)
     st3 = c.stats()
     assert st3["calls"] == 1 and st3["hits"] == 0

@@ -3,16 +3,18 @@ bench.py times.
 
 * Unified-cache decode (262144-row shared cache, 8 sequences x 32768 rows,
   32 q heads, 8 KV heads, D = 128): every output row against the oracle.
+* Block-sparse decode through the block cache, cold and warm, against the
+  oracle and bit for bit against an all-resident run split the same way.
 * Long-context window + host tail (1,048,576 rows, q8_0 K / q4_0 V, window
-  131072, 28 tail tiles of 32768 rows): the full call on the GPU; the oracle
-  recomputes the rows of sampled KV heads (first and last), which it can do
-  one head group at a time.
+  131072, 28 tail tiles of 32768 rows chosen by the library's planner): the
+  full call on the GPU; the oracle recomputes every KV head's rows, one head
+  group at a time.
 """
 import numpy as np
 import pytest
 
 from split_kv_flash_attn_gb300 import workloads as wl
-from tests.gpu_util import check_attention, dev, pinned, vmax_of
+from tests.gpu_util import check_attention, dev, head_columns, oracle_one_head, pinned, vmax_of
 
 pytestmark = pytest.mark.gpu
 
@@ -41,8 +43,8 @@ def test_unified_cache_full_size(skv, oracle_mod):
 def test_block_sparse_full_size(skv, oracle_mod):
     """4 sequences x 4 KV heads x 512 of 4096 64-row blocks from a pinned
     paged cache of 262144 rows through a 2048-page block cache (demand above
-    capacity): every output row against the oracle, and bit for bit against
-    the same paged attention with the whole cache resident."""
+    capacity): every output row against the oracle, cold and warm, and bit
+    for bit against the same paged attention with the whole cache resident."""
     import torch
     w = wl.block_sparse_decode()
     sel = w.extra["sel"]
@@ -57,39 +59,39 @@ def test_block_sparse_full_size(skv, oracle_mod):
                                           n_rows0=w.extra["n_kv"], layout=oracle_mod.PAGED, page_rows=br,
                                           n_keys=rows.shape[-1], kv_rows=rows, rows_per_head=True)
     check_attention(o, l, want_o, want_l, float(np.abs(w.v.view(np.float16)).max()), "block sparse full")
-    ids = (sel * w.Hk + np.arange(w.Hk, dtype=np.int32)[None, :, None]).astype(np.int32)
-    r_o, r_l = skv.attn_paged(h, q, dev(w.k), dev(w.v), dev(ids), Hk=w.Hk, page_rows=br)
+    from tests.test_gpu_bcache import _resident
+    r_o, r_l = _resident(skv, h, c, w, q, sel, dev(w.k), dev(w.v))
     assert torch.equal(o, r_o) and torch.equal(l, r_l)
-    o2, l2 = c.attn(q, dev(sel))                       # warm call: same bits
-    assert torch.equal(o2, o) and torch.equal(l2, l)
+    o2, l2 = c.attn(q, dev(sel))                       # warm call: hits and misses mixed
+    r_o, r_l = _resident(skv, h, c, w, q, sel, dev(w.k), dev(w.v))
+    assert torch.equal(o2, r_o) and torch.equal(l2, r_l)
+    check_attention(o2, l2, want_o, want_l, float(np.abs(w.v.view(np.float16)).max()), "block sparse warm")
+    st = c.stats()
+    assert st["last_misses"] > 0 and st["last_overflow"] > 0 and st["hits"] > 0
     assert c.check() == 0
     c.close()
     h.close()
 
 
-def _head_slice(rows, kh, seg):
-    return np.ascontiguousarray(rows[:, kh * seg:(kh + 1) * seg])
-
-
-def test_long_context_full_size_sampled_heads(skv, oracle_mod):
+def test_long_context_full_size_all_heads(skv, oracle_mod):
+    """The whole window + tail call, tail tiles sized by the library's own
+    planner (tile_rows = 0 -> skv_plan_tail_tile: 28 tiles of 32768 rows),
+    against the oracle on every KV head."""
     w = wl.long_context_decode()
+    assert skv.plan_tail_tile(w.k_tail.shape[0], w.k_tail.shape[1] + w.v_tail.shape[1]) == (32768, 28)
     h = skv.Handle(0)
     o, l = skv.attn_window_tail(h, dev(w.q), dev(w.k), dev(w.v), pinned(w.k_tail), pinned(w.v_tail), Hk=w.Hk,
-                                tile_rows=w.tile_rows, k_type=w.k_type, v_type=w.v_type)
+                                k_type=w.k_type, v_type=w.v_type)
     o = o.cpu()
     l = l.cpu()
     G = w.H // w.Hk
-    sk, sv = wl.segment_bytes(w.k_type, w.D), wl.segment_bytes(w.v_type, w.D)
-    for kh in (0, w.Hk - 1):
-        kwin, vwin = _head_slice(w.k, kh, sk), _head_slice(w.v, kh, sv)
-        ktail, vtail = _head_slice(w.k_tail, kh, sk), _head_slice(w.v_tail, kh, sv)
-        qh = np.ascontiguousarray(w.q[:, :, kh * G:(kh + 1) * G])
-        want_o, want_l = oracle_mod.attention(qh, D=w.D, H=G, Hk=1, scale=w.scale, k_type=w.k_type,
-                                              v_type=w.v_type, k0=kwin, v0=vwin, n_rows0=kwin.shape[0],
-                                              k_row_bytes0=sk, v_row_bytes0=sv, k1=ktail, v1=vtail,
-                                              n_rows1=ktail.shape[0], k_row_bytes1=sk, v_row_bytes1=sv,
-                                              n_keys=w.n_keys)
-        vmax = max(vmax_of(oracle_mod, w.v_type, vwin, w.D), vmax_of(oracle_mod, w.v_type, vtail, w.D))
+    sv = wl.segment_bytes(w.v_type, w.D)
+    for kh in range(w.Hk):
+        want_o, want_l = oracle_one_head(oracle_mod, w, kh, k_type=w.k_type, v_type=w.v_type, k0=w.k, v0=w.v,
+                                         k1=w.k_tail, v1=w.v_tail, n_keys=w.n_keys)
+        vmax = max(vmax_of(oracle_mod, w.v_type, head_columns(w.v, kh, sv), w.D),
+                   vmax_of(oracle_mod, w.v_type, head_columns(w.v_tail, kh, sv), w.D))
         check_attention(o[:, :, kh * G:(kh + 1) * G], l[:, :, kh * G:(kh + 1) * G], want_o, want_l, vmax,
                         f"long context head {kh}")
+    assert h.status() == 0
     h.close()

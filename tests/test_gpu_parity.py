@@ -159,19 +159,28 @@ def test_attn_rows_padding(skv, h, oracle_mod, per_head):
     check_attention(o, l, want_o, want_l, vmax_of(oracle_mod, wl.F16, V, D), "rows")
 
 
-def test_identity_rows_bitwise_equal_dense(skv, h):
-    D, H, Hk, n = 128, 32, 8, 4096
-    rng = wl.generator(2, salt=3)
-    q = wl.normal_f16(rng, (2, 1, H, D))
+@pytest.mark.parametrize("S,H,Hk,n,b,e,per_head", [
+    (2, 32, 8, 4096, 0, 4096, False),     # whole range, several splits
+    (3, 40, 8, 3000, 0, 3000, True),      # G = 5, ragged last tile, per-head lists
+    (1, 8, 2, 20000, 333, 19001, False),  # a sub-range starting mid-tile, many splits
+])
+def test_identity_rows_bitwise_equal_dense(skv, h, S, H, Hk, n, b, e, per_head):
+    """An identity row list takes the same split plan and the same kernel as
+    the dense range (both plan from the key count and the units alone), so
+    the results must agree bit for bit: the gather changes only where the
+    rows come from."""
+    import torch
+    D = 128
+    rng = wl.generator(2, salt=3 + n)
+    q = wl.normal_f16(rng, (S, 1, H, D))
     K = dev(wl.cache_rows(rng, wl.F16, n, Hk, D))
     V = dev(wl.cache_rows(rng, wl.F16, n, Hk, D))
-    rows = dev(np.tile(np.arange(n, dtype=np.int32), (2, 1)))
+    ident = np.arange(n, dtype=np.int32)
+    rows = dev(np.tile(ident, (S, Hk, 1)) if per_head else np.tile(ident, (S, 1)))
     qd = dev(q)
-    o1, l1 = skv.attn_partial(h, qd, K, V, Hk=Hk, kv_rows=rows, kv_end=n)
-    o2, l2 = skv.attn_partial(h, qd, K, V, Hk=Hk, kv_end=n)
-    # the dense and list launches may split differently; same split -> same bits
-    import torch
-    assert torch.allclose(o1, o2, atol=1e-5) and torch.allclose(l1, l2, atol=1e-5)
+    o1, l1 = skv.attn_partial(h, qd, K, V, Hk=Hk, kv_rows=rows, kv_rows_per_head=per_head, kv_begin=b, kv_end=e)
+    o2, l2 = skv.attn_partial(h, qd, K, V, Hk=Hk, kv_begin=b, kv_end=e)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
 def test_unified_cache_reduced(skv, h, oracle_mod):

@@ -1,8 +1,11 @@
 """Residency planning (host logic, no GPU): the resident window and the tail
-tiles, against the rules restated in oracle/planner.py (bit-exact on random
-inputs) and against numbers the Rolling KV page states: 32768-key tiles (the
-coarsening from 2048 keys, which gave 128 tiles at 256k keys), four slots of
-a tile within 512 MiB, windows aligned to the 256-key stride, and the
+tiles.  The library's planner is written as closed forms of the constraints;
+oracle/planner.py restates the Rolling KV page's rules step by step in the
+page's order.  The two codings must agree on random inputs (bit-exact), both
+must meet the constraints (alignment, budget, a step of tail, coverage, the
+slot cap), and both must give the numbers the page states: 32768-key tiles
+(the coarsening from 2048 keys, which gave 128 tiles at 256k keys), four slots
+of a tile within 512 MiB, windows aligned to the 256-key stride, and the
 long-context workload's 32768-row tiles of raw q8_0/q4_0 bytes."""
 import numpy as np
 import pytest
@@ -36,6 +39,31 @@ def test_window_rounds_down_and_clamps(skv):
     assert skv.plan_window(MIB, 1 << 20, 80 << 30, target_bytes=2048 * MIB) == 512
     # padding above 256 sets the alignment
     assert skv.plan_window(MIB, 1 << 20, 10 << 30, n_pad=1024) == 8192
+
+
+def test_window_non_power_of_two_padding(skv):
+    # the alignment must be a multiple of both the padding and the 256-key
+    # stride: lcm(384, 256) = 768, where the page's larger-of-the-two rule
+    # (written for power-of-two paddings) would give 384
+    got = skv.plan_window(MIB, 1 << 20, 10 << 30, n_pad=384)
+    assert got % 768 == 0 and got == 8448
+    rng = np.random.default_rng(2)
+    for _ in range(2000):
+        per_cell = int(rng.integers(1, 1 << 22))
+        kv = int(rng.integers(1, 1 << 21))
+        free = int(rng.integers(0, 1 << 40))
+        n_pad = int(rng.integers(1, 2000))
+        step = np.lcm(n_pad, 256)
+        got = skv.plan_window(per_cell, kv, free, 0, 1536 * MIB, n_pad)
+        budget = max(0, free - 1536 * MIB)
+        if per_cell * kv <= budget:
+            assert got == kv
+            continue
+        assert got % step == 0 and got >= step
+        if got > step:
+            assert got * per_cell <= budget          # above one step only while it fits
+        if kv > step:
+            assert got <= max(step, kv - step)       # a step of tail stays (or one step)
 
 
 def test_window_matches_restated_rules(skv):
@@ -79,3 +107,9 @@ def test_tail_tiles_match_restated_rules(skv):
         assert (rows, tiles) == ref.tail_tile(n, per_key, slots, cap, target, align)
         if n:
             assert rows % align == 0 and tiles * rows >= n and (tiles - 1) * rows < n
+            # no more tiles than the target count or the slot cap asks for
+            # (whole blocks, spread evenly), nor fewer than the target asks for
+            n_blk = -(-n // align)
+            cap_keys = max(align, cap // (per_key * slots)) if per_key else n
+            want = min(n_blk, max(1, -(-n // target), -(-n // cap_keys)))
+            assert tiles <= want and -(-n_blk // tiles) == -(-n_blk // want)
