@@ -53,7 +53,7 @@ def parse():
 
 
 PROFILE_CASES = ("decode_unified", "decode_q8q4_window", "prefill_window", "prefill_q8q4_window",
-                 "prefill_row_list", "append_q8_0")
+                 "prefill_row_list", "append_q8_0", "block_sparse_warm")
 
 
 def run_profile_case(name: str) -> int:
@@ -61,8 +61,9 @@ def run_profile_case(name: str) -> int:
     with the inputs the bench times: the unified-cache decode, the q8_0/q4_0
     long-context window (131072 rows), the prefill chunk's window (512 tokens
     over 32768 fp16 keys), the same prefill over q8_0-K / q4_0-V rows, the
-    8-sequence row-list prefill over the unified cache, and a 32768-row
-    q8_0 append."""
+    8-sequence row-list prefill over the unified cache, a 32768-row q8_0
+    append, and a warm block-sparse call through the block cache (three
+    warm-up calls first, so the profiled calls see the steady state)."""
     import torch
     import split_kv_flash_attn_gb300 as skv
     from split_kv_flash_attn_gb300 import build as skv_build
@@ -91,6 +92,16 @@ def run_profile_case(name: str) -> int:
         w = wl.prefill_row_lists()
         q, k, v, rows, qp = cu(w.q), cu(w.k), cu(w.v), cu(w.kv_rows), cu(w.q_pos)
         call = lambda: skv.attn_partial(h, q, k, v, Hk=w.Hk, kv_rows=rows, q_pos=qp)   # noqa: E731
+    elif name == "block_sparse_warm":
+        w = wl.block_sparse_decode()
+        sel = w.extra["sel"]
+        hk, hv = torch.from_numpy(w.k).pin_memory(), torch.from_numpy(w.v).pin_memory()
+        c = skv.BlockCache(h, hk, hv, n_blocks=w.extra["n_blocks"], block_rows=64, Hk=w.Hk, D=w.D,
+                           n_slots=w.extra["cache_pages"], max_lookups=sel.size)
+        q, sel_d = cu(w.q), cu(sel)
+        for _ in range(3):
+            c.attn(q, sel_d)
+        call = lambda: c.attn(q, sel_d)   # noqa: E731
     else:
         rng = wl.generator(6, salt=7)
         Hk, D, n = 8, 128, 32768

@@ -83,12 +83,27 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(const float *
         (static_cast<int64_t>(blockIdx.x) * (kAppendThreads / 32) + (threadIdx.x >> 5)) * kItemsPerWarp;
     float v[kItemsPerWarp][VPL];
     int64_t p[kItemsPerWarp];
+    int hd[kItemsPerWarp];                                        // KV head of each item
+    // (row, head) of the warp's first item with one division; the next items
+    // step through the heads.
+    const int64_t row_first = first / Hk;
+    {
+        int hh = static_cast<int>(first - row_first * Hk);
+#pragma unroll
+        for (int it = 0; it < kItemsPerWarp; ++it) {
+            hd[it] = hh;
+            hh = hh + 1 == Hk ? 0 : hh + 1;
+        }
+    }
 #pragma unroll
     for (int it = 0; it < kItemsPerWarp; ++it) {
         const int64_t item = first + it;
         p[it] = -1;
         if (item >= total) continue;
-        p[it] = pos[item / Hk];
+        int64_t row = row_first;
+#pragma unroll
+        for (int u = 1; u <= it; ++u) row += hd[u] == 0 ? 1 : 0;   // a head wrap starts the next row
+        p[it] = pos[row];
         const float *src = x + item * DD;                         // values lane*VPL .. lane*VPL + VPL - 1
         if (VPL == 4) {
             const float4 a = reinterpret_cast<const float4 *>(src)[lane];
@@ -102,7 +117,7 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(const float *
     for (int it = 0; it < kItemsPerWarp; ++it) {
         const int64_t item = first + it;
         if (p[it] < 0) continue;                                  // beyond the items, or not written
-        const int h = static_cast<int>(item % Hk);
+        const int h = hd[it];
         if (p[it] >= n_rows0 + n_rows1) {
             if (lane == 0 && h == 0) atomicOr(status, 2);
             continue;

@@ -9,14 +9,16 @@
 
 namespace skv {
 
-// One CTA of 256 threads per output row.  The parts' weights are computed
-// in parallel into shared memory (after the maximum); then warp w takes parts
-// w, w + 8, ... and lane l elements 4l .. 4l+3 (16-byte loads), so each warp
-// keeps several parts' loads in flight; the eight warps' sums are added in
-// shared memory.
-constexpr int kCombineThreads = 256;
+// One CTA per output row.  The parts' weights are computed in parallel into
+// shared memory (after the maximum); then warp w takes parts w, w + W, ...
+// (W warps) and lane l elements 4l .. 4l+3 (16-byte loads), so each warp keeps
+// several parts' loads in flight; the warps' sums are added in shared memory.
+// Few rows with many parts (a long range split across the whole GPU for a
+// handful of query rows) take 1024 threads a row, so that each warp walks
+// fewer parts; otherwise 256.
 constexpr int kCombineMaxParts = 4096;
 
+template <int kCombineThreads>
 __global__ void __launch_bounds__(kCombineThreads) splitkv_combine_kernel(int n_parts,
                                                                           const float *__restrict__ o_parts,
                                                                           const float *__restrict__ lse_parts,
@@ -26,6 +28,7 @@ __global__ void __launch_bounds__(kCombineThreads) splitkv_combine_kernel(int n_
     __shared__ float w_s[kCombineMaxParts];
     __shared__ float red[kCombineThreads / 32];
     __shared__ float4 acc_s[kCombineThreads / 32][32];
+    static_assert(kCombineThreads % 32 == 0 && kCombineThreads <= 1024, "threads per row");
     const int64_t row = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float M = -INFINITY;
@@ -117,8 +120,12 @@ int launch_combine(int n_parts, const float *o_parts, const float *lse_parts, in
 {
     if (rows <= 0) return SKV_OK;
     if (rows > 0x7fffffff || n_parts > kCombineMaxParts || D > 128 || D % 4) return SKV_EUNSUPPORTED;
-    splitkv_combine_kernel<<<static_cast<unsigned>(rows), kCombineThreads, 0, st>>>(n_parts, o_parts, lse_parts, rows,
-                                                                                   D, o, lse);
+    if (n_parts >= 64 && rows <= 512)
+        splitkv_combine_kernel<1024><<<static_cast<unsigned>(rows), 1024, 0, st>>>(n_parts, o_parts, lse_parts, rows, D,
+                                                                                    o, lse);
+    else
+        splitkv_combine_kernel<256><<<static_cast<unsigned>(rows), 256, 0, st>>>(n_parts, o_parts, lse_parts, rows, D,
+                                                                                  o, lse);
     return cudaGetLastError() == cudaSuccess ? SKV_OK : SKV_ECUDA;
 }
 

@@ -186,16 +186,19 @@ def test_prefill_per_head_lists(skv, h, oracle_mod):
 
 
 def test_identity_list_matches_tma_bitwise(skv, h):
+    """One 128-row query tile per (sequence, KV head): the dense range and the
+    identity row list both run the single-tile kernel (TMA producers against
+    software producers) with the same split plan."""
     import torch
     rng = wl.generator(4, salt=500)
-    S, nq, H, Hk, n = 1, 128, 32, 8, 3000
+    S, nq, H, Hk, n = 2, 32, 32, 8, 3000
     q = wl.normal_f16(rng, (S, nq, H, D))
     K = wl.cache_rows(rng, wl.F16, n, Hk, D)
     V = wl.cache_rows(rng, wl.F16, n, Hk, D)
     qd, Kd, Vd = dev(q), dev(K), dev(V)
-    q_pos = dev((n - nq + np.arange(nq, dtype=np.int32)).reshape(1, nq))
+    q_pos = dev(np.tile(n - nq + np.arange(nq, dtype=np.int32), (S, 1)))
     o_tma, l_tma = skv.attn_partial(h, qd, Kd, Vd, Hk=Hk, q_pos=q_pos)
-    rows = dev(np.arange(n, dtype=np.int32).reshape(1, n))
+    rows = dev(np.tile(np.arange(n, dtype=np.int32), (S, 1)))
     o_sw, l_sw = skv.attn_partial(h, qd, Kd, Vd, Hk=Hk, kv_rows=rows, q_pos=q_pos)
     assert torch.equal(o_tma, o_sw) and torch.equal(l_tma, l_sw)
     assert h.status() == 0
