@@ -2,10 +2,9 @@
 
 * The prefill chunk: 512 causal tokens at positions 65024..65535 x 32 heads
   over 65536 fp16 keys (32768 in device memory + a 32768-row pinned tail in
-  8192-row tiles).  Every token of KV heads 0 and 7 (all 16 query tiles of
-  each) against the oracle; every token of every head against the split-KV
-  decode kernel (one query token per sequence, 512 sequences, the same keys
-  and causal positions), which covers all 128 query tiles.
+  8192-row tiles).  All 512 x 32 rows (every KV head, all 128 query tiles)
+  against the oracle, and against the split-KV decode kernel (one query token
+  per sequence, 512 sequences, the same keys and causal positions).
 * The same shape over q8_0-K / q4_0-V rows (32768 rows on the device): every
   token of KV heads 0 and 7 against the oracle.
 * Row-list prefill over the unified cache: 8 sequences x 64 tokens, each over
@@ -58,7 +57,7 @@ def test_prefill_chunk_full_size(skv, h, oracle_mod):
                                 tile_rows=w.tile_rows, q_pos=dev(w.q_pos))
     torch.cuda.synchronize()
     assert h.status() == 0
-    _check_heads(oracle_mod, w, o, l, HEADS, wl.F16, wl.F16, "prefill chunk", k0=w.k, v0=w.v, k1=w.k_tail,
+    _check_heads(oracle_mod, w, o, l, range(w.Hk), wl.F16, wl.F16, "prefill chunk", k0=w.k, v0=w.v, k1=w.k_tail,
                  v1=w.v_tail, n_keys=w.n_keys, q_pos=w.q_pos)
 
     # every token through the decode kernel: token t becomes sequence t with
