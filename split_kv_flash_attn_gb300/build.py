@@ -36,7 +36,7 @@ def _sources():
 
 def _deps():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu*")) + glob.glob(os.path.join(CSRC, "*.h")) +
-                  glob.glob(os.path.join(PKG, "..", "include", "*.h")))
+                  glob.glob(os.path.join(PKG, "..", "include", "*.h")) + [os.path.join(PKG, "exports.map")])
 
 
 def _stale(target, deps):
@@ -74,7 +74,11 @@ def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> 
     objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in _sources()]
     if force or jobs or _stale(LIB, objs):
         tmp = LIB + f".tmp{os.getpid()}"
-        res = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
+        # export the C ABI only (skv_*): internal symbols stay local, so two
+        # copies of the library in one process never share internal state
+        exports = os.path.join(PKG, "exports.map")
+        res = subprocess.run([cc, *ARCH, "-shared", "-Xlinker", f"--version-script={exports}", "-o", tmp, *objs],
+                             capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError("link failed:\n" + res.stderr)
         os.replace(tmp, LIB)

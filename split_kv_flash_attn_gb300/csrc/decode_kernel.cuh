@@ -643,12 +643,17 @@ __global__ void __launch_bounds__(128) splitkv_decode_kernel(const DecodeArgs a)
     if (tid == 0) a.counters[unit] = 0;              // ready for the next launch
 }
 
+namespace {
+// One cache per instance and translation unit (internal linkage: a static in
+// an external template would be merged across every copy of the library a
+// process loads).
 template <int D, int KT, int VT>
 KernelAttrCache &decode_attr_cache()
 {
     static KernelAttrCache c;
     return c;
 }
+}  // namespace
 
 template <int D, int KT, int VT>
 int launch_decode_t(skv_handle *h, const DecodeArgs &a, cudaStream_t st)

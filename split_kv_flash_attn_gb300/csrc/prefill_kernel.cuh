@@ -883,13 +883,23 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
     if (tid == 0) a.counters[unit] = 0;
 }
 
+namespace {
+// One cache per instance and translation unit (internal linkage, see
+// decode_attr_cache).
+template <int MODE, int KT, int VT>
+KernelAttrCache &prefill_attr_cache()
+{
+    static KernelAttrCache c;
+    return c;
+}
+}  // namespace
+
 // Launch one instance (its shared-memory opt-in is made once per device).
 template <int MODE, int KT, int VT>
 int launch_prefill_t(skv_handle *h, const CUtensorMap &mk, const CUtensorMap &mv, const PrefillArgs &a, dim3 grid,
                      cudaStream_t st)
 {
-    static KernelAttrCache attrs;
-    cudaError_t e = kernel_smem_optin(attrs, reinterpret_cast<const void *>(splitkv_prefill_kernel<MODE, KT, VT>),
+    cudaError_t e = kernel_smem_optin(prefill_attr_cache<MODE, KT, VT>(), reinterpret_cast<const void *>(splitkv_prefill_kernel<MODE, KT, VT>),
                                       smem_bytes<KT, VT>(), Cfg<MODE>::kThreads, nullptr);
     if (e != cudaSuccess) return cuda_fail(h, e, "cudaFuncSetAttribute(prefill)");
     if (h->prof_before) cudaEventRecord(h->prof_before, st);
