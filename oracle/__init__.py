@@ -15,6 +15,10 @@ Functions (all results float64 numpy arrays):
                                       indirection with -1 padding, causal
                                       positions, additive fp16 mask).
 * ``combine(o_parts, lse_parts)``     log-sum-exp merge of partial results.
+
+Also in the package, in plain Python: ``planner`` (the residency planner's
+rules in the Rolling KV page's order) and ``bcache_model`` (the block cache's
+CLOCK residency decisions as a sequential loop).
 """
 from __future__ import annotations
 

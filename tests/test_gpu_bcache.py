@@ -3,13 +3,16 @@
 Parity is against the oracle over the selected rows, and bitwise against the
 same paged attention with the whole cache resident on the device (identity
 page table), the check the Strata KV-streaming parity test makes.  After every
-resolve the page table and the slot map must be inverse maps with no claimed
-page left, and the counters must add up."""
+resolve the page table and the slot map must be inverse maps, and the counters
+must add up.  The residency decisions themselves (the slot of every page, the
+overflow, the hand) are compared call by call with a plain sequential CLOCK
+model of the page's resolve rules (oracle/bcache_model.py)."""
 import math
 
 import numpy as np
 import pytest
 
+from oracle.bcache_model import ClockCache
 from split_kv_flash_attn_gb300 import workloads as wl
 from tests.gpu_util import check_attention, dev, pinned
 
@@ -100,6 +103,42 @@ def test_block_cache_cold_warm_drift(skv, h, oracle_mod, n_slots):
     assert torch.equal(o3, o0) and torch.equal(l3, l0)
     st3 = c.stats()
     assert st3["calls"] == 1 and st3["hits"] == 0
+    c.close()
+
+
+@pytest.mark.parametrize("n_slots", [96, 700, 5000])
+def test_resolve_matches_clock_model(skv, h, n_slots):
+    """Every resolve's page ids and counters against the plain sequential
+    CLOCK model (oracle/bcache_model.py): cold, warm, three drift steps, a
+    selection of already-resident pages, a reset, cold again.  96 slots wrap
+    the sweep and overflow, 700 take cold slots only after the first calls,
+    5000 hold everything."""
+    import torch
+    w = wl.block_sparse_decode(n_kv=64 * 512, S=4, H=32, Hk=4, D=128, n_sel=64, cache_pages=n_slots)
+    n_blocks, Hk = w.extra["n_blocks"], w.Hk
+    c = skv.BlockCache(h, pinned(w.k), pinned(w.v), n_blocks=n_blocks, block_rows=64, Hk=Hk, D=w.D,
+                       n_slots=n_slots, max_lookups=w.S * Hk * 64)
+    model = ClockCache(n_blocks * Hk, n_slots)
+    rng = np.random.default_rng(31)
+    sels = [w.extra["sel"], w.extra["sel"]]
+    for _ in range(3):
+        sels.append(wl.redraw_selection(sels[-1], n_blocks, 0.1, rng))
+    sels.append(np.ascontiguousarray(sels[-1][:, :, :16]))
+    sels += ["reset", w.extra["sel"]]
+    for i, sel in enumerate(sels):
+        if isinstance(sel, str):
+            c.reset()
+            model.reset()
+            continue
+        ids = torch.empty(sel.shape, dtype=torch.int32, device="cuda")
+        c.resolve(dev(sel), ids)
+        pages = (sel.astype(np.int64) * Hk + np.arange(Hk)[None, :, None]).reshape(-1).tolist()
+        want = np.array(model.resolve(pages), dtype=np.int32).reshape(sel.shape)
+        assert np.array_equal(ids.cpu().numpy(), want), f"call {i}: page ids differ from the CLOCK model"
+        st = c.stats()
+        assert (st["calls"], st["lookups"], st["hits"], st["misses"], st["overflow"]) == \
+            (model.calls, model.lookups, model.hits, model.misses, model.overflow), f"call {i}: counters"
+        assert c.check() == 0
     c.close()
 
 
