@@ -375,8 +375,9 @@ int skv_bcache_attn(skv_bcache *c, const skv_shape *shape, const void *q, const 
 /* Cumulative counters (synchronises the device). */
 int skv_bcache_stats(skv_bcache *c, skv_bcache_counters *out);
 
-/* Count violations of the residency invariants (page table and slot map are
- * inverse maps; no page left claimed); synchronises the device. */
+/* Count violations of the residency invariants (every page-table entry is -1
+ * or a slot, and the page table and the slot map are inverse maps);
+ * synchronises the device. */
 int skv_bcache_check(skv_bcache *c, int32_t *violations);
 
 /* Ring layout ("Strata compare", KV streaming: a reader that only ever reads
