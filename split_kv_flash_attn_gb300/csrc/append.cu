@@ -20,12 +20,12 @@
 //
 // Both divisions are replaced by products with a reciprocal, with the exact
 // division kept for the few values where the two could decide differently:
-//  * the code: t0 = x * rcp(d), rcp correctly rounded, lies within 2^-23 |t0|
-//    of x/d, and the fp32 quotient fl(x/d) within 2^-17 of it for |x/d| < 256;
-//    so when t0 is more than 2^-14 away from every half-integer, rint(t0) =
-//    rint(fl(x/d)).  Nearer than that (about 1 value in 8000, and every exact
-//    tie), the code is taken from the IEEE division itself; |t0| >= 130 clamps
-//    either way.
+//  * the code: rd = rcp.approx(d) has a relative error of at most 2^-22, so
+//    t0 = x * rd lies within 2^-21.6 |t0| of x/d (5e-5 for |x/d| < 130), and
+//    the fp32 quotient fl(x/d) within 2^-17 of x/d; so when t0 is more than
+//    2^-13 (1.2e-4) away from every half-integer, rint(t0) = rint(fl(x/d)).
+//    Nearer than that (about 1 value in 4000, and every exact tie), the code
+//    is taken from the IEEE division itself; |t0| >= 130 clamps either way.
 //  * the scale: s0 = amax * fl(1/qmax) lies within 2^-22.4 (relative) of
 //    fl(amax/qmax); when s0 (1 - 2^-20) and s0 (1 + 2^-20) round to the same
 //    fp16 value, so does fl(amax/qmax) (rounding is monotone); otherwise the
@@ -53,13 +53,21 @@ __device__ __forceinline__ __half block_scale(float amax, float qmax, float inv_
     return __float2half_rn(__fdiv_rn(amax, qmax));
 }
 
-// rint(fl(x / d)) for d > 0, rd = rcp_rn(d) (see the header).
+// 1/d to within 2^-22 (relative), one instruction; d is a normal fp32 value.
+__device__ __forceinline__ float rcp_approx(float d)
+{
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(d));
+    return r;
+}
+
+// rint(fl(x / d)) for d > 0, rd = rcp_approx(d) (see the header).
 __device__ __forceinline__ int nearest_code(float x, float d, float rd)
 {
     const float t0 = __fmul_rn(x, rd);
     if (fabsf(t0) >= 130.f) return t0 > 0.f ? 1024 : -1024;       // clamped by every code range
     const float r0 = rintf(t0);
-    if (0.5f - fabsf(t0 - r0) > 0x1p-14f) return static_cast<int>(r0);
+    if (0.5f - fabsf(t0 - r0) > 0x1p-13f) return static_cast<int>(r0);
     return __float2int_rn(__fdiv_rn(x, d));
 }
 
@@ -150,7 +158,7 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(const float *
             for (int off = LPB / 2; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
             const __half d16 = block_scale(amax, QMAX, INV_QMAX);
             const float d = __half2float(d16);
-            const float rd = d > 0.f ? __frcp_rn(d) : 0.f;
+            const float rd = d > 0.f ? rcp_approx(d) : 0.f;
             uint32_t packed = 0;                                  // VPL code bytes / nibbles, value j0 + i in byte i
 #pragma unroll
             for (int i = 0; i < VPL; ++i) {
