@@ -76,8 +76,9 @@ namespace skv {
 // ctl words (uint64): 0 epoch of the last resolve, 1 hand, 2 calls, 3 lookups,
 // 4 hits, 5 misses, 6 overflow, 7 last misses, 8 last overflow, 9 pages a ring
 // restore fetches, 11 misses placed in slots by the last resolve, 12 misses of
-// the last resolve.
+// the last resolve, 13 pages the running fetch has handed out.
 constexpr int kCtlWords = 16;
+constexpr int kCtlNext = 13;
 constexpr int kVictimThreads = 512;
 
 struct ResolveState {
@@ -145,7 +146,9 @@ __global__ void __launch_bounds__(256) bcache_lookup_kernel(ResolveState r, cons
 //  2. Victims: thread t owns hand-relative positions [t*per, (t+1)*per);
 //     position i is slot (hand + i) % n_slots.
 //  3. Placement (below).
-constexpr int kClaimItems = 16;
+constexpr int kClaimItems = 16;   // lookups per thread and tile of step 1
+constexpr int kSlotItems = 16;    // slots per thread whose classes stay in registers in step 2
+constexpr int kPlaceBatch = 16;   // misses per thread and round of step 3
 __global__ void __launch_bounds__(kVictimThreads) bcache_victim_kernel(ResolveState r, const int32_t *__restrict__ sel,
                                                                        int64_t n_look, int n_sel, int Hk)
 {
@@ -153,27 +156,43 @@ __global__ void __launch_bounds__(kVictimThreads) bcache_victim_kernel(ResolveSt
     __shared__ typename Scan::TempStorage scan_tmp;
     __shared__ int s_stop;
     const int epoch = static_cast<int>(r.ctl[0]) + 1;
+    if (threadIdx.x == 0) r.ctl[kCtlNext] = 0;      // the fetch's page counter
     // 1. the miss list in lookup order
     int64_t need = 0;
     for (int64_t t0 = 0; t0 < n_look; t0 += static_cast<int64_t>(kVictimThreads) * kClaimItems) {
         const int64_t e0 = t0 + static_cast<int64_t>(threadIdx.x) * kClaimItems;
-        unsigned own = 0;                            // bit u: lookup e0 + u owns its page
+        // lookups are [S][Hk][n_sel]: the KV head of e0, stepped item by item
+        const int64_t row = e0 / n_sel;
+        int col = static_cast<int>(e0 - row * n_sel);
+        int kh = static_cast<int>(row % Hk);
+        int32_t pg[kClaimItems];
 #pragma unroll
         for (int u = 0; u < kClaimItems; ++u) {
             const int64_t e = e0 + u;
+            int32_t p = -1;
             if (e < n_look) {
-                const int64_t p = lookup_page(sel, e, n_sel, Hk, r.n_pages);
-                if (p >= 0 && r.page_claim[p] == claim_key(epoch, e)) own |= 1u << u;
+                const int64_t blk = sel[e];
+                const int64_t pp = blk * Hk + kh;
+                if (blk >= 0 && pp < r.n_pages) p = static_cast<int32_t>(pp);   // out-of-range ids: no page
+            }
+            pg[u] = p;
+            if (++col == n_sel) {
+                col = 0;
+                if (++kh == Hk) kh = 0;
             }
         }
+        unsigned own = 0;                            // bit u: lookup e0 + u owns its page
+#pragma unroll
+        for (int u = 0; u < kClaimItems; ++u)
+            if (pg[u] >= 0 && r.page_claim[pg[u]] == claim_key(epoch, e0 + u)) own |= 1u << u;
         unsigned long long before = 0, total = 0;
         Scan(scan_tmp).ExclusiveSum(static_cast<unsigned long long>(__popc(own)), before, total);
         int64_t m = need + static_cast<int64_t>(before);
+#pragma unroll
         for (int u = 0; u < kClaimItems; ++u) {
             if (own & (1u << u)) {
-                const int32_t p = static_cast<int32_t>(lookup_page(sel, e0 + u, n_sel, Hk, r.n_pages));
-                r.miss_page[m] = p;
-                r.page_miss[p] = static_cast<int32_t>(m);
+                r.miss_page[m] = pg[u];
+                r.page_miss[pg[u]] = static_cast<int32_t>(m);
                 ++m;
             }
         }
@@ -185,15 +204,38 @@ __global__ void __launch_bounds__(kVictimThreads) bcache_victim_kernel(ResolveSt
     const int hand = static_cast<int>(r.ctl[1] % static_cast<uint64_t>(n));
     const int per = (n + kVictimThreads - 1) / kVictimThreads;
     const int i0 = min(n, static_cast<int>(threadIdx.x) * per), i1 = min(n, i0 + per);
-    auto slot_at = [&](int i) { return static_cast<int>((static_cast<int64_t>(hand) + i) % n); };
+    const int cnt = i1 - i0;
+    // slot of hand-relative position i0 + k (k < per <= n)
+    auto slot_k = [&](int k) {
+        int j = hand + i0 + k;
+        j -= j >= n ? n : 0;
+        j -= j >= n ? n : 0;
+        return j;
+    };
     // 0: in use by this call, 1: cold (free or unreferenced), 2: warm (referenced)
-    auto class_of = [&](int j) {
-        if (r.slot_epoch[j] == epoch) return 0;
-        return (r.slot_page[j] < 0 || r.slot_ref[j] == 0) ? 1 : 2;
+    auto class_of = [&](int32_t ep, int32_t pgid, int32_t ref) { return ep == epoch ? 0 : (pgid < 0 || ref == 0) ? 1 : 2; };
+    uint32_t cls = 0;                                // classes of positions k < kSlotItems, 2 bits each
+    {
+        int32_t ep[kSlotItems], sp[kSlotItems], rf[kSlotItems];
+#pragma unroll
+        for (int k = 0; k < kSlotItems; ++k) {       // every load in flight at once
+            const int j = slot_k(k);
+            const bool in = k < cnt;
+            ep[k] = in ? r.slot_epoch[j] : 0;
+            sp[k] = in ? r.slot_page[j] : 0;
+            rf[k] = in ? r.slot_ref[j] : 0;
+        }
+#pragma unroll
+        for (int k = 0; k < kSlotItems; ++k) cls |= static_cast<uint32_t>(class_of(ep[k], sp[k], rf[k])) << (2 * k);
+    }
+    auto class_at = [&](int k) {
+        if (k < kSlotItems) return static_cast<int>((cls >> (2 * k)) & 3u);
+        const int j = slot_k(k);
+        return class_of(r.slot_epoch[j], r.slot_page[j], r.slot_ref[j]);
     };
     unsigned long long mine = 0;                 // cold count | warm count << 32
-    for (int i = i0; i < i1; ++i) {
-        const int c = class_of(slot_at(i));
+    for (int k = 0; k < cnt; ++k) {
+        const int c = class_at(k);
         mine += c == 1 ? 1ull : (c == 2 ? (1ull << 32) : 0ull);
     }
     unsigned long long before = 0, total = 0;
@@ -207,13 +249,13 @@ __global__ void __launch_bounds__(kVictimThreads) bcache_victim_kernel(ResolveSt
     if (threadIdx.x == 0) s_stop = -1;
     __syncthreads();
     int64_t rc = static_cast<int64_t>(before & 0xffffffffull), rw = static_cast<int64_t>(before >> 32);
-    for (int i = i0; i < i1; ++i) {
-        const int j = slot_at(i);
-        const int c = class_of(j);
+    for (int k = 0; k < cnt; ++k) {
+        const int c = class_at(k);
+        const int j = slot_k(k);
         if (c == 1) {
             if (rc < need) {
                 r.victim[rc] = j;
-                if (rc == (wraps ? (warm_taken == 0 ? n_cold - 1 : -1) : need - 1)) s_stop = i;
+                if (rc == (wraps ? (warm_taken == 0 ? n_cold - 1 : -1) : need - 1)) s_stop = i0 + k;
             }
             ++rc;
         } else if (c == 2) {
@@ -221,7 +263,7 @@ __global__ void __launch_bounds__(kVictimThreads) bcache_victim_kernel(ResolveSt
                 r.slot_ref[j] = 0;
                 if (rw < warm_taken) {
                     r.victim[n_cold + rw] = j;
-                    if (rw == warm_taken - 1) s_stop = i;
+                    if (rw == warm_taken - 1) s_stop = i0 + k;
                 }
             }
             ++rw;
@@ -231,17 +273,14 @@ __global__ void __launch_bounds__(kVictimThreads) bcache_victim_kernel(ResolveSt
     const int stop = s_stop;
     if (!wraps && stop >= 0) {
         // one partial round: the warm slots before the stop lose their reference bit
-        for (int i = i0; i < min(i1, stop); ++i) {
-            const int j = slot_at(i);
-            if (class_of(j) == 2) r.slot_ref[j] = 0;
-        }
+        for (int k = 0; k < min(cnt, stop - i0); ++k)
+            if (class_at(k) == 2) r.slot_ref[slot_k(k)] = 0;
     }
     __syncthreads();                                 // victim[] complete
     // 3. placement: miss m < placed takes victim[m]; the rest go to the
     //    overflow area (pool page n_slots + m - placed), for this call only.
     //    Each thread places kPlaceBatch misses at a time, all their loads
     //    issued before any store.
-    constexpr int kPlaceBatch = 8;
     for (int64_t m0 = threadIdx.x; m0 < need; m0 += static_cast<int64_t>(kVictimThreads) * kPlaceBatch) {
         int pg[kPlaceBatch], vj[kPlaceBatch], old[kPlaceBatch];
 #pragma unroll
@@ -286,8 +325,11 @@ __global__ void __launch_bounds__(kVictimThreads) bcache_victim_kernel(ResolveSt
 //  * With sel != NULL, the pool page id of every lookup: its slot (hits, and
 //    misses placed in a slot by this call) or its overflow page.
 //  * Every page of the miss list (count entries) is copied from the host copy
-//    into its pool page: one warp per page in turn, each lane keeping 8 loads
-//    of 16 bytes in flight over the host link.
+//    into its pool page: one warp per page, each lane keeping 8 loads of 16
+//    bytes in flight over the host link.  Warps take pages from a counter
+//    (ctl word kCtlNext, zero before the launch), so CTAs that start late --
+//    the SMs busy with other work -- take fewer pages instead of holding up
+//    the copy.
 constexpr int kFetchThreads = 256;
 __global__ void __launch_bounds__(kFetchThreads, 1) bcache_fetch_kernel(const uint64_t *__restrict__ count,
                                                                         const int32_t *__restrict__ miss_page,
@@ -314,10 +356,13 @@ __global__ void __launch_bounds__(kFetchThreads, 1) bcache_fetch_kernel(const ui
     constexpr int kU = 4;
     const int64_t n = static_cast<int64_t>(*count);
     const int lane = threadIdx.x & 31;
-    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     const int64_t n16 = page_bytes / 16;
-    for (int64_t m = warp; m < n; m += n_warps) {
+    unsigned long long *next = reinterpret_cast<unsigned long long *>(r.ctl + kCtlNext);
+    for (;;) {
+        unsigned long long i = 0;
+        if (lane == 0) i = atomicAdd(next, 1ull);
+        const int64_t m = static_cast<int64_t>(__shfl_sync(0xffffffffu, i, 0));
+        if (m >= n) break;
         const int64_t src = static_cast<int64_t>(miss_page[m]) * page_bytes;
         const int64_t dst = static_cast<int64_t>(miss_dest[m]) * page_bytes;
         const uint4 *sk = reinterpret_cast<const uint4 *>(host_k + src);
@@ -453,7 +498,10 @@ __global__ void ring_restore_kernel(int64_t first, int n_blk, int Hk, int64_t ri
         miss_dest[i] = slot;
         slot_page[slot] = static_cast<int32_t>(b * Hk + k);
     }
-    if (threadIdx.x == 0) ctl[9] = static_cast<uint64_t>(n);
+    if (threadIdx.x == 0) {
+        ctl[9] = static_cast<uint64_t>(n);
+        ctl[kCtlNext] = 0;                       // the fetch's page counter
+    }
 }
 
 // Page lists [S][Hk][n_blk] of blocks first .. first + n_blk - 1 through the ring.
@@ -755,6 +803,7 @@ extern "C" int skv_bcache_ring_restore(skv_bcache *c, int64_t n_keys, void *stre
     if (e != cudaSuccess) return skv::cuda_fail(h, e, "ring restore launch");
     ResolveState none;
     memset(&none, 0, sizeof(none));
+    none.ctl = c->ctl;                           // the fetch's page counter
     bcache_fetch_kernel<<<h->sm_count, kFetchThreads, 0, st>>>(c->ctl + 9, c->miss_page, c->miss_dest, c->host_k,
                                                                c->host_v, c->pool_k, c->pool_v, c->page_bytes, none,
                                                                nullptr, 0, 0, 0, nullptr);
