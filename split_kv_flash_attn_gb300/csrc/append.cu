@@ -24,8 +24,11 @@
 //    t0 = x * rd lies within 2^-21.6 |t0| of x/d (5e-5 for |x/d| < 130), and
 //    the fp32 quotient fl(x/d) within 2^-17 of x/d; so when t0 is more than
 //    2^-13 (1.2e-4) away from every half-integer, rint(t0) = rint(fl(x/d)).
-//    Nearer than that (about 1 value in 4000, and every exact tie), the code
-//    is taken from the IEEE division itself; |t0| >= 130 clamps either way.
+//    Nearer than that (about 1 value in 4000, and every exact tie), the
+//    codes are taken from the IEEE division itself.  With a normal fp16
+//    scale |x/d| < qmax + 0.5, so only a subnormal scale needs the clamp, and
+//    for it (d < 2^-14) a large |t0| rounds far from any half-integer and
+//    clamps the same either way.
 //  * the scale: s0 = amax * fl(1/qmax) lies within 2^-22.4 (relative) of
 //    fl(amax/qmax); when s0 (1 - 2^-20) and s0 (1 + 2^-20) round to the same
 //    fp16 value, so does fl(amax/qmax) (rounding is monotone); otherwise the
@@ -61,14 +64,10 @@ __device__ __forceinline__ float rcp_approx(float d)
     return r;
 }
 
-// rint(fl(x / d)) for d > 0, rd = rcp_approx(d) (see the header).
-__device__ __forceinline__ int nearest_code(float x, float d, float rd)
+// Bytes 0 of four words, in order, as one word.
+__device__ __forceinline__ uint32_t low_bytes4(uint32_t a, uint32_t b, uint32_t c, uint32_t d)
 {
-    const float t0 = __fmul_rn(x, rd);
-    if (fabsf(t0) >= 130.f) return t0 > 0.f ? 1024 : -1024;       // clamped by every code range
-    const float r0 = rintf(t0);
-    if (0.5f - fabsf(t0 - r0) > 0x1p-13f) return static_cast<int>(r0);
-    return __float2int_rn(__fdiv_rn(x, d));
+    return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
 }
 
 // Each warp takes kItemsPerWarp consecutive (row, head) items: it loads all of
@@ -158,15 +157,36 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(const float *
             for (int off = LPB / 2; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
             const __half d16 = block_scale(amax, QMAX, INV_QMAX);
             const float d = __half2float(d16);
+            // d = 0 (a zero block, or a scale below fp16's range) makes every
+            // product, and so every code, 0.
             const float rd = d > 0.f ? rcp_approx(d) : 0.f;
-            uint32_t packed = 0;                                  // VPL code bytes / nibbles, value j0 + i in byte i
+            // The lane's codes rint(x * rd), kept when every product is more
+            // than 2^-13 from a half-integer; otherwise all VPL codes of the
+            // lane come from the IEEE division (see the header).
+            int q[VPL];
+            float off = 0.f;
 #pragma unroll
             for (int i = 0; i < VPL; ++i) {
-                const int q = d > 0.f ? nearest_code(v[it][i], d, rd) : 0;
-                const uint32_t c = T == SKV_Q8_0 ? static_cast<uint32_t>(max(-127, min(127, q)) & 0xff)
-                                                 : static_cast<uint32_t>(max(0, min(15, q + 8)));
-                packed |= c << (8 * i);
+                const float t0 = __fmul_rn(v[it][i], rd);
+                const float r0 = rintf(t0);
+                off = fmaxf(off, fabsf(t0 - r0));
+                q[i] = static_cast<int>(r0);
             }
+            if (off >= 0.5f - 0x1p-13f) {
+#pragma unroll
+                for (int i = 0; i < VPL; ++i) q[i] = __float2int_rn(__fdiv_rn(v[it][i], d));
+            }
+            // A normal fp16 scale is within 2^-11 of amax / qmax, so |x / d| <
+            // qmax + 0.5 and every code is in range; a subnormal one is not.
+            if (d < 0x1p-14f) {
+                constexpr int QLO = T == SKV_Q8_0 ? -127 : -8, QHI = T == SKV_Q8_0 ? 127 : 7;   // codes -127..127, 0..15
+#pragma unroll
+                for (int i = 0; i < VPL; ++i) q[i] = max(QLO, min(QHI, q[i]));
+            }
+            uint32_t c[4] = {0u, 0u, 0u, 0u};                      // code bytes / nibbles of values j0 + i
+#pragma unroll
+            for (int i = 0; i < VPL; ++i) c[i] = static_cast<uint32_t>(T == SKV_Q8_0 ? q[i] : q[i] + 8);
+            const uint32_t packed = low_bytes4(c[0], c[1], c[2], c[3]);   // value j0 + i in byte i
             uint8_t *blk = row + static_cast<int64_t>(h) * VPL * BLK + b * BLK;   // 2-byte aligned
             if (T == SKV_Q8_0) {
                 uint16_t *dst = reinterpret_cast<uint16_t *>(blk + 2 + j0);

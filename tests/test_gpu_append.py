@@ -65,10 +65,13 @@ def _tie_blocks(rng, x, qmax):
     where a product with a reciprocal and the fp32 quotient could decide
     differently: values on and within 3 ulps of half-integer multiples of the
     block's scale (exact ties included), block maxima whose amax/qmax falls
-    exactly between two fp16 values, and blocks with fp16-subnormal scales."""
+    exactly between two fp16 values, and blocks with fp16-subnormal scales --
+    some so small that the rounded scale leaves |x / d| past qmax + 0.5 (the
+    clamps: q8_0 at +-127, q4_0 at 0 and 15) or rounds to zero."""
     blocks = x.reshape(-1, 32)
     nb = blocks.shape[0]
-    kind = rng.integers(0, 4, nb)              # 0: untouched, 1: ties, 2: fp16-midpoint scale, 3: subnormal scale
+    # 0: untouched, 1: ties, 2: fp16-midpoint scale, 3: subnormal scale, 4: a few fp16 ulps of scale
+    kind = rng.integers(0, 5, nb)
     d = rng.uniform(1e-3, 0.05, nb).astype(np.float16).astype(np.float32)
     k = rng.integers(-qmax, qmax, (nb, 32)).astype(np.float32)
     t = (k + 0.5) * d[:, None]                 # exact in fp32 (9-bit x 11-bit products)
@@ -87,6 +90,8 @@ def _tie_blocks(rng, x, qmax):
     blocks[mid, 5] = -qmax * m[mid]            # exact: 12-bit x 7-bit product
     sub = kind == 3
     blocks[sub] *= np.float32(2e-5)
+    tiny = kind == 4
+    blocks[tiny] *= np.float32(1e-6)
     return x
 
 
