@@ -71,17 +71,19 @@ __device__ __forceinline__ uint32_t low_bytes4(uint32_t a, uint32_t b, uint32_t 
 }
 
 // Each warp takes kItemsPerWarp consecutive (row, head) items: it loads all of
-// their values first (D/32 per lane each), then converts and stores, so a warp
-// keeps several loads in flight.  Positions outside [0, n_rows0 + n_rows1) are
-// skipped; a non-negative one also sets bit 1 of *status.
+// their values first, then converts and stores, so a warp keeps several loads
+// in flight.  Positions outside [0, n_rows0 + n_rows1) are skipped; a
+// non-negative one also sets bit 1 of *status.  The fp16 kernel gives each
+// lane D/32 values of an item.
 constexpr int kItemsPerWarp = 4;
 constexpr int kAppendThreads = 256;
 
-template <int T, bool VEC8, int DD>
-__global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(const float *__restrict__ x,
-                                                                   const int32_t *__restrict__ pos, int n, int Hk,
-                                                                   int64_t row_bytes, uint8_t *dst0, int64_t n_rows0,
-                                                                   uint8_t *dst1, int64_t n_rows1, int *status)
+template <bool VEC8, int DD>
+__global__ void __launch_bounds__(kAppendThreads) kv_append_f16_kernel(const float *__restrict__ x,
+                                                                       const int32_t *__restrict__ pos, int n, int Hk,
+                                                                       int64_t row_bytes, uint8_t *dst0,
+                                                                       int64_t n_rows0, uint8_t *dst1,
+                                                                       int64_t n_rows1, int *status)
 {
     constexpr int VPL = DD / 32;                                  // values per lane per item
     const int lane = threadIdx.x & 31;
@@ -130,81 +132,139 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(const float *
             continue;
         }
         uint8_t *row = p[it] < n_rows0 ? dst0 + p[it] * row_bytes : dst1 + (p[it] - n_rows0) * row_bytes;
-        if constexpr (T == SKV_F16) {
-            uint8_t *out = row + static_cast<int64_t>(h) * DD * 2 + lane * VPL * 2;
-            if (VPL == 4) {
-                const uint32_t w0 = pack_half2(v[it][0], v[it][1]), w1 = pack_half2(v[it][2], v[it][3]);
-                if (VEC8) {
-                    *reinterpret_cast<uint2 *>(out) = make_uint2(w0, w1);
-                } else {
-                    reinterpret_cast<uint32_t *>(out)[0] = w0;        // rows are 4-byte aligned
-                    reinterpret_cast<uint32_t *>(out)[1] = w1;
-                }
+        uint8_t *out = row + static_cast<int64_t>(h) * DD * 2 + lane * VPL * 2;
+        if (VPL == 4) {
+            const uint32_t w0 = pack_half2(v[it][0], v[it][1]), w1 = pack_half2(v[it][2], v[it][3]);
+            if (VEC8) {
+                *reinterpret_cast<uint2 *>(out) = make_uint2(w0, w1);
             } else {
-                *reinterpret_cast<uint32_t *>(out) = pack_half2(v[it][0], v[it][1]);
+                reinterpret_cast<uint32_t *>(out)[0] = w0;        // rows are 4-byte aligned
+                reinterpret_cast<uint32_t *>(out)[1] = w1;
             }
         } else {
-            // lane holds values j0 .. j0 + VPL - 1 of block b (LPB lanes per block)
-            constexpr int BLK = T == SKV_Q8_0 ? 34 : 18;
-            constexpr int LPB = 32 / VPL;
-            constexpr float QMAX = T == SKV_Q8_0 ? 127.f : 7.f;
-            constexpr float INV_QMAX = 1.f / QMAX;
-            const int b = lane / LPB, j0 = (lane % LPB) * VPL;
-            float amax = 0.f;
+            *reinterpret_cast<uint32_t *>(out) = pack_half2(v[it][0], v[it][1]);
+        }
+    }
+}
+
+// Quantising append with eight values a lane: LPI = D / 8 lanes per (row,
+// head) item and four lanes per 32-value block, so 32 / LPI items share each
+// warp instruction and the per-block work (maximum, scale, reciprocal) and the
+// per-item work (position, destination) are spread over eight values.  Each
+// warp takes kItemsPerWarp consecutive items; all their values are loaded
+// before any is converted.  The codes are decided as described at the top.
+template <int T, int DD>
+__global__ void __launch_bounds__(kAppendThreads) kv_append_quant_kernel(const float *__restrict__ x,
+                                                                         const int32_t *__restrict__ pos, int n,
+                                                                         int Hk, int64_t row_bytes, uint8_t *dst0,
+                                                                         int64_t n_rows0, uint8_t *dst1,
+                                                                         int64_t n_rows1, int *status)
+{
+    constexpr int LPI = DD / 8;                                   // lanes per item
+    constexpr int IPS = 32 / LPI;                                 // items per warp step
+    constexpr int STEPS = kItemsPerWarp / IPS;
+    static_assert(STEPS * IPS == kItemsPerWarp, "items per warp");
+    constexpr int BLK = T == SKV_Q8_0 ? 34 : 18;
+    constexpr float QMAX = T == SKV_Q8_0 ? 127.f : 7.f;
+    constexpr float INV_QMAX = 1.f / QMAX;
+    const int lane = threadIdx.x & 31;
+    const int l = lane % LPI;                                     // lane within its item
+    const int b = l >> 2, j0 = (l & 3) * 8;                       // block, first value of the lane
+    const int64_t total = static_cast<int64_t>(n) * Hk;
+    const int64_t first =
+        (static_cast<int64_t>(blockIdx.x) * (kAppendThreads / 32) + (threadIdx.x >> 5)) * kItemsPerWarp;
+    // (row, head) of the warp's first item with one division; the lane's items
+    // first + s * IPS + lane / LPI step through the heads from there.
+    const int64_t row_first = first / Hk;
+    const int h_first = static_cast<int>(first - row_first * Hk);
+    float v[STEPS][8];
+    int64_t p[STEPS];
+    int hd[STEPS];
 #pragma unroll
-            for (int i = 0; i < VPL; ++i) amax = fmaxf(amax, fabsf(v[it][i]));
+    for (int s = 0; s < STEPS; ++s) {
+        const int o = s * IPS + lane / LPI;                       // item offset within the warp, < kItemsPerWarp
+        int hh = h_first;
+        int64_t row = row_first;
 #pragma unroll
-            for (int off = LPB / 2; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-            const __half d16 = block_scale(amax, QMAX, INV_QMAX);
-            const float d = __half2float(d16);
-            // d = 0 (a zero block, or a scale below fp16's range) makes every
-            // product, and so every code, 0.
-            const float rd = d > 0.f ? rcp_approx(d) : 0.f;
-            // The lane's codes rint(x * rd), kept when every product is more
-            // than 2^-13 from a half-integer; otherwise all VPL codes of the
-            // lane come from the IEEE division (see the header).
-            int q[VPL];
-            float off = 0.f;
-#pragma unroll
-            for (int i = 0; i < VPL; ++i) {
-                const float t0 = __fmul_rn(v[it][i], rd);
-                const float r0 = rintf(t0);
-                off = fmaxf(off, fabsf(t0 - r0));
-                q[i] = static_cast<int>(r0);
-            }
-            if (off >= 0.5f - 0x1p-13f) {
-#pragma unroll
-                for (int i = 0; i < VPL; ++i) q[i] = __float2int_rn(__fdiv_rn(v[it][i], d));
-            }
-            // A normal fp16 scale is within 2^-11 of amax / qmax, so |x / d| <
-            // qmax + 0.5 and every code is in range; a subnormal one is not.
-            if (d < 0x1p-14f) {
-                constexpr int QLO = T == SKV_Q8_0 ? -127 : -8, QHI = T == SKV_Q8_0 ? 127 : 7;   // codes -127..127, 0..15
-#pragma unroll
-                for (int i = 0; i < VPL; ++i) q[i] = max(QLO, min(QHI, q[i]));
-            }
-            uint32_t c[4] = {0u, 0u, 0u, 0u};                      // code bytes / nibbles of values j0 + i
-#pragma unroll
-            for (int i = 0; i < VPL; ++i) c[i] = static_cast<uint32_t>(T == SKV_Q8_0 ? q[i] : q[i] + 8);
-            const uint32_t packed = low_bytes4(c[0], c[1], c[2], c[3]);   // value j0 + i in byte i
-            uint8_t *blk = row + static_cast<int64_t>(h) * VPL * BLK + b * BLK;   // 2-byte aligned
-            if (T == SKV_Q8_0) {
-                uint16_t *dst = reinterpret_cast<uint16_t *>(blk + 2 + j0);
-#pragma unroll
-                for (int w = 0; w < VPL / 2; ++w) dst[w] = static_cast<uint16_t>(packed >> (16 * w));
-            } else {
-                // byte j holds value j (low nibble) and value j + 16 (high
-                // nibble): the lane LPB/2 further on holds values j0 + 16 ..
-                const uint32_t high = __shfl_down_sync(0xffffffffu, packed, LPB / 2);
-                if (j0 < 16) {
-                    const uint32_t bytes = packed | (high << 4);
-                    uint16_t *dst = reinterpret_cast<uint16_t *>(blk + 2 + j0);
-#pragma unroll
-                    for (int w = 0; w < VPL / 2; ++w) dst[w] = static_cast<uint16_t>(bytes >> (16 * w));
+        for (int k = 0; k < kItemsPerWarp - 1; ++k) {
+            if (k < o) {
+                if (++hh == Hk) {
+                    hh = 0;
+                    ++row;
                 }
             }
-            if (j0 == 0) *reinterpret_cast<__half *>(blk) = d16;
         }
+        hd[s] = hh;
+        const int64_t item = first + o;
+        p[s] = -1;
+        if (item < total) {
+            p[s] = pos[row];
+            const float4 *src = reinterpret_cast<const float4 *>(x + item * DD) + 2 * l;
+            const float4 a0 = src[0], a1 = src[1];
+            v[s][0] = a0.x; v[s][1] = a0.y; v[s][2] = a0.z; v[s][3] = a0.w;
+            v[s][4] = a1.x; v[s][5] = a1.y; v[s][6] = a1.z; v[s][7] = a1.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[s][i] = 0.f;
+        }
+    }
+#pragma unroll
+    for (int s = 0; s < STEPS; ++s) {
+        // every lane takes part in the block's shuffles; only valid items store
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[s][i]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        const __half d16 = block_scale(amax, QMAX, INV_QMAX);
+        const float d = __half2float(d16);
+        const float rd = d > 0.f ? rcp_approx(d) : 0.f;           // d = 0: every code 0
+        int q[8];
+        float off = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float t0 = __fmul_rn(v[s][i], rd);
+            const float r0 = rintf(t0);
+            off = fmaxf(off, fabsf(t0 - r0));
+            q[i] = static_cast<int>(r0);
+        }
+        if (off >= 0.5f - 0x1p-13f) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) q[i] = __float2int_rn(__fdiv_rn(v[s][i], d));
+        }
+        if (d < 0x1p-14f) {
+            constexpr int QLO = T == SKV_Q8_0 ? -127 : -8, QHI = T == SKV_Q8_0 ? 127 : 7;   // codes -127..127, 0..15
+#pragma unroll
+            for (int i = 0; i < 8; ++i) q[i] = max(QLO, min(QHI, q[i]));
+        }
+        uint32_t c[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) c[i] = static_cast<uint32_t>(T == SKV_Q8_0 ? q[i] : q[i] + 8);
+        uint32_t w0 = low_bytes4(c[0], c[1], c[2], c[3]), w1 = low_bytes4(c[4], c[5], c[6], c[7]);
+        if (T == SKV_Q4_0) {
+            // byte j holds value j (low nibble) and value j + 16 (high nibble):
+            // the lane two further on holds values j0 + 16 ..
+            const uint32_t h0 = __shfl_down_sync(0xffffffffu, w0, 2), h1 = __shfl_down_sync(0xffffffffu, w1, 2);
+            w0 |= h0 << 4;
+            w1 |= h1 << 4;
+        }
+        const int64_t ps = p[s];
+        if (ps < 0) continue;                                     // beyond the items, or not written
+        const int h = hd[s];
+        if (ps >= n_rows0 + n_rows1) {
+            if (l == 0 && h == 0) atomicOr(status, 2);
+            continue;
+        }
+        uint8_t *row = ps < n_rows0 ? dst0 + ps * row_bytes : dst1 + (ps - n_rows0) * row_bytes;
+        uint8_t *blk = row + static_cast<int64_t>(h) * (DD / 32) * BLK + b * BLK;   // 2-byte aligned
+        if (T == SKV_Q8_0 || j0 < 16) {
+            uint16_t *dst = reinterpret_cast<uint16_t *>(blk + 2 + j0);
+            dst[0] = static_cast<uint16_t>(w0);
+            dst[1] = static_cast<uint16_t>(w0 >> 16);
+            dst[2] = static_cast<uint16_t>(w1);
+            dst[3] = static_cast<uint16_t>(w1 >> 16);
+        }
+        if (j0 == 0) *reinterpret_cast<__half *>(blk) = d16;
     }
 }
 
@@ -260,25 +320,30 @@ extern "C" int skv_kv_append(skv_handle *h, int32_t type, int32_t Hk, int32_t D,
         return fail(h, SKV_EUNSUPPORTED, "too many rows for one launch");
     const unsigned grid = static_cast<unsigned>((items + per_block - 1) / per_block);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-#define SKV_APPEND(TT, V, DDD)                                                                                     \
-    kv_append_kernel<TT, V, DDD><<<grid, kAppendThreads, 0, st>>>(x, positions, n, Hk, row_bytes, d0, n_rows0, d1, \
+#define SKV_APPEND(V, DDD)                                                                                    \
+    kv_append_f16_kernel<V, DDD><<<grid, kAppendThreads, 0, st>>>(x, positions, n, Hk, row_bytes, d0, n_rows0, d1, \
                                                                   n_rows1, h->status)
-#define SKV_APPEND_D(TT, V) \
-    do {                    \
-        if (D == 64)        \
-            SKV_APPEND(TT, V, 64); \
-        else                \
-            SKV_APPEND(TT, V, 128); \
-    } while (0)
     if (type == SKV_F16) {
-        if (vec8) SKV_APPEND_D(SKV_F16, true);
-        else SKV_APPEND_D(SKV_F16, false);
-    } else if (type == SKV_Q8_0) {
-        SKV_APPEND_D(SKV_Q8_0, false);
+        if (vec8) {
+            if (D == 64) SKV_APPEND(true, 64);
+            else SKV_APPEND(true, 128);
+        } else {
+            if (D == 64) SKV_APPEND(false, 64);
+            else SKV_APPEND(false, 128);
+        }
     } else {
-        SKV_APPEND_D(SKV_Q4_0, false);
+#define SKV_APPEND_Q(TT, DDD)                                                                              \
+    kv_append_quant_kernel<TT, DDD><<<grid, kAppendThreads, 0, st>>>(x, positions, n, Hk, row_bytes, d0, \
+                                                                     n_rows0, d1, n_rows1, h->status)
+        if (type == SKV_Q8_0) {
+            if (D == 64) SKV_APPEND_Q(SKV_Q8_0, 64);
+            else SKV_APPEND_Q(SKV_Q8_0, 128);
+        } else {
+            if (D == 64) SKV_APPEND_Q(SKV_Q4_0, 64);
+            else SKV_APPEND_Q(SKV_Q4_0, 128);
+        }
+#undef SKV_APPEND_Q
     }
-#undef SKV_APPEND_D
 #undef SKV_APPEND
     return cuda_fail(h, cudaGetLastError(), "append launch");
 }
