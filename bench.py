@@ -537,7 +537,8 @@ def run_extras(torch, skv, wl, h, hbm_peak):
             hit_b = bs["call_bytes"] - miss_b
             t_hit, t_miss = hit_b / (hbm_peak * 1e9) * 1e3, miss_b / (h2d * 1e9) * 1e3
             bs.update({"bound_ms_serial": t_hit + t_miss, "bound_ms_overlapped": max(t_hit, t_miss),
-                       "frac_of_serial_bound": (t_hit + t_miss) / bs["warm_ms"]})
+                       "frac_of_serial_bound": (t_hit + t_miss) / bs["warm_ms"],
+                       "frac_of_overlapped_bound": max(t_hit, t_miss) / bs["warm_ms"]})
         out["block_sparse"] = bs
     except Exception as exc:  # noqa: BLE001
         out["block_sparse_error"] = repr(exc)[:300]
