@@ -366,9 +366,22 @@ int skv_bcache_resolve(skv_bcache *c, const int32_t *sel, int32_t S, int32_t n_s
 int skv_bcache_append(skv_bcache *c, const float *k_new, const float *v_new, const int32_t *positions, int32_t n,
                       void *stream);
 
-/* Resolve, then attention through the pool (skv_attn_paged with page_rows =
- * block_rows) for q of shape [S][nq][H][D] ("Strata compare", KV streaming:
- * resolve, copy the missed blocks, attend), all on `stream`. */
+/* Resolve, copy the missed blocks and attend, for q of shape [S][nq][H][D]
+ * ("Strata compare", KV streaming), all on `stream`; residency decisions and
+ * counters are those of skv_bcache_resolve.
+ * With block_rows = 64 and at most 8 query rows per KV head (nq * H / Hk <=
+ * 8), the copy and the attention are one pass: after the lookup, one
+ * persistent launch reads each missed page from the host copy in the work
+ * item (8 pages of one list) of the page's first lookup, writes it to that
+ * lookup's overflow page and attends to it; later lookups of the page read it
+ * from there once written; resident pages are read from their slots; the
+ * claim / victim / placement pass runs inside the same launch, and the misses
+ * it places in slots are moved there afterwards.  The result is bitwise that
+ * of the same call on a cache that holds every page (all hits), and the last
+ * page ids (skv_bcache_pool) are the slots of resident and placed pages and
+ * the overflow page of each other page's first lookup.
+ * Otherwise: skv_bcache_resolve, then skv_attn_paged (page_rows = block_rows)
+ * through the pool. */
 int skv_bcache_attn(skv_bcache *c, const skv_shape *shape, const void *q, const int32_t *sel, int32_t n_sel,
                     float *o, float *lse, void *stream);
 

@@ -754,6 +754,65 @@ int skv_attn_paged(skv_handle *h, const skv_shape *shape, const void *q, const v
 
 namespace skv {
 
+int attn_paged_fused(skv_handle *h, const skv_shape *shape, const void *q, const void *k_pages, const void *v_pages,
+                     const int32_t *page_ids, int32_t pages_per_list, float *o, float *lse, cudaStream_t st,
+                     const DecodeArgs &fuse)
+{
+    if (!shape) return fail(h, SKV_EINVAL, "shape is NULL");
+    if (shape->k_type != SKV_F16 || shape->v_type != SKV_F16)
+        return fail(h, SKV_EUNSUPPORTED, "paged attention reads fp16 pages");
+    skv_shape sh = *shape;
+    sh.k_row_bytes = sh.v_row_bytes = static_cast<int64_t>(sh.Hk) * 2 * sh.D;
+    int G = 0, n_cg = 0;
+    int rc = check_shape(h, &sh, &G, &n_cg);
+    if (rc) return rc;
+    if (n_cg != 1) return fail(h, SKV_EUNSUPPORTED, "the fused block-cache attention takes one column group");
+    if (!q || !o || !lse || !k_pages || !v_pages || !page_ids || pages_per_list <= 0)
+        return fail(h, SKV_EINVAL, "NULL pointer or empty page lists");
+    const int D = sh.D;
+    const int64_t R = static_cast<int64_t>(sh.S) * sh.nq * sh.H;
+    // splits of kFusedSplitPages pages: the work items the persistent grid
+    // takes in lookup order, small enough that the host link stays busy to
+    // the end
+    const int32_t n_splits = (pages_per_list + kFusedSplitPages - 1) / kFusedSplitPages;
+    if (n_splits > kMaxSplits) return fail(h, SKV_EUNSUPPORTED, "%d splits exceed %d", n_splits, kMaxSplits);
+    if (static_cast<int64_t>(sh.S) * sh.Hk > kMaxUnits) return fail(h, SKV_EUNSUPPORTED, "too many units");
+    DecodeArgs a = base_args(&sh, G, n_cg, q, nullptr, 0, nullptr, 0);
+    a.k = static_cast<const uint8_t *>(k_pages);
+    a.v = static_cast<const uint8_t *>(v_pages);
+    a.row_mode = ROWS_PAGED;
+    a.rows = page_ids;
+    a.rows_ld = pages_per_list;
+    a.rows_per_head = 1;
+    a.page_rows = kDecodeTile;
+    a.n_local = static_cast<int64_t>(pages_per_list) * kDecodeTile;
+    a.n_splits = n_splits;
+    a.split_len = static_cast<int64_t>(kFusedSplitPages) * kDecodeTile;
+    a.counters = h->counters;
+    a.o_out = o;
+    a.lse_out = lse;
+    a.status = h->status;
+    a.rstate = fuse.rstate;
+    a.sel = fuse.sel;
+    a.n_look = fuse.n_look;
+    a.page_ids_out = fuse.page_ids_out;
+    a.host_k = fuse.host_k;
+    a.host_v = fuse.host_v;
+    a.page_ready = fuse.page_ready;
+    a.epoch = fuse.epoch;
+    a.steal = fuse.steal;
+    if (n_splits > 1) {
+        const size_t o_bytes = round_up(static_cast<size_t>(n_splits) * R * D * sizeof(float), 256);
+        if ((rc = ensure_workspace(h, o_bytes + static_cast<size_t>(n_splits) * R * sizeof(float), st))) return rc;
+        a.o_split = static_cast<float *>(h->workspace);
+        a.lse_split = reinterpret_cast<float *>(static_cast<uint8_t *>(h->workspace) + o_bytes);
+    }
+    if (h->prof_before) cudaEventRecord(h->prof_before, st);
+    rc = launch_decode_fused(h, a, D, st);
+    if (h->prof_after) cudaEventRecord(h->prof_after, st);
+    return rc;
+}
+
 int attn_paged_range(skv_handle *h, const skv_shape *shape, const void *q, const void *k_pages, const void *v_pages,
                      int32_t page_rows, const int32_t *page_ids, int32_t pages_per_list, int64_t key_lo,
                      int64_t key_hi, float *o, float *lse, cudaStream_t st)

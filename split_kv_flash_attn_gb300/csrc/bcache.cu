@@ -27,19 +27,23 @@
 //   fetch + ids  (persistent grid)  every missed page is copied from the host
 //                    copy into its pool page over the host link, and every
 //                    lookup gets its pool page id.
-// Attention then reads the pages through the ids.  (Attending to the pages
-// resident at entry while the misses stream, with the partial results merged
-// afterwards, was measured and not kept: an attention launch over a page list
-// costs nearly as much when most of its pages are absent, so the part left
-// after the fetch did not shrink.)  Two readings of our own: the unit is a
-// (block, KV head) page because the selection is per KV head, and an
-// oversubscribed call reads its excess misses from the host once instead of
-// failing.
+// Attention then reads the pages through the ids.  skv_bcache_attn on 64-row
+// pages copies and attends in one pass instead: the lookup, the fused
+// attention (decode_kernel.cuh), whose CTA 0 runs the claim / victim /
+// placement pass while the other CTAs stage every missed page from the host
+// copy in the overflow page of its first lookup, and a last launch that moves
+// the misses placed in slots there (bcache_attn_fused below).  (Attending to
+// the pages resident at entry on another stream while the misses stream was
+// measured and not kept: on this part a kernel that saturates HBM slows the
+// host-link copy beside it by about as much as it takes.)  Two readings of
+// our own: the unit is a (block, KV head) page because the selection is per KV
+// head, and an oversubscribed call reads its excess misses from the host once
+// instead of failing.
 #include <string.h>
 
 #include <algorithm>
-#include <cub/block/block_scan.cuh>
 
+#include "bcache_resolve.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -69,49 +73,21 @@ struct skv_bcache {
     uint8_t *pool_k = nullptr;         // [(n_slots + max_lookups) pages][page_bytes]; ring: [n_slots]
     uint8_t *pool_v = nullptr;
     int64_t ring_blocks = 0;           // > 0: ring layout, page (b, k) -> slot (b % ring_blocks) * Hk + k
+    void *rstate = nullptr;            // the ResolveState of this cache, in device memory (fused attention)
+    int32_t *page_ready = nullptr;     // [pool pages] epoch of the call that last published the page
 };
 
 namespace skv {
-
-// ctl words (uint64): 0 epoch of the last resolve, 1 hand, 2 calls, 3 lookups,
-// 4 hits, 5 misses, 6 overflow, 7 last misses, 8 last overflow, 9 pages a ring
-// restore fetches, 11 misses placed in slots by the last resolve, 12 misses of
-// the last resolve, 13 pages the running fetch has handed out.
-constexpr int kCtlWords = 16;
-constexpr int kCtlNext = 13;
-constexpr int kVictimThreads = 512;
-
-struct ResolveState {
-    int32_t *page_table;
-    uint64_t *page_claim;
-    int32_t *page_miss;
-    int32_t *slot_page, *slot_epoch, *slot_ref, *victim;
-    int32_t *miss_page, *miss_dest;
-    uint64_t *ctl;
-    int n_slots;
-    int64_t n_pages;
-};
-
-__device__ __forceinline__ int64_t lookup_page(const int32_t *sel, int64_t e, int n_sel, int Hk, int64_t n_pages)
-{
-    const int64_t b = sel[e];
-    const int64_t p = b * Hk + (e / n_sel) % Hk;
-    return (b < 0 || p >= n_pages) ? -1 : p;     // out-of-range ids are rejected here; never indexed
-}
-
-// Claim key of lookup e in call `epoch`: a later call, then an earlier lookup,
-// compares larger.
-__device__ __forceinline__ unsigned long long claim_key(int epoch, int64_t e)
-{
-    return (static_cast<unsigned long long>(static_cast<uint32_t>(epoch)) << 32) |
-           static_cast<unsigned long long>(0xffffffffu - static_cast<uint32_t>(e));
-}
 
 // Lookup pass (this call's epoch is one past the last resolve's).
 __global__ void __launch_bounds__(256) bcache_lookup_kernel(ResolveState r, const int32_t *__restrict__ sel,
                                                             int64_t n_look, int n_sel, int Hk)
 {
     const int epoch = static_cast<int>(r.ctl[0]) + 1;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        r.ctl[kCtlEpochNow] = static_cast<uint64_t>(epoch);
+        r.ctl[kCtlSteal] = 0;
+    }
     unsigned looks = 0, hits = 0;
     for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n_look;
          e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -139,186 +115,11 @@ __global__ void __launch_bounds__(256) bcache_lookup_kernel(ResolveState r, cons
     }
 }
 
-// Claim, victim and placement pass, one CTA.
-//  1. Miss list: lookup e owns page p when p's claim word holds e's key (the
-//     first lookup of this call naming a missing p); owners are numbered in
-//     lookup order by a block scan, tile by tile.
-//  2. Victims: thread t owns hand-relative positions [t*per, (t+1)*per);
-//     position i is slot (hand + i) % n_slots.
-//  3. Placement (below).
-constexpr int kClaimItems = 16;   // lookups per thread and tile of step 1
-constexpr int kSlotItems = 16;    // slots per thread whose classes stay in registers in step 2
-constexpr int kPlaceBatch = 16;   // misses per thread and round of step 3
+// Claim, victim and placement pass as its own launch (one CTA).
 __global__ void __launch_bounds__(kVictimThreads) bcache_victim_kernel(ResolveState r, const int32_t *__restrict__ sel,
                                                                        int64_t n_look, int n_sel, int Hk)
 {
-    using Scan = cub::BlockScan<unsigned long long, kVictimThreads>;
-    __shared__ typename Scan::TempStorage scan_tmp;
-    __shared__ int s_stop;
-    const int epoch = static_cast<int>(r.ctl[0]) + 1;
-    if (threadIdx.x == 0) r.ctl[kCtlNext] = 0;      // the fetch's page counter
-    // 1. the miss list in lookup order
-    int64_t need = 0;
-    for (int64_t t0 = 0; t0 < n_look; t0 += static_cast<int64_t>(kVictimThreads) * kClaimItems) {
-        const int64_t e0 = t0 + static_cast<int64_t>(threadIdx.x) * kClaimItems;
-        // lookups are [S][Hk][n_sel]: the KV head of e0, stepped item by item
-        const int64_t row = e0 / n_sel;
-        int col = static_cast<int>(e0 - row * n_sel);
-        int kh = static_cast<int>(row % Hk);
-        int32_t pg[kClaimItems];
-#pragma unroll
-        for (int u = 0; u < kClaimItems; ++u) {
-            const int64_t e = e0 + u;
-            int32_t p = -1;
-            if (e < n_look) {
-                const int64_t blk = sel[e];
-                const int64_t pp = blk * Hk + kh;
-                if (blk >= 0 && pp < r.n_pages) p = static_cast<int32_t>(pp);   // out-of-range ids: no page
-            }
-            pg[u] = p;
-            if (++col == n_sel) {
-                col = 0;
-                if (++kh == Hk) kh = 0;
-            }
-        }
-        unsigned own = 0;                            // bit u: lookup e0 + u owns its page
-#pragma unroll
-        for (int u = 0; u < kClaimItems; ++u)
-            if (pg[u] >= 0 && r.page_claim[pg[u]] == claim_key(epoch, e0 + u)) own |= 1u << u;
-        unsigned long long before = 0, total = 0;
-        Scan(scan_tmp).ExclusiveSum(static_cast<unsigned long long>(__popc(own)), before, total);
-        int64_t m = need + static_cast<int64_t>(before);
-#pragma unroll
-        for (int u = 0; u < kClaimItems; ++u) {
-            if (own & (1u << u)) {
-                r.miss_page[m] = pg[u];
-                r.page_miss[pg[u]] = static_cast<int32_t>(m);
-                ++m;
-            }
-        }
-        need += static_cast<int64_t>(total);
-        __syncthreads();                             // scan_tmp is reused
-    }
-    // 2. victims
-    const int n = r.n_slots;
-    const int hand = static_cast<int>(r.ctl[1] % static_cast<uint64_t>(n));
-    const int per = (n + kVictimThreads - 1) / kVictimThreads;
-    const int i0 = min(n, static_cast<int>(threadIdx.x) * per), i1 = min(n, i0 + per);
-    const int cnt = i1 - i0;
-    // slot of hand-relative position i0 + k (k < per <= n)
-    auto slot_k = [&](int k) {
-        int j = hand + i0 + k;
-        j -= j >= n ? n : 0;
-        j -= j >= n ? n : 0;
-        return j;
-    };
-    // 0: in use by this call, 1: cold (free or unreferenced), 2: warm (referenced)
-    auto class_of = [&](int32_t ep, int32_t pgid, int32_t ref) { return ep == epoch ? 0 : (pgid < 0 || ref == 0) ? 1 : 2; };
-    uint32_t cls = 0;                                // classes of positions k < kSlotItems, 2 bits each
-    {
-        int32_t ep[kSlotItems], sp[kSlotItems], rf[kSlotItems];
-#pragma unroll
-        for (int k = 0; k < kSlotItems; ++k) {       // every load in flight at once
-            const int j = slot_k(k);
-            const bool in = k < cnt;
-            ep[k] = in ? r.slot_epoch[j] : 0;
-            sp[k] = in ? r.slot_page[j] : 0;
-            rf[k] = in ? r.slot_ref[j] : 0;
-        }
-#pragma unroll
-        for (int k = 0; k < kSlotItems; ++k) cls |= static_cast<uint32_t>(class_of(ep[k], sp[k], rf[k])) << (2 * k);
-    }
-    auto class_at = [&](int k) {
-        if (k < kSlotItems) return static_cast<int>((cls >> (2 * k)) & 3u);
-        const int j = slot_k(k);
-        return class_of(r.slot_epoch[j], r.slot_page[j], r.slot_ref[j]);
-    };
-    unsigned long long mine = 0;                 // cold count | warm count << 32
-    for (int k = 0; k < cnt; ++k) {
-        const int c = class_at(k);
-        mine += c == 1 ? 1ull : (c == 2 ? (1ull << 32) : 0ull);
-    }
-    unsigned long long before = 0, total = 0;
-    Scan(scan_tmp).ExclusiveSum(mine, before, total);
-    const int64_t n_cold = static_cast<int64_t>(total & 0xffffffffull), n_warm = static_cast<int64_t>(total >> 32);
-    const int64_t placed = min(need, n_cold + n_warm);
-    // The sweep wraps once the cold slots run out: the hand has then passed --
-    // and cleared -- every warm slot, and takes warm slots on its second round.
-    const bool wraps = need > n_cold;
-    const int64_t warm_taken = wraps ? placed - n_cold : 0;
-    if (threadIdx.x == 0) s_stop = -1;
-    __syncthreads();
-    int64_t rc = static_cast<int64_t>(before & 0xffffffffull), rw = static_cast<int64_t>(before >> 32);
-    for (int k = 0; k < cnt; ++k) {
-        const int c = class_at(k);
-        const int j = slot_k(k);
-        if (c == 1) {
-            if (rc < need) {
-                r.victim[rc] = j;
-                if (rc == (wraps ? (warm_taken == 0 ? n_cold - 1 : -1) : need - 1)) s_stop = i0 + k;
-            }
-            ++rc;
-        } else if (c == 2) {
-            if (wraps) {
-                r.slot_ref[j] = 0;
-                if (rw < warm_taken) {
-                    r.victim[n_cold + rw] = j;
-                    if (rw == warm_taken - 1) s_stop = i0 + k;
-                }
-            }
-            ++rw;
-        }
-    }
-    __syncthreads();
-    const int stop = s_stop;
-    if (!wraps && stop >= 0) {
-        // one partial round: the warm slots before the stop lose their reference bit
-        for (int k = 0; k < min(cnt, stop - i0); ++k)
-            if (class_at(k) == 2) r.slot_ref[slot_k(k)] = 0;
-    }
-    __syncthreads();                                 // victim[] complete
-    // 3. placement: miss m < placed takes victim[m]; the rest go to the
-    //    overflow area (pool page n_slots + m - placed), for this call only.
-    //    Each thread places kPlaceBatch misses at a time, all their loads
-    //    issued before any store.
-    for (int64_t m0 = threadIdx.x; m0 < need; m0 += static_cast<int64_t>(kVictimThreads) * kPlaceBatch) {
-        int pg[kPlaceBatch], vj[kPlaceBatch], old[kPlaceBatch];
-#pragma unroll
-        for (int u = 0; u < kPlaceBatch; ++u) {
-            const int64_t m = m0 + static_cast<int64_t>(u) * kVictimThreads;
-            pg[u] = m < need ? r.miss_page[m] : -1;
-            vj[u] = m < placed ? r.victim[m] : -1;
-        }
-#pragma unroll
-        for (int u = 0; u < kPlaceBatch; ++u) old[u] = vj[u] >= 0 ? r.slot_page[vj[u]] : -1;
-#pragma unroll
-        for (int u = 0; u < kPlaceBatch; ++u) {
-            const int64_t m = m0 + static_cast<int64_t>(u) * kVictimThreads;
-            if (m >= need) continue;
-            if (vj[u] >= 0) {
-                const int j = vj[u];
-                if (old[u] >= 0) r.page_table[old[u]] = -1;   // a resident page no lookup of this call named
-                r.slot_page[j] = pg[u];
-                r.slot_ref[j] = 1;
-                r.slot_epoch[j] = epoch;
-                r.page_table[pg[u]] = j;
-                r.miss_dest[m] = j;
-            } else {
-                r.miss_dest[m] = static_cast<int32_t>(n + (m - placed));
-            }
-        }
-    }
-    if (threadIdx.x == 0) {
-        if (stop >= 0) r.ctl[1] = static_cast<uint64_t>((static_cast<int64_t>(hand) + stop + 1) % n);
-        r.ctl[0] = static_cast<uint64_t>(epoch);
-        r.ctl[2] += 1;
-        r.ctl[5] += static_cast<uint64_t>(need);
-        r.ctl[6] += static_cast<uint64_t>(need - placed);
-        r.ctl[7] = static_cast<uint64_t>(need);
-        r.ctl[8] = static_cast<uint64_t>(need - placed);
-        r.ctl[11] = static_cast<uint64_t>(placed);
-        r.ctl[12] = static_cast<uint64_t>(need);
-    }
+    victim_pass<kVictimThreads>(r, sel, n_look, n_sel, Hk);
 }
 
 // Fetch and ids pass, a persistent grid of one CTA per SM.
@@ -435,7 +236,8 @@ __global__ void __launch_bounds__(256) bcache_append_kernel(const float *__restr
 }
 
 __global__ void bcache_reset_kernel(int32_t *page_table, uint64_t *page_claim, int64_t n_pages, int32_t *slot_page,
-                                    int32_t *slot_epoch, int32_t *slot_ref, int n_slots, uint64_t *ctl)
+                                    int32_t *slot_epoch, int32_t *slot_ref, int n_slots, uint64_t *ctl,
+                                    int32_t *page_ready, int64_t n_pool)
 {
     const int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t st = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -443,6 +245,7 @@ __global__ void bcache_reset_kernel(int32_t *page_table, uint64_t *page_claim, i
         page_table[i] = -1;
         page_claim[i] = 0;
     }
+    for (int64_t i = i0; i < n_pool; i += st) page_ready[i] = 0;   // the stamps restart with the epochs
     for (int64_t i = i0; i < n_slots; i += st) {
         slot_page[i] = -1;
         slot_epoch[i] = 0;
@@ -564,6 +367,106 @@ static int bcache_resolve_launch(skv_bcache *c, const int32_t *sel, int32_t S, i
     return cuda_fail(h, cudaGetLastError(), "resolve launch");
 }
 
+// The cache's resolve state.
+static ResolveState resolve_state_of(const skv_bcache *c)
+{
+    ResolveState r;
+    r.page_table = c->page_table;
+    r.page_claim = c->page_claim;
+    r.page_miss = c->page_miss;
+    r.slot_page = c->slot_page;
+    r.slot_epoch = c->slot_epoch;
+    r.slot_ref = c->slot_ref;
+    r.victim = c->victim;
+    r.miss_page = c->miss_page;
+    r.miss_dest = c->miss_dest;
+    r.ctl = c->ctl;
+    r.n_slots = c->n_slots;
+    r.n_pages = c->n_blocks * c->Hk;
+    return r;
+}
+
+// After the fused attention: the misses the claim pass placed in slots are
+// moved from their overflow pages (that of each page's first lookup) into
+// their slots, and their lookups' page ids become the slots.
+__global__ void __launch_bounds__(256) bcache_place_kernel(ResolveState r, const int32_t *__restrict__ sel,
+                                                           int64_t n_look, int n_sel, int Hk, uint8_t *pool_k,
+                                                           uint8_t *pool_v, int64_t page_bytes,
+                                                           int32_t *__restrict__ ids)
+{
+    const int64_t placed = static_cast<int64_t>(r.ctl[11]);
+    const uint32_t epoch = static_cast<uint32_t>(r.ctl[0]);
+    const int64_t n16 = page_bytes / 16;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t m = warp; m < placed; m += n_warps) {
+        const int32_t p = r.miss_page[m];
+        const int64_t first = 0xffffffffll - static_cast<int64_t>(r.page_claim[p] & 0xffffffffull);
+        const int64_t src = (r.n_slots + first) * page_bytes, dst = static_cast<int64_t>(r.miss_dest[m]) * page_bytes;
+        const uint4 *sk = reinterpret_cast<const uint4 *>(pool_k + src);
+        const uint4 *sv = reinterpret_cast<const uint4 *>(pool_v + src);
+        uint4 *dk = reinterpret_cast<uint4 *>(pool_k + dst);
+        uint4 *dv = reinterpret_cast<uint4 *>(pool_v + dst);
+        for (int64_t i = lane; i < n16; i += 32) {
+            dk[i] = sk[i];
+            dv[i] = sv[i];
+        }
+    }
+    for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n_look;
+         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t p = lookup_page(sel, e, n_sel, Hk, r.n_pages);
+        if (p >= 0 && (r.page_claim[p] >> 32) == epoch && r.page_miss[p] < placed) ids[e] = r.miss_dest[r.page_miss[p]];
+    }
+}
+
+// Resolve and attention as one pass over the host link ("Strata compare", KV
+// streaming: resolve, copy, attend): the lookup pass, then the fused
+// attention (splitkv_decode_kernel with FUSE), which stages each missed page
+// from the host copy while one of its CTAs runs the claim / victim /
+// placement pass, then the move of the placed misses into their slots.
+// Taken for whole lists of kDecodeTile-row pages and one column group of
+// query rows per KV head; *taken says whether it was.  The pool page ids
+// recorded for the call are the slots of resident and placed pages and, for
+// the rest, the overflow page of each page's first lookup.
+static int bcache_attn_fused(skv_bcache *c, const skv_shape *shape, const void *q, const int32_t *sel, int32_t n_sel,
+                             float *o, float *lse, cudaStream_t st, bool *taken)
+{
+    *taken = false;
+    skv_handle *h = c->h;
+    if (c->ring_blocks > 0 || c->block_rows != kDecodeTile || !c->rstate || !c->page_ready) return SKV_OK;
+    if (shape->k_type != SKV_F16 || shape->v_type != SKV_F16 || shape->Hk <= 0 || shape->H % shape->Hk != 0 ||
+        shape->nq <= 0 || shape->nq * (shape->H / shape->Hk) > 8 || n_sel <= 0 || !q || !o || !lse)
+        return SKV_OK;
+    if (!sel || shape->S <= 0) return fail(h, SKV_EINVAL, "bad selection");
+    const int64_t n_look = static_cast<int64_t>(shape->S) * c->Hk * n_sel;
+    if (n_look > c->max_lookups)
+        return fail(h, SKV_EINVAL, "%lld lookups exceed max_lookups %lld", (long long)n_look,
+                    (long long)c->max_lookups);
+    *taken = true;
+    const ResolveState r = resolve_state_of(c);
+    const unsigned g_look = static_cast<unsigned>(std::min<int64_t>((n_look + 255) / 256, 4 * h->sm_count));
+    bcache_lookup_kernel<<<g_look, 256, 0, st>>>(r, sel, n_look, n_sel, c->Hk);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(h, e, "block-cache lookup");
+    DecodeArgs f;
+    memset(&f, 0, sizeof(f));
+    f.rstate = c->rstate;
+    f.sel = sel;
+    f.n_look = n_look;
+    f.page_ids_out = c->page_ids;
+    f.host_k = c->host_k;
+    f.host_v = c->host_v;
+    f.page_ready = c->page_ready;
+    f.epoch = c->ctl + kCtlEpochNow;
+    f.steal = reinterpret_cast<unsigned long long *>(c->ctl + kCtlSteal);
+    int rc = attn_paged_fused(h, shape, q, c->pool_k, c->pool_v, sel, n_sel, o, lse, st, f);
+    if (rc) return rc;
+    bcache_place_kernel<<<h->sm_count, 256, 0, st>>>(r, sel, n_look, n_sel, c->Hk, c->pool_k, c->pool_v,
+                                                     c->page_bytes, c->page_ids);
+    return cuda_fail(h, cudaGetLastError(), "block-cache placement");
+}
+
 }  // namespace skv
 
 using namespace skv;
@@ -587,6 +490,8 @@ int skv_bcache_destroy(skv_bcache *c)
     cudaFree(c->check);
     cudaFree(c->pool_k);
     cudaFree(c->pool_v);
+    cudaFree(c->rstate);
+    cudaFree(c->page_ready);
     delete c;
     return SKV_OK;
 }
@@ -601,7 +506,8 @@ int skv_bcache_reset(skv_bcache *c, void *stream)
                                                                             c->n_slots, c->ctl);
     else
         bcache_reset_kernel<<<256, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-            c->page_table, c->page_claim, n_pages, c->slot_page, c->slot_epoch, c->slot_ref, c->n_slots, c->ctl);
+            c->page_table, c->page_claim, n_pages, c->slot_page, c->slot_epoch, c->slot_ref, c->n_slots, c->ctl,
+            c->page_ready, static_cast<int64_t>(c->n_slots) + c->max_lookups);
     return cuda_fail(c->h, cudaGetLastError(), "block-cache reset");
 }
 
@@ -663,10 +569,23 @@ static int bcache_create_impl(skv_handle *h, int64_t n_blocks, int32_t block_row
     A(reinterpret_cast<void **>(&c->check), sizeof(int32_t));
     A(reinterpret_cast<void **>(&c->pool_k), pool_pages * c->page_bytes);
     A(reinterpret_cast<void **>(&c->pool_v), pool_pages * c->page_bytes);
+    if (ring_blocks == 0) {
+        A(&c->rstate, sizeof(ResolveState));
+        A(reinterpret_cast<void **>(&c->page_ready), sizeof(int32_t) * pool_pages);
+    }
     if (e != cudaSuccess) {
         cudaGetLastError();
         skv_bcache_destroy(c);
         return fail(h, SKV_ENOMEM, "block-cache allocation: %s", cudaGetErrorString(e));
+    }
+    if (c->rstate) {
+        const ResolveState r = resolve_state_of(c);
+        e = cudaMemcpy(c->rstate, &r, sizeof(r), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            skv_bcache_destroy(c);
+            return fail(h, SKV_ECUDA, "block-cache state: %s", cudaGetErrorString(e));
+        }
     }
     int rc = skv_bcache_reset(c, nullptr);
     if (rc == SKV_OK) rc = cuda_fail(h, cudaDeviceSynchronize(), "block-cache init");
@@ -780,7 +699,11 @@ extern "C" int skv_bcache_attn(skv_bcache *c, const skv_shape *shape, const void
     if (shape->Hk != c->Hk || shape->D != c->D)
         return skv::fail(c->h, SKV_EINVAL, "shape (Hk=%d, D=%d) does not match the cache (Hk=%d, D=%d)", shape->Hk,
                          shape->D, c->Hk, c->D);
-    int rc = skv_bcache_resolve(c, sel, shape->S, n_sel, c->page_ids, stream);
+    c->h->err[0] = 0;
+    bool taken = false;
+    int rc = skv::bcache_attn_fused(c, shape, q, sel, n_sel, o, lse, static_cast<cudaStream_t>(stream), &taken);
+    if (taken || rc) return rc;
+    rc = skv_bcache_resolve(c, sel, shape->S, n_sel, c->page_ids, stream);
     if (rc) return rc;
     return skv_attn_paged(c->h, shape, q, c->pool_k, c->pool_v, c->block_rows, c->page_ids, n_sel, o, lse, stream);
 }

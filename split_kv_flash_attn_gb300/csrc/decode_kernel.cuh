@@ -31,6 +31,9 @@
 // conversion kernel).
 #pragma once
 
+#include <algorithm>
+
+#include "bcache_resolve.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -159,8 +162,11 @@ __device__ __forceinline__ void convert_codes(const uint8_t *raw, __half *code, 
     }
 }
 
-template <int D, int KT, int VT>
-__global__ void __launch_bounds__(128) splitkv_decode_kernel(const DecodeArgs a)
+// One split of one unit: the CTA's whole job in an ordinary launch, one work
+// item of the fused block-cache instance (FUSE, below the kernel).
+template <int D, int KT, int VT, bool FUSE>
+__device__ __forceinline__ void decode_split(const DecodeArgs &a, const int cg, const int kh, const int split,
+                                             const int s, uint8_t *smem)
 {
     using C = DecodeCfg<D, KT, VT>;
     constexpr int kTile = C::kTile;
@@ -173,21 +179,17 @@ __global__ void __launch_bounds__(128) splitkv_decode_kernel(const DecodeArgs a)
     constexpr bool QV = Seg<VT, D>::quant;
     constexpr int NB = D / 32;   // 32-value blocks per head
 
-    extern __shared__ __align__(128) uint8_t smem[];
     int32_t *idx_s = reinterpret_cast<int32_t *>(smem + C::idx_off);
+    static_assert(!FUSE || (KT == SKV_F16 && VT == SKV_F16), "the fused instance reads fp16 pages");
+    constexpr int kPubTiles = FUSE ? kMaxListSplit / C::kTile : 1;
+    int32_t *src_s = idx_s + kMaxListSplit / 2;      // fused: each page's source (tables of at most 33 pages)
+    __shared__ int s_pub[kPubTiles];                 // fused: warps that have written tile t's rows to its pool page
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
 
     // ---- unit and split -------------------------------------------------
-    // Grid: x = (KV head, column group) fastest, y = split, z = sequence, so
-    // CTAs that run side by side read the other heads' segments of the same
-    // cache rows.
-    const int cg = blockIdx.x % a.n_cg;
-    const int kh = blockIdx.x / a.n_cg;
-    const int split = blockIdx.y;
-    const int s = blockIdx.z;
     const int unit = (s * a.Hk + kh) * a.n_cg + cg;
     const int64_t j_lo = a.key_lo + static_cast<int64_t>(split) * a.split_len;
     const int64_t j_hi = min(a.n_local, j_lo + a.split_len);
@@ -203,7 +205,37 @@ __global__ void __launch_bounds__(128) splitkv_decode_kernel(const DecodeArgs a)
     if (a.row_mode == ROWS_PAGED) {
         const int32_t *src = a.rows + list * a.rows_ld + page_lo;
         const int n = j_hi > j_lo ? static_cast<int>(((j_hi - 1) >> lg_pr) - page_lo + 1) : 0;
-        for (int i = tid; i < n; i += C::kThreads) cp_async4(smem_addr(idx_s + i), src + i, 4);
+        if constexpr (FUSE) {
+            // Each page's pool page and source, from the lookup pass's claims:
+            // a page this call missed is staged in the overflow page of its
+            // first lookup (n_slots + that lookup), read from the host by the
+            // first lookup and from the pool by later ones; any other page is
+            // resident at entry, and its table entry stays put for the call.
+            const ResolveState &r = *static_cast<const ResolveState *>(a.rstate);
+            const uint32_t ep = static_cast<uint32_t>(*a.epoch);
+            for (int i = tid; i < n; i += C::kThreads) {
+                const int64_t e = list * a.rows_ld + page_lo + i;
+                const int64_t blk = a.sel[e];
+                const int64_t p = blk * a.Hk + kh;
+                int32_t id = -1, from = -1;
+                if (blk >= 0 && p < r.n_pages) {
+                    const unsigned long long claim = r.page_claim[p];
+                    if ((claim >> 32) == ep) {
+                        const int64_t first = 0xffffffffll - static_cast<int64_t>(claim & 0xffffffffull);
+                        id = static_cast<int32_t>(r.n_slots + first);
+                        from = first == e ? static_cast<int32_t>(p) : -2;
+                    } else {
+                        id = r.page_table[p];
+                    }
+                }
+                idx_s[i] = id;
+                src_s[i] = from;
+                a.page_ids_out[e] = id;
+            }
+            for (int i = tid; i < kPubTiles; i += C::kThreads) s_pub[i] = 0;
+        } else {
+            for (int i = tid; i < n; i += C::kThreads) cp_async4(smem_addr(idx_s + i), src + i, 4);
+        }
         cp_async_commit();
         cp_async_wait<0>();
         __syncthreads();
@@ -235,6 +267,29 @@ __global__ void __launch_bounds__(128) splitkv_decode_kernel(const DecodeArgs a)
     const int64_t stride_k = paged ? SEGK : a.k_row_bytes;
     const int64_t stride_v = paged ? SEGV : a.v_row_bytes;
 
+    // Fused: wait (bounded) until pool page pg carries this call's stamp.
+    const int epoch = FUSE ? static_cast<int>(*a.epoch) : 0;
+    auto wait_published = [&](int32_t pg) {
+        if (lane == 0) {
+            uint64_t t0 = 0;
+            for (uint32_t it = 0;; ++it) {
+                int v;
+                asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a.page_ready + pg) : "memory");
+                if (v == epoch) break;
+                if ((it & 63) == 0) {
+                    uint64_t t;
+                    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+                    if (it == 0) t0 = t;
+                    else if (t - t0 > 2000000000ull) {
+                        atomicOr(a.status, 1);
+                        break;
+                    }
+                }
+                __nanosleep(128);
+            }
+        }
+        __syncwarp();
+    };
     // Stage this warp's 16 keys of tile t into stage st.
     auto load_tile = [&](int t, int st) {
         uint8_t *sk_ = smem + st * C::stage_bytes;
@@ -246,14 +301,37 @@ __global__ void __launch_bounds__(128) splitkv_decode_kernel(const DecodeArgs a)
             constexpr int RPW = 32 / CPR;
             const int ch = lane % CPR;
             const uint32_t dk = smem_addr(sk_), dv = smem_addr(sv_);
+            // fused: tile t is page t of the split; a host source moves the
+            // rows from pool page pg to host page sr
+            const uint8_t *kb = a.k, *vb = a.v;
+            int64_t shift = 0;
+            if constexpr (FUSE) {
+                const int32_t sr = src_s[t], pg = idx_s[t];
+                if (pg >= 0 && sr >= 0) {
+                    kb = a.host_k;
+                    vb = a.host_v;
+                    shift = static_cast<int64_t>(sr - pg) << lg_pr;
+                } else if (pg >= 0 && sr == -2) {
+                    wait_published(pg);
+                }
+            }
 #pragma unroll
             for (int it = 0; it < 16 / RPW; ++it) {
                 const int rr = lane / CPR + RPW * it;
                 const int r = wrow + rr;
-                const int64_t row = key_row(t, rr);
-                const bool ok = row >= 0;
-                const uint8_t *src_k = a.k + (ok ? row * stride_k + head_k + ch * 16 : 0);
-                const uint8_t *src_v = a.v + (ok ? row * stride_v + head_v + ch * 16 : 0);
+                const uint8_t *src_k, *src_v;
+                bool ok;
+                if constexpr (FUSE) {
+                    const int64_t row = key_row(t, rr) + shift;
+                    ok = row >= shift;
+                    src_k = kb + (ok ? row * stride_k + head_k + ch * 16 : 0);
+                    src_v = vb + (ok ? row * stride_v + head_v + ch * 16 : 0);
+                } else {                                 // the same with no shift, written out: cheaper code
+                    const int64_t row = key_row(t, rr);
+                    ok = row >= 0;
+                    src_k = a.k + (ok ? row * stride_k + head_k + ch * 16 : 0);
+                    src_v = a.v + (ok ? row * stride_v + head_v + ch * 16 : 0);
+                }
                 cp_async16(dk + swz<D>(r, ch), src_k, ok ? 16 : 0);
                 cp_async16(dv + swz<D>(r, ch), src_v, ok ? 16 : 0);
             }
@@ -360,6 +438,32 @@ __global__ void __launch_bounds__(128) splitkv_decode_kernel(const DecodeArgs a)
     for (int i = 0; i < n_tiles; ++i) {
         cp_async_wait<STAGES - 2>();
         __syncwarp();
+        if constexpr (FUSE) {
+            // tile i = page i: a page read from the host is written to its
+            // pool page (this warp's 16 rows), then published by the last warp
+            const int32_t sr = src_s[i], pg = idx_s[i];
+            if (sr >= 0 && pg >= 0) {
+                const uint8_t *skp = smem + (i % STAGES) * C::stage_bytes;
+                const uint8_t *svp = skp + C::stage_k;
+                uint8_t *dk = const_cast<uint8_t *>(a.k) + (static_cast<int64_t>(pg) << lg_pr) * stride_k;
+                uint8_t *dv = const_cast<uint8_t *>(a.v) + (static_cast<int64_t>(pg) << lg_pr) * stride_v;
+                constexpr int CPR = D / 8;
+#pragma unroll 4
+                for (int c = lane; c < 16 * CPR; c += 32) {
+                    const int r = wrow + c / CPR, ch = c % CPR;
+                    *reinterpret_cast<uint4 *>(dk + r * stride_k + ch * 16) =
+                        *reinterpret_cast<const uint4 *>(skp + swz<D>(r, ch));
+                    *reinterpret_cast<uint4 *>(dv + r * stride_v + ch * 16) =
+                        *reinterpret_cast<const uint4 *>(svp + swz<D>(r, ch));
+                }
+                __threadfence();
+                __syncwarp();
+                if (lane == 0 && atomicAdd(&s_pub[i], 1) == C::kWarps - 1) {
+                    __threadfence();
+                    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(a.page_ready + pg), "r"(epoch) : "memory");
+                }
+            }
+        }
         {
             const int nt = i + STAGES - 1;
             if (nt < n_tiles) load_tile(nt, nt % STAGES);
@@ -643,11 +747,59 @@ __global__ void __launch_bounds__(128) splitkv_decode_kernel(const DecodeArgs a)
     if (tid == 0) a.counters[unit] = 0;              // ready for the next launch
 }
 
+// An ordinary launch: one CTA per (unit, split) -- grid x = (KV head, column
+// group) fastest, y = split, z = sequence, so CTAs that run side by side read
+// the other heads' segments of the same cache rows.
+//
+// FUSE: the block-cache attention that also fetches (fp16 pages of kTile
+// rows, whole lists, one column group), launched right after the lookup pass.
+// CTA 0 first runs the claim / victim / placement pass (NT = 128), which only
+// decides where the missed pages will live; the pages themselves are staged
+// meanwhile.  A persistent grid takes (unit, split) work items from a counter
+// in lookup order (sequence, KV head, split).  A page this call missed is read
+// from the host copy by its first lookup and, once the CTA's four warps have
+// it in shared memory, written to the overflow page of that lookup and
+// published (its stamp set to this call's epoch); a later lookup of the page
+// reads it there once published -- its publisher's item was taken earlier and
+// waits only for items taken before it, so every wait ends (and each is
+// bounded).  Resident pages are read from their slots.  Pages and arithmetic
+// are those of an ordinary launch with the same splits over the pool.
+template <int D, int KT, int VT, bool FUSE = false>
+__global__ void __launch_bounds__(128) splitkv_decode_kernel(const DecodeArgs a)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    if constexpr (!FUSE) {
+        decode_split<D, KT, VT, false>(a, blockIdx.x % a.n_cg, blockIdx.x / a.n_cg, blockIdx.y, blockIdx.z, smem);
+    } else {
+        __shared__ unsigned long long s_item;
+        const unsigned long long items =
+            static_cast<unsigned long long>(a.S) * a.Hk * a.n_cg * static_cast<unsigned long long>(a.n_splits);
+        if (blockIdx.x == 0) {
+            victim_pass<DecodeCfg<D, KT, VT>::kThreads>(*static_cast<const ResolveState *>(a.rstate), a.sel, a.n_look,
+                                     static_cast<int>(a.rows_ld), a.Hk);
+            __syncthreads();
+        }
+        for (;;) {
+            if (threadIdx.x == 0) s_item = atomicAdd(a.steal, 1ull);
+            __syncthreads();
+            const unsigned long long w = s_item;
+            __syncthreads();                         // s_item is read before it is taken again
+            if (w >= items) break;
+            const int split = static_cast<int>(w % a.n_splits);
+            const unsigned long long u = w / a.n_splits;   // (s * Hk + kh) * n_cg + cg
+            decode_split<D, KT, VT, true>(a, static_cast<int>(u % a.n_cg), static_cast<int>((u / a.n_cg) % a.Hk),
+                                          split, static_cast<int>(u / (static_cast<unsigned long long>(a.n_cg) * a.Hk)),
+                                          smem);
+            __syncthreads();                         // shared memory is reused by the next item
+        }
+    }
+}
+
 namespace {
 // One cache per instance and translation unit (internal linkage: a static in
 // an external template would be merged across every copy of the library a
 // process loads).
-template <int D, int KT, int VT>
+template <int D, int KT, int VT, bool FUSE = false>
 KernelAttrCache &decode_attr_cache()
 {
     static KernelAttrCache c;
@@ -669,6 +821,28 @@ int launch_decode_t(skv_handle *h, const DecodeArgs &a, cudaStream_t st)
     dim3 grid(static_cast<unsigned>(a.Hk * a.n_cg), static_cast<unsigned>(a.n_splits), static_cast<unsigned>(a.S));
     splitkv_decode_kernel<D, KT, VT><<<grid, C::kThreads, C::smem, st>>>(a);
     return cuda_fail(h, cudaGetLastError(), "decode kernel launch");
+}
+
+// The fused block-cache instance: a persistent grid of at most the CTAs
+// resident at once, launched cooperatively since its CTAs wait for pages
+// others publish.
+template <int D>
+int launch_decode_fused_t(skv_handle *h, const DecodeArgs &a, cudaStream_t st)
+{
+    using C = DecodeCfg<D, SKV_F16, SKV_F16>;
+    const void *fn = reinterpret_cast<const void *>(splitkv_decode_kernel<D, SKV_F16, SKV_F16, true>);
+    int per_sm = 0;
+    cudaError_t e = kernel_smem_optin(decode_attr_cache<D, SKV_F16, SKV_F16, true>(), fn, C::smem, C::kThreads, &per_sm);
+    if (e != cudaSuccess) return cuda_fail(h, e, "cudaFuncSetAttribute(fused decode)");
+    if (per_sm <= 0) return fail(h, SKV_EUNSUPPORTED, "the fused decode kernel cannot be resident");
+    const int64_t items = static_cast<int64_t>(a.S) * a.Hk * a.n_cg * a.n_splits;
+    const int64_t ctas = std::min<int64_t>(items, static_cast<int64_t>(per_sm) * h->sm_count);
+    if (ctas <= 0) return SKV_OK;
+    DecodeArgs arg = a;
+    void *args[] = {&arg};
+    e = cudaLaunchCooperativeKernel(fn, dim3(static_cast<unsigned>(ctas)), dim3(C::kThreads), args,
+                                    static_cast<size_t>(C::smem), st);
+    return cuda_fail(h, e, "fused decode launch");
 }
 
 template <int D, int KT, int VT>

@@ -99,6 +99,21 @@ struct DecodeArgs {
     float *lse_out;             // [R]
     int64_t R;                  // S*nq*H
     int *status;                // device status word (kernels with bounded waits)
+    // The fused block-cache instance (paged mode, pages of kDecodeTile rows):
+    // the cache's resolve state (device memory), the call's selection
+    // [S][Hk][rows_ld] of block ids and its lookup count, where every lookup's
+    // pool page is recorded, the device-mapped host copy in the pool's page
+    // layout, the pool pages' publication stamps, this call's epoch and the
+    // counter the work items are taken from (zero before the launch).
+    const void *rstate;
+    const int32_t *sel;
+    int64_t n_look;
+    int32_t *page_ids_out;
+    const uint8_t *host_k;
+    const uint8_t *host_v;
+    int32_t *page_ready;
+    const uint64_t *epoch;
+    unsigned long long *steal;
 };
 
 // Splits of one launch merged by the last-arriving CTA of each unit are
@@ -110,6 +125,9 @@ constexpr int kMaxUnits = 65536;
 // Launch the split-KV decode kernel (one CTA per (split, unit)).
 int launch_decode(skv_handle *h, const DecodeArgs &a, int k_type, int v_type, int D, cudaStream_t st);
 int launch_decode_f16(skv_handle *h, const DecodeArgs &a, int D, cudaStream_t st);
+// The fused block-cache instance (fp16 pages, a.page_src set): a persistent
+// cooperative grid of at most the CTAs resident at once.
+int launch_decode_fused(skv_handle *h, const DecodeArgs &a, int D, cudaStream_t st);
 int launch_decode_quant(skv_handle *h, const DecodeArgs &a, int k_type, int v_type, int D, cudaStream_t st);
 // CTAs of the decode kernel resident per SM for this type/D pairing (0 if unsupported).
 int decode_ctas_per_sm(skv_handle *h, int k_type, int v_type, int D);
@@ -170,6 +188,14 @@ int plan_splits_cost(int64_t n_keys, int64_t n_units, int sm_count, int ctas_per
 int attn_paged_range(skv_handle *h, const skv_shape *shape, const void *q, const void *k_pages, const void *v_pages,
                      int32_t page_rows, const int32_t *page_ids, int32_t pages_per_list, int64_t key_lo,
                      int64_t key_hi, float *o, float *lse, cudaStream_t st);
+// Pages per split of the fused block-cache attention (its work items).
+constexpr int kFusedSplitPages = 8;
+// The fused block-cache attention over whole lists of kDecodeTile-row pages
+// (`fuse` carries rstate .. steal).  SKV_EUNSUPPORTED for a shape it does
+// not take (more than one column group of query rows per KV head).
+int attn_paged_fused(skv_handle *h, const skv_shape *shape, const void *q, const void *k_pages, const void *v_pages,
+                     const int32_t *page_ids, int32_t pages_per_list, float *o, float *lse, cudaStream_t st,
+                     const DecodeArgs &fuse);
 
 int launch_dequant(int type, const void *blocks, int64_t n_values, float *out, cudaStream_t st);
 int launch_gather(const void *src, int64_t row_bytes, const int32_t *rows, int64_t n, void *dst,

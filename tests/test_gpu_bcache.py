@@ -1,12 +1,16 @@
 """Block cache (selection-driven residency over a pinned paged host copy).
 
 Parity is against the oracle over the selected rows, and bitwise against the
-same paged attention with the whole cache resident on the device (identity
-page table), the check the Strata KV-streaming parity test makes.  After every
-resolve the page table and the slot map must be inverse maps, and the counters
-must add up.  The residency decisions themselves (the slot of every page, the
-overflow, the hand) are compared call by call with a plain sequential CLOCK
-model of the page's resolve rules (oracle/bcache_model.py)."""
+same call with every page resident, the check the Strata KV-streaming parity
+test makes: a second cache that holds all pages, called twice with the
+selection so that the second call reads every page from its pool.  The
+resolve-then-attend path (skv_bcache_resolve, then skv_attn_paged through the
+pool) is checked bitwise against skv_attn_paged over the whole cache on the
+device (identity page table).  After every resolve the page table and the
+slot map must be inverse maps, and the counters must add up.  The residency
+decisions themselves (the slot of every page, the overflow, the hand) are
+compared call by call with a plain sequential CLOCK model of the page's
+resolve rules (oracle/bcache_model.py)."""
 import math
 
 import numpy as np
@@ -33,11 +37,39 @@ def h(skv):
     return skv.Handle(0)
 
 
-def _resident(skv, h, c, w, q_d, sel, k_full, v_full):
-    """The same paged attention with every page resident on the device
-    (identity page table: page id = block * Hk + head)."""
+class AllResident:
+    """The same block-cache call with every page resident: a cache with a slot
+    for every page, called twice with the selection (the first call fetches
+    what is not resident yet, the second reads every page from the pool)."""
+
+    def __init__(self, skv, h, w, hk, hv, max_lookups):
+        self.c = skv.BlockCache(h, hk, hv, n_blocks=w.extra["n_blocks"], block_rows=w.extra["block_rows"], Hk=w.Hk,
+                                D=w.D, n_slots=w.extra["n_blocks"] * w.Hk, max_lookups=max_lookups)
+
+    def __call__(self, q_d, sel):
+        self.c.attn(q_d, dev(sel))
+        o, l = self.c.attn(q_d, dev(sel))
+        assert self.c.stats()["last_misses"] == 0
+        return o, l
+
+    def close(self):
+        self.c.close()
+
+
+def _identity(skv, h, w, q_d, sel, k_full, v_full):
+    """skv_attn_paged with every page resident on the device (identity page
+    table: page id = block * Hk + head)."""
     ids = (sel * w.Hk + np.arange(w.Hk, dtype=np.int32)[None, :, None]).astype(np.int32)
     return skv.attn_paged(h, q_d, k_full, v_full, dev(ids), Hk=w.Hk, page_rows=w.extra["block_rows"])
+
+
+def _resolved(skv, h, c, w, q_d, sel):
+    """skv_bcache_resolve, then skv_attn_paged through the cache's pool."""
+    import torch
+    ids = torch.empty(sel.shape, dtype=torch.int32, device="cuda")
+    c.resolve(dev(sel), ids)
+    k_pool, v_pool, _, _ = c.pool()
+    return skv.attn_paged(h, q_d, k_pool, v_pool, ids, Hk=w.Hk, page_rows=w.extra["block_rows"])
 
 
 def _oracle(oracle_mod, w, sel):
@@ -58,15 +90,15 @@ def test_block_cache_cold_warm_drift(skv, h, oracle_mod, n_slots):
     c = skv.BlockCache(h, hk, hv, n_blocks=n_blocks, block_rows=64, Hk=w.Hk, D=w.D, n_slots=n_slots,
                        max_lookups=w.S * w.Hk * sel.shape[-1])
     q_d = dev(w.q)
-    k_full, v_full = dev(w.k), dev(w.v)
     vmax = float(np.abs(w.v.view(np.float16)).max())
     lookups = w.S * w.Hk * sel.shape[-1]
     distinct = len({(int(b), k) for s in range(w.S) for k in range(w.Hk) for b in sel[s, k]})
+    resident = AllResident(skv, h, w, hk, hv, lookups)
 
     o0, l0 = c.attn(q_d, dev(sel))                            # cold
     want_o, want_l = _oracle(oracle_mod, w, sel)
     check_attention(o0, l0, want_o, want_l, vmax, "cold")
-    r_o, r_l = _resident(skv, h, c, w, q_d, sel, k_full, v_full)
+    r_o, r_l = resident(q_d, sel)
     assert torch.equal(o0, r_o) and torch.equal(l0, r_l), "cold call differs from the all-resident run"
     assert c.check() == 0
     st = c.stats()
@@ -74,7 +106,7 @@ def test_block_cache_cold_warm_drift(skv, h, oracle_mod, n_slots):
     assert st["misses"] == distinct and st["overflow"] == max(0, distinct - n_slots)
 
     o1, l1 = c.attn(q_d, dev(sel))                            # warm, same selection
-    r_o, r_l = _resident(skv, h, c, w, q_d, sel, k_full, v_full)
+    r_o, r_l = resident(q_d, sel)
     assert torch.equal(o1, r_o) and torch.equal(l1, r_l), "warm call differs from the all-resident run"
     check_attention(o1, l1, want_o, want_l, vmax, "warm")
     assert c.check() == 0
@@ -92,7 +124,7 @@ def test_block_cache_cold_warm_drift(skv, h, oracle_mod, n_slots):
     for step in range(3):                                     # drift: 10% of the blocks redrawn per step
         cur = wl.redraw_selection(cur, n_blocks, 0.1, rng)
         o2, l2 = c.attn(q_d, dev(cur))
-        r_o, r_l = _resident(skv, h, c, w, q_d, cur, k_full, v_full)
+        r_o, r_l = resident(q_d, cur)
         assert torch.equal(o2, r_o) and torch.equal(l2, r_l), f"drift step {step}"
         assert c.check() == 0
     want_o, want_l = _oracle(oracle_mod, w, cur)
@@ -103,6 +135,16 @@ def test_block_cache_cold_warm_drift(skv, h, oracle_mod, n_slots):
     assert torch.equal(o3, o0) and torch.equal(l3, l0)
     st3 = c.stats()
     assert st3["calls"] == 1 and st3["hits"] == 0
+
+    # resolve, then paged attention through the pool (the path for shapes the
+    # call does not fuse): bitwise the same as over the whole cache on the device
+    k_full, v_full = dev(w.k), dev(w.v)
+    for sl in (sel, cur):
+        p_o, p_l = _resolved(skv, h, c, w, q_d, sl)
+        i_o, i_l = _identity(skv, h, w, q_d, sl, k_full, v_full)
+        assert torch.equal(p_o, i_o) and torch.equal(p_l, i_l), "resolve + paged attention differs"
+    assert c.check() == 0
+    resident.close()
     c.close()
 
 

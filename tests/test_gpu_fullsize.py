@@ -44,12 +44,13 @@ def test_block_sparse_full_size(skv, oracle_mod):
     """4 sequences x 4 KV heads x 512 of 4096 64-row blocks from a pinned
     paged cache of 262144 rows through a 2048-page block cache (demand above
     capacity): every output row against the oracle, cold and warm, and bit
-    for bit against the same paged attention with the whole cache resident."""
+    for bit against the same call with every page resident."""
     import torch
     w = wl.block_sparse_decode()
     sel = w.extra["sel"]
     h = skv.Handle(0)
-    c = skv.BlockCache(h, pinned(w.k), pinned(w.v), n_blocks=w.extra["n_blocks"], block_rows=64, Hk=w.Hk, D=w.D,
+    hk, hv = pinned(w.k), pinned(w.v)
+    c = skv.BlockCache(h, hk, hv, n_blocks=w.extra["n_blocks"], block_rows=64, Hk=w.Hk, D=w.D,
                        n_slots=w.extra["cache_pages"], max_lookups=sel.size)
     q = dev(w.q)
     o, l = c.attn(q, dev(sel))
@@ -59,12 +60,13 @@ def test_block_sparse_full_size(skv, oracle_mod):
                                           n_rows0=w.extra["n_kv"], layout=oracle_mod.PAGED, page_rows=br,
                                           n_keys=rows.shape[-1], kv_rows=rows, rows_per_head=True)
     check_attention(o, l, want_o, want_l, float(np.abs(w.v.view(np.float16)).max()), "block sparse full")
-    from tests.test_gpu_bcache import _resident
-    r_o, r_l = _resident(skv, h, c, w, q, sel, dev(w.k), dev(w.v))
+    from tests.test_gpu_bcache import AllResident
+    resident = AllResident(skv, h, w, hk, hv, sel.size)
+    r_o, r_l = resident(q, sel)
     assert torch.equal(o, r_o) and torch.equal(l, r_l)
     o2, l2 = c.attn(q, dev(sel))                       # warm call: hits and misses mixed
-    r_o, r_l = _resident(skv, h, c, w, q, sel, dev(w.k), dev(w.v))
     assert torch.equal(o2, r_o) and torch.equal(l2, r_l)
+    resident.close()
     check_attention(o2, l2, want_o, want_l, float(np.abs(w.v.view(np.float16)).max()), "block sparse warm")
     st = c.stats()
     assert st["last_misses"] > 0 and st["last_overflow"] > 0 and st["hits"] > 0
