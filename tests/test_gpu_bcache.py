@@ -74,7 +74,8 @@ def _resolved(skv, h, c, w, q_d, sel):
 
 def _oracle(oracle_mod, w, sel):
     br = w.extra["block_rows"]
-    rows = (sel[..., None] * br + np.arange(br, dtype=np.int32)).reshape(sel.shape[0], sel.shape[1], -1)
+    rows = np.where(sel[..., None] >= 0, sel[..., None] * br + np.arange(br, dtype=np.int32), -1)
+    rows = rows.reshape(sel.shape[0], sel.shape[1], -1)
     return oracle_mod.attention(w.q, D=w.D, H=w.H, Hk=w.Hk, scale=w.scale, k0=w.k, v0=w.v,
                                 n_rows0=w.extra["n_kv"], layout=oracle_mod.PAGED, page_rows=br,
                                 n_keys=rows.shape[-1], kv_rows=rows.astype(np.int32), rows_per_head=True)
@@ -144,6 +145,43 @@ def test_block_cache_cold_warm_drift(skv, h, oracle_mod, n_slots):
         i_o, i_l = _identity(skv, h, w, q_d, sl, k_full, v_full)
         assert torch.equal(p_o, i_o) and torch.equal(p_l, i_l), "resolve + paged attention differs"
     assert c.check() == 0
+    resident.close()
+    c.close()
+
+
+@pytest.mark.parametrize("n_slots", [40, 4096])
+def test_block_cache_repeats_and_absent_blocks(skv, h, oracle_mod, n_slots):
+    """Selections that name a block twice in one list (a later lookup of a
+    page the same work item fetches), name the same blocks in every list, and
+    hold absent entries (-1, and ids past the cache): against the oracle, and
+    bit for bit against the same call with every page resident, cold and
+    warm; 40 slots overflow, 4096 hold everything."""
+    import torch
+    w = wl.block_sparse_decode(n_kv=64 * 256, S=3, H=16, Hk=2, D=128, n_sel=40, cache_pages=n_slots)
+    n_blocks = w.extra["n_blocks"]
+    sel = w.extra["sel"].copy()
+    sel[0, 0, 3] = sel[0, 0, 1]                 # same work item (8 pages a work item)
+    sel[0, 1, 30] = sel[0, 1, 2]                # a later work item of the same list
+    sel[1, 0, :10] = sel[0, 0, :10]             # the first lookups are in list (0, 0)
+    sel[2, 1, 5] = -1
+    sel[2, 1, 17] = n_blocks + 3                # past the cache: absent
+    sel[1, 1, 39] = -1
+    hk, hv = pinned(w.k), pinned(w.v)
+    lookups = w.S * w.Hk * sel.shape[-1]
+    c = skv.BlockCache(h, hk, hv, n_blocks=n_blocks, block_rows=64, Hk=w.Hk, D=w.D, n_slots=n_slots,
+                       max_lookups=lookups)
+    resident = AllResident(skv, h, w, hk, hv, lookups)
+    q_d = dev(w.q)
+    vmax = float(np.abs(w.v.view(np.float16)).max())
+    want_o, want_l = _oracle(oracle_mod, w, np.where(sel < n_blocks, sel, -1))
+    r_o, r_l = resident(q_d, sel)
+    for what in ("cold", "warm"):
+        o, l = c.attn(q_d, dev(sel))
+        torch.cuda.synchronize()
+        assert h.status() == 0
+        check_attention(o, l, want_o, want_l, vmax, what)
+        assert torch.equal(o, r_o) and torch.equal(l, r_l), f"{what} call differs from the all-resident run"
+        assert c.check() == 0
     resident.close()
     c.close()
 
