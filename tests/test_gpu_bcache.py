@@ -149,15 +149,15 @@ def test_block_cache_cold_warm_drift(skv, h, oracle_mod, n_slots):
     c.close()
 
 
-@pytest.mark.parametrize("n_slots", [40, 4096])
-def test_block_cache_repeats_and_absent_blocks(skv, h, oracle_mod, n_slots):
+@pytest.mark.parametrize("n_slots,D", [(40, 128), (4096, 128), (40, 64)])
+def test_block_cache_repeats_and_absent_blocks(skv, h, oracle_mod, n_slots, D):
     """Selections that name a block twice in one list (a later lookup of a
     page the same work item fetches), name the same blocks in every list, and
     hold absent entries (-1, and ids past the cache): against the oracle, and
     bit for bit against the same call with every page resident, cold and
-    warm; 40 slots overflow, 4096 hold everything."""
+    warm; 40 slots overflow, 4096 hold everything; head dims 128 and 64."""
     import torch
-    w = wl.block_sparse_decode(n_kv=64 * 256, S=3, H=16, Hk=2, D=128, n_sel=40, cache_pages=n_slots)
+    w = wl.block_sparse_decode(n_kv=64 * 256, S=3, H=16, Hk=2, D=D, n_sel=40, cache_pages=n_slots)
     n_blocks = w.extra["n_blocks"]
     sel = w.extra["sel"].copy()
     sel[0, 0, 3] = sel[0, 0, 1]                 # same work item (8 pages a work item)
