@@ -421,7 +421,7 @@ int skv_attn_partial(skv_handle *h, const skv_shape *shape, const void *q, const
         const int64_t units_p = static_cast<int64_t>(shape->S) * prefill_units(shape);
         int64_t split_len = 0;
         int32_t n_splits = 0;
-        if ((rc = plan_splits_cost(n_local, units_p, h->sm_count, 1, kPrefillTile, 0, kPrefillOverheadTiles,
+        if ((rc = plan_splits_cost(n_local, units_p, h->sm_count, 1, kPrefillTile, 0, prefill_overhead_tiles(shape),
                                    &split_len, &n_splits)))
             return fail(h, rc, "split planning failed");
         if (units_p > kMaxUnits) return fail(h, SKV_EUNSUPPORTED, "too many query tiles");
@@ -565,7 +565,7 @@ int skv_attn_window_tail(skv_handle *h, const skv_shape *shape, const void *q, c
 
     int64_t w_len = 0, t_len = 0;
     int32_t w_splits = 0, t_splits = 0;
-    const int overhead = use_tc ? kPrefillOverheadTiles : 1;
+    const int overhead = use_tc ? prefill_overhead_tiles(shape) : 1;
     if ((rc = plan_splits_cost(n_win, units, h->sm_count, ctas, tile, 0, overhead, &w_len, &w_splits)))
         return fail(h, rc, "split planning failed");
     const int64_t n_tt = n_tail > 0 ? (n_tail + tile_rows - 1) / tile_rows : 0;

@@ -177,8 +177,13 @@ int prefill_units(const skv_shape *sh);    // (KV head, 128-row query tile) pair
 int launch_prefill(skv_handle *h, const PrefillLaunch &L, cudaStream_t st);
 constexpr int kPrefillTile = 128;
 // Per-CTA fixed cost of the prefill kernel in 128-key tiles (TMEM allocation,
-// barrier set-up, Q staging, pipeline fill, epilogue and split merge).
-constexpr int kPrefillOverheadTiles = 6;
+// barrier set-up, Q staging, pipeline fill, epilogue and split merge): about
+// 11 us, which is ~9 fp16 tiles (1.2-1.4 us each) but only ~4 tiles of
+// q8_0 / q4_0 rows (2.6 us each, the producers decode the codes).  Fitted to
+// 128 query tiles over 32768 keys on 152 SMs, where one split per tile beat
+// seven (312 against 331 us over fp16 rows, 363 against 397 us over fp16 row
+// lists) and seven beat one over q8_0 / q4_0 rows (667 against 710 us).
+inline int prefill_overhead_tiles(const skv_shape *sh) { return sh->k_type == SKV_F16 ? 10 : 4; }
 
 int plan_splits_cost(int64_t n_keys, int64_t n_units, int sm_count, int ctas_per_sm, int tile, int64_t max_split,
                      int overhead_tiles, int64_t *split_len, int32_t *n_splits);
