@@ -611,6 +611,9 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
             tc::tc_fence_after();
             int last_bar = -1;                      // barrier and phase of the last commit
             uint32_t last_par = 0;
+            // operand descriptors of the first K and V slots; the rest are offsets
+            const uint64_t dk0 = tc::smem_desc(sbase + kOffK, 16, 1024);
+            const uint64_t dv0 = tc::smem_desc(sbase + kOffV, kHalfTile, 1024);
             for (int jj = 0; ok && jj <= n_tiles; ++jj) {
                 if (jj < n_tiles) {
                     const int b = jj & 1;
@@ -625,8 +628,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                     for (int ks = 0; ks < KSTEPS; ++ks) {
                         const int kk = ks % (kPD / 16);
                         const uint32_t off = (kk >> 2) * kHalfTile + (kk & 3) * 32;
-                        const uint64_t bd = tc::smem_desc(
-                            sbase + kOffK + (KLO ? (ks / (kPD / 16)) : b) * kTileBytes + off, 16, 1024);
+                        const uint64_t bd = tc::desc_add(dk0, (KLO ? (ks / (kPD / 16)) : b) * kTileBytes + off);
                         tc::mma_f16_ts(d_s, tmem + static_cast<uint32_t>(kQCol + kk * 8), bd, kIdescS, ks > 0);
                     }
                     tc::mma_commit(bar(B_SFULL + sb));
@@ -648,7 +650,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                         // V tile as B in MN-major layout: 16 keys = 2048 bytes per k-step;
                         // the second 64-wide d block is kHalfTile away (leading offset),
                         // 8-key row groups are 1024 bytes apart (stride offset).
-                        const uint64_t bd = tc::smem_desc(sbase + kOffV + b * kTileBytes + kk * 2048, kHalfTile, 1024);
+                        const uint64_t bd = tc::desc_add(dv0, b * kTileBytes + kk * 2048);
                         tc::mma_f16_ts(d_o, a_t, bd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
                     }
                     tc::mma_commit(bar(B_VEMPTY + b));

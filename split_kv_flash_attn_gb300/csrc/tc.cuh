@@ -185,6 +185,11 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo_bytes,
     return d;
 }
 
+// The descriptor of the same layout `bytes` further on in shared memory: the
+// start address is held in 16-byte units in the low 14 bits, which shared
+// addresses below 256 KiB never carry out of.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+
 // Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1), fp16
 // A and B (bits 7-9, 10-12 = 0), A K-major (bit 15 = 0), B K-major or
 // MN-major (bit 16), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
