@@ -18,7 +18,12 @@
 //                   are staged in shared memory by cp.async one tile ahead,
 //                   then decoded to fp16(d*q) and stored in the same
 //                   layout.
-//   MMA warp      : S_j = Q K_j^T        tcgen05.mma kind::f16, M=N=128, into
+//   MMA issue     : MODE 0, one thread issues the S MMAs and a thread of
+//                   another warp the PV MMAs (a thread's issue of eight MMAs
+//                   takes about as long as the tensor core runs them, so one
+//                   thread for both put them in series); MODE 1 and 2, one
+//                   thread issues both:
+//                   S_j = Q K_j^T        tcgen05.mma kind::f16, M=N=128, into
 //                                        one of two TMEM S buffers (fp32); Q
 //                                        is the A operand in tensor memory
 //                                        (placed there once by the softmax
@@ -94,8 +99,8 @@ constexpr int kPubAfter = 16;
 // quantised rows converted by software, MODE 2: fp16 row lists by cp.async).
 template <int MODE>
 struct Cfg {
-    // MODE 0: 11 warps, at most 3 per SM sub-partition, so the softmax warps
-    // keep up to 168 registers; one warp streams K tiles and one V tiles, so
+    // MODE 0: 12 warps, 3 per SM sub-partition, so the softmax warps keep
+    // up to 168 registers; one warp streams K tiles and one V tiles, so
     // neither waits behind the other's ring slot (two lanes of one warp would
     // share its issue).  MODE 1 and 2: 13 warps, four of them producers (MODE
     // 1: each thread fetches and converts one key row of a tile; MODE 2: two
@@ -104,8 +109,13 @@ struct Cfg {
     // worth more than the softmax's spare registers (two producer warps: 1.6x
     // the kernel time).
     static constexpr int kProducerWarps = MODE == 0 ? 2 : (MODE == 1 ? 4 : 2 * kRowWarps);
+    // MMA issue: MODE 0, one warp for S = Q K^T and one for O += P V; the
+    // software-producer modes, one warp for both (a fourteenth warp measured
+    // 2 % slower there).
+    static constexpr bool kSplitIssue = MODE == 0;
     static constexpr int kMmaWarp = kSoftmaxWarps + kProducerWarps;
-    static constexpr int kThreads = (kMmaWarp + 1) * 32;
+    static constexpr int kPvWarp = kMmaWarp + (kSplitIssue ? 1 : 0);
+    static constexpr int kThreads = (kPvWarp + 1) * 32;
     // arrivals that fill a K or V stage: the TMA thread's expect-tx, every
     // producer thread (MODE 1), or the threads of the operand's two warps
     static constexpr uint32_t kFullCount = MODE == 0 ? 1 : (MODE == 1 ? kProducerWarps * 32 : kRowWarps * 32);
@@ -604,65 +614,119 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
             }
             cp_async_wait<0>();
         }
-    } else if (warp == C::kMmaWarp) {
-        // ---------------- MMA issuer ----------------------------------------
+    } else if (warp == C::kMmaWarp || warp == C::kPvWarp) {
+        // ---------------- MMA issue -------------------------------------------
+        // MODE 0: this warp's thread issues the S MMAs and the next warp's the
+        // PV MMAs, so that PV of one tile and S of a later one go out side by
+        // side (a thread's issue of eight MMAs takes about as long as the
+        // tensor core runs them).  MODE 1 and 2: one thread issues S of tile
+        // jj, then PV of tile jj-1.  Each issuer drains its own MMAs on abort:
+        // a commit covers every MMA its thread issued before it.
         if (lane == 0 && n_tiles > 0) {
-            bool ok = wait(B_QFULL, 0);
-            tc::tc_fence_after();
-            int last_bar = -1;                      // barrier and phase of the last commit
-            uint32_t last_par = 0;
             // operand descriptors of the first K and V slots; the rest are offsets
             const uint64_t dk0 = tc::smem_desc(sbase + kOffK, 16, 1024);
             const uint64_t dv0 = tc::smem_desc(sbase + kOffV, kHalfTile, 1024);
-            for (int jj = 0; ok && jj <= n_tiles; ++jj) {
-                if (jj < n_tiles) {
-                    const int b = jj & 1;
-                    const int kb = KLO ? 0 : b;
-                    const int sb = jj % kSBuf;
-                    if (!wait(B_KFULL + kb, KLO ? (jj & 1) : ((jj >> 1) & 1))) break;
-                    if (jj >= kSBuf && !wait(B_SFREE + sb, ((jj / kSBuf) - 1) & 1)) break;
+            int last_bar = -1;                      // barrier and phase of this thread's last commit
+            uint32_t last_par = 0;
+            if constexpr (C::kSplitIssue) {
+                if (warp == C::kMmaWarp) {
+                    bool ok = wait(B_QFULL, 0);
                     tc::tc_fence_after();
-                    const uint32_t d_s = tmem + static_cast<uint32_t>(sb * kPN);
-                    constexpr int KSTEPS = (KLO ? 2 : 1) * kPD / 16;   // hi then lo
+                    for (int jj = 0; ok && jj < n_tiles; ++jj) {
+                        const int b = jj & 1;
+                        const int kb = KLO ? 0 : b;
+                        const int sb = jj % kSBuf;
+                        if (!wait(B_KFULL + kb, KLO ? (jj & 1) : ((jj >> 1) & 1))) break;
+                        if (jj >= kSBuf && !wait(B_SFREE + sb, ((jj / kSBuf) - 1) & 1)) break;
+                        tc::tc_fence_after();
+                        const uint32_t d_s = tmem + static_cast<uint32_t>(sb * kPN);
+                        constexpr int KSTEPS = (KLO ? 2 : 1) * kPD / 16;   // hi then lo
 #pragma unroll
-                    for (int ks = 0; ks < KSTEPS; ++ks) {
-                        const int kk = ks % (kPD / 16);
-                        const uint32_t off = (kk >> 2) * kHalfTile + (kk & 3) * 32;
-                        const uint64_t bd = tc::desc_add(dk0, (KLO ? (ks / (kPD / 16)) : b) * kTileBytes + off);
-                        tc::mma_f16_ts(d_s, tmem + static_cast<uint32_t>(kQCol + kk * 8), bd, kIdescS, ks > 0);
+                        for (int ks = 0; ks < KSTEPS; ++ks) {
+                            const int kk = ks % (kPD / 16);
+                            const uint32_t off = (kk >> 2) * kHalfTile + (kk & 3) * 32;
+                            const uint64_t bd = tc::desc_add(dk0, (KLO ? (ks / (kPD / 16)) : b) * kTileBytes + off);
+                            tc::mma_f16_ts(d_s, tmem + static_cast<uint32_t>(kQCol + kk * 8), bd, kIdescS, ks > 0);
+                        }
+                        tc::mma_commit(bar(B_SFULL + sb));
+                        tc::mma_commit(bar(B_KEMPTY + kb));
+                        last_bar = B_SFULL + sb;
+                        last_par = (jj / kSBuf) & 1;
                     }
-                    tc::mma_commit(bar(B_SFULL + sb));
-                    tc::mma_commit(bar(B_KEMPTY + kb));
-                    last_bar = B_SFULL + sb;
-                    last_par = (jj / kSBuf) & 1;
+                } else {
+                    for (int j = 0; j < n_tiles; ++j) {
+                        const int b = j & 1;
+                        if (!wait(B_PFULL, j & 1)) break;
+                        if (!wait(B_VFULL + b, (j >> 1) & 1)) break;
+                        tc::tc_fence_after();
+                        const uint32_t d_o = tmem + kOCol;
+#pragma unroll
+                        for (int kk = 0; kk < kPN / 16; ++kk) {
+                            // P of keys 16kk .. 16kk+15: fp16 pairs in columns kPCol + 8kk ..
+                            const uint32_t a_t = tmem + static_cast<uint32_t>(kPCol + kk * 8);
+                            // V tile as B in MN-major layout: 16 keys = 2048 bytes per k-step;
+                            // the second 64-wide d block is kHalfTile away (leading offset),
+                            // 8-key row groups are 1024 bytes apart (stride offset).
+                            const uint64_t bd = tc::desc_add(dv0, b * kTileBytes + kk * 2048);
+                            tc::mma_f16_ts(d_o, a_t, bd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        tc::mma_commit(bar(B_VEMPTY + b));
+                        tc::mma_commit(bar(B_PFREE));
+                        last_bar = B_PFREE;
+                        last_par = j & 1;
+                    }
                 }
-                if (jj >= 1) {
-                    const int j = jj - 1;
-                    const int b = j & 1;
-                    if (!wait(B_PFULL, j & 1)) break;
-                    if (!wait(B_VFULL + b, (j >> 1) & 1)) break;
-                    tc::tc_fence_after();
-                    const uint32_t d_o = tmem + kOCol;
+            } else {
+                bool ok = wait(B_QFULL, 0);
+                tc::tc_fence_after();
+                for (int jj = 0; ok && jj <= n_tiles; ++jj) {
+                    if (jj < n_tiles) {
+                        const int b = jj & 1;
+                        const int kb = KLO ? 0 : b;
+                        const int sb = jj % kSBuf;
+                        if (!wait(B_KFULL + kb, KLO ? (jj & 1) : ((jj >> 1) & 1))) break;
+                        if (jj >= kSBuf && !wait(B_SFREE + sb, ((jj / kSBuf) - 1) & 1)) break;
+                        tc::tc_fence_after();
+                        const uint32_t d_s = tmem + static_cast<uint32_t>(sb * kPN);
+                        constexpr int KSTEPS = (KLO ? 2 : 1) * kPD / 16;   // hi then lo
 #pragma unroll
-                    for (int kk = 0; kk < kPN / 16; ++kk) {
-                        // P of keys 16kk .. 16kk+15: fp16 pairs in columns kPCol + 8kk ..
-                        const uint32_t a_t = tmem + static_cast<uint32_t>(kPCol + kk * 8);
-                        // V tile as B in MN-major layout: 16 keys = 2048 bytes per k-step;
-                        // the second 64-wide d block is kHalfTile away (leading offset),
-                        // 8-key row groups are 1024 bytes apart (stride offset).
-                        const uint64_t bd = tc::desc_add(dv0, b * kTileBytes + kk * 2048);
-                        tc::mma_f16_ts(d_o, a_t, bd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                        for (int ks = 0; ks < KSTEPS; ++ks) {
+                            const int kk = ks % (kPD / 16);
+                            const uint32_t off = (kk >> 2) * kHalfTile + (kk & 3) * 32;
+                            const uint64_t bd = tc::desc_add(dk0, (KLO ? (ks / (kPD / 16)) : b) * kTileBytes + off);
+                            tc::mma_f16_ts(d_s, tmem + static_cast<uint32_t>(kQCol + kk * 8), bd, kIdescS, ks > 0);
+                        }
+                        tc::mma_commit(bar(B_SFULL + sb));
+                        tc::mma_commit(bar(B_KEMPTY + kb));
+                        last_bar = B_SFULL + sb;
+                        last_par = (jj / kSBuf) & 1;
                     }
-                    tc::mma_commit(bar(B_VEMPTY + b));
-                    tc::mma_commit(bar(B_PFREE));
-                    last_bar = B_PFREE;
-                    last_par = j & 1;
+                    if (jj >= 1) {
+                        const int j = jj - 1;
+                        const int b = j & 1;
+                        if (!wait(B_PFULL, j & 1)) break;
+                        if (!wait(B_VFULL + b, (j >> 1) & 1)) break;
+                        tc::tc_fence_after();
+                        const uint32_t d_o = tmem + kOCol;
+#pragma unroll
+                        for (int kk = 0; kk < kPN / 16; ++kk) {
+                            // P of keys 16kk .. 16kk+15: fp16 pairs in columns kPCol + 8kk ..
+                            const uint32_t a_t = tmem + static_cast<uint32_t>(kPCol + kk * 8);
+                            // V tile as B in MN-major layout: 16 keys = 2048 bytes per k-step;
+                            // the second 64-wide d block is kHalfTile away (leading offset),
+                            // 8-key row groups are 1024 bytes apart (stride offset).
+                            const uint64_t bd = tc::desc_add(dv0, b * kTileBytes + kk * 2048);
+                            tc::mma_f16_ts(d_o, a_t, bd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        tc::mma_commit(bar(B_VEMPTY + b));
+                        tc::mma_commit(bar(B_PFREE));
+                        last_bar = B_PFREE;
+                        last_par = j & 1;
+                    }
                 }
             }
             if (*reinterpret_cast<volatile int *>(&s_abort) && last_bar >= 0)
-            {   // drain issued MMAs: the last commit covers every MMA issued before it
                 tc::mbar_wait(bar(last_bar), last_par, nullptr, 100000000ull);
-            }
         }
     } else {
         // ---------------- softmax warps (two threads per query row) -----------
