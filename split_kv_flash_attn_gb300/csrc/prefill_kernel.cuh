@@ -24,21 +24,24 @@
 //                   thread for both put them in series); MODE 1 and 2, one
 //                   thread issues both:
 //                   S_j = Q K_j^T        tcgen05.mma kind::f16, M=N=128, into
-//                                        one of two TMEM S buffers (fp32); Q
-//                                        is the A operand in tensor memory
-//                                        (placed there once by the softmax
-//                                        warps), which runs the MMA at twice
-//                                        the rate of an A read from shared
-//                                        memory;
+//                                        one of two TMEM S buffers (fp32).  Q
+//                                        is the A operand in shared memory
+//                                        (MODE 0; it runs at the same rate as
+//                                        an A in tensor memory when nothing
+//                                        else sits between the MMAs) or in
+//                                        tensor memory (MODE 1 and 2), placed
+//                                        once by the softmax warps;
 //                   O  += P_j V_j        into the TMEM O accumulator; V is the
 //                                        B operand in MN-major layout.
 //   softmax (0-7) : two threads per query row (TMEM lane), 64 key columns
 //                   each: tcgen05.ld S_j, causal / padding mask, online
-//                   softmax in log2 units, P_j (fp16) into its own tensor-memory
-//                   columns, where the PV MMA reads it as its A operand.  An S
-//                   buffer is released as soon as the softmax warps have loaded
-//                   it, so S_{j+1} and S_{j+2} are computed while P_j is; P_j
-//                   is written once PV_{j-1} has read P_{j-1}.  O is
+//                   softmax in log2 units, P_j (fp16) into tensor memory,
+//                   where the PV MMA reads it as its A operand.  An S buffer
+//                   is released as soon as the softmax warps have loaded it,
+//                   so S_{j+1} and S_{j+2} are computed while P_j is.  MODE 0
+//                   keeps two P buffers (the tensor-memory columns Q would
+//                   take), so P_j is written once PV_{j-2} has read P_{j-2};
+//                   MODE 1 and 2 one, written once PV_{j-1} is done.  O is
 //                   rescaled in TMEM only when a row maximum grows by more than
 //                   2^8 (the stale maximum stays the reference otherwise,
 //                   exactly as in the plain online softmax with another shift),
@@ -69,19 +72,25 @@ constexpr int kTileBytes = kPN * kPD * 2;       // 32 KiB per K or V tile
 constexpr int kHalfTile = kTileBytes / 2;       // one 64-column swizzle block
 constexpr int kOffK = 0;                        // 2 stages (quantised keys: hi and lo of one stage)
 constexpr int kOffV = kOffK + 2 * kTileBytes;   // 2 stages
-constexpr int kOffBar = kOffV + 2 * kTileBytes;   // (Q and P live in tensor memory)
+// TMA instance (MODE 0): Q (the S MMA's A operand) after the V stages, then
+// the barriers.  Software-producer instances keep Q in tensor memory and put
+// the barriers right after the V stages; the quantised ones then stage raw
+// row segments (two tiles of K and V segments), so that a tile's global
+// loads are in flight while the previous tile is decoded.
+constexpr int kOffQ = kOffV + 2 * kTileBytes;
+constexpr int kOffBar = kOffQ;                  // software-producer instances
+constexpr int kOffBarQ = kOffQ + kTileBytes;    // TMA instance
 constexpr int kSmem = kOffBar + 256 + 1024;     // + barriers + alignment slack
-// Quantised instances also stage raw row segments (two tiles of K and V
-// segments) after the barriers, so that a tile's global loads are in flight
-// while the previous tile is decoded.
 constexpr int kOffRaw = kOffBar + 256;
 __host__ __device__ constexpr int seg_bytes_of(int t) { return t == SKV_F16 ? 256 : (t == SKV_Q8_0 ? 136 : 72); }
-template <int KT, int VT>
+template <int MODE, int KT, int VT>
 __host__ __device__ constexpr int smem_bytes()
 {
-    return KT == SKV_F16 ? kSmem : kSmem + 2 * kPN * (seg_bytes_of(KT) + seg_bytes_of(VT));
+    return MODE == 0 ? kOffBarQ + 256 + 1024
+                     : kSmem + (KT == SKV_F16 ? 0 : 2 * kPN * (seg_bytes_of(KT) + seg_bytes_of(VT)));
 }
 static_assert(kSmem + 2 * kPN * (136 + 136) <= 227 * 1024, "shared memory per CTA");
+static_assert(kOffBarQ + 256 + 1024 <= 227 * 1024, "shared memory per CTA");
 constexpr uint32_t kIdescS = tc::idesc_f16(kPM, kPN, false);
 constexpr uint32_t kIdescPV = tc::idesc_f16(kPM, kPD, true);
 constexpr float kRescaleLog2 = 8.0f;            // rescale O only when the max grows by > 2^8
@@ -125,23 +134,29 @@ struct Cfg {
 };
 
 // barrier slots (8 bytes each) inside the barrier area
-// Tensor memory: kSBuf S buffers (fp32), then P (fp16 pairs), Q (fp16 pairs:
-// row m in lane m, dims 2c, 2c+1 in column c) and O (fp32).  S full (MMA
-// commit) and S free (the softmax warps have loaded S) are per S buffer: tile
-// j's are buffer j % kSBuf, phase j / kSBuf.  P full (softmax) and P free
-// (commit after PV: P read, O updated) are single barriers, phase j % 2; no
-// waiter can be two phases away from the phase it waits for (mbarrier waits
-// are by phase parity), because each side needs the other's next step before
-// it can complete another phase.  A commit arrives once every earlier MMA of
-// the issuing thread is done, so "PV of tile j done" means every earlier PV is.
+// Tensor memory: kSBuf S buffers (fp32), then two 64-column slots and O
+// (fp32).  TMA instance: the slots are two P buffers (fp16 pairs), tile j's
+// P in slot j % 2, so a tile's P is written while PV of the previous tile
+// still reads its own; Q is in shared memory.  Software-producer instances
+// (quantised raw staging leaves no shared memory for Q, and over row lists
+// the shared-memory Q measured 2 % slower): slot 0 holds P, slot 1 Q (row m
+// in lane m, dims 2c, 2c+1 in column c).  S full (MMA commit) and S free
+// (the softmax warps have loaded S) are per S buffer: tile j's are buffer
+// j % kSBuf, phase j / kSBuf.  P full (softmax) and P free (commit after PV:
+// P read, O updated) are per P buffer: tile j's are buffer j % 2, phase j / 2
+// (software producers: buffer 0, phase j).  No waiter can be two phases away from the
+// phase it waits for (mbarrier waits are by phase parity), because each side
+// needs the other's next step before it can complete another phase.  A commit
+// arrives once every earlier MMA of the issuing thread is done, so "PV of
+// tile j done" means every earlier PV is.
 constexpr int kSBuf = 2;
-constexpr int kPCol = kSBuf * kPN;              // P: keys 2c, 2c+1 of the tile in column kPCol + c
-constexpr int kQCol = kPCol + kPN / 2;
+constexpr int kPCol = kSBuf * kPN;              // P: keys 2c, 2c+1 of the tile in column kPCol (+64) + c
+constexpr int kQCol = kPCol + kPN / 2;          // software-producer instances
 constexpr int kOCol = kQCol + kPD / 2;          // first TMEM column of O
 // (M full: row-list mode, a tile's padding mask is in shared memory; 4 slots,
 // tile j in slot j % 4.)
 enum { B_KFULL = 0, B_KEMPTY = 2, B_VFULL = 4, B_VEMPTY = 6, B_QFULL = 8, B_SFULL = 9, B_SFREE = 9 + kSBuf,
-       B_PFULL = 9 + 2 * kSBuf, B_PFREE = 10 + 2 * kSBuf, B_MFULL = 11 + 2 * kSBuf, B_COUNT = 15 + 2 * kSBuf };
+       B_PFULL = 9 + 2 * kSBuf, B_PFREE = 11 + 2 * kSBuf, B_MFULL = 13 + 2 * kSBuf, B_COUNT = 17 + 2 * kSBuf };
 static_assert(B_COUNT * 8 <= 256, "barrier area");
 static_assert(kOCol + kPD <= 512, "tensor memory columns");
 
@@ -287,10 +302,11 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
     // the two K slots, and S = Q hi^T + Q lo^T (16 k-steps), so that scores
     // use the exact key values; fp16 keys: a 2-deep K ring.
     constexpr bool KLO = KT != SKV_F16;
+    constexpr bool P2 = MODE == 0;              // two P buffers, Q in shared memory
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_addr(sm);
-    const uint32_t bar0 = sbase + kOffBar;
+    const uint32_t bar0 = sbase + (P2 ? kOffBarQ : kOffBar);
     auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
@@ -347,8 +363,10 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
             tc::mbar_init(bar(B_SFULL + i), 1);
             tc::mbar_init(bar(B_SFREE + i), kSoftmaxThreads);   // S buffer free: the softmax warps loaded it
         }
-        tc::mbar_init(bar(B_PFULL), kSoftmaxThreads);
-        tc::mbar_init(bar(B_PFREE), 1);                          // PV of the last P done
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(bar(B_PFULL + i), kSoftmaxThreads);
+            tc::mbar_init(bar(B_PFREE + i), 1);                  // PV of the buffer's last P done
+        }
         tc::mbar_init(bar(B_QFULL), kSoftmaxThreads);
         for (int i = 0; i < 4; ++i) tc::mbar_init(bar(B_MFULL + i), C::kMaskCount);
         tc::fence_barrier_init();
@@ -626,6 +644,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
             // operand descriptors of the first K and V slots; the rest are offsets
             const uint64_t dk0 = tc::smem_desc(sbase + kOffK, 16, 1024);
             const uint64_t dv0 = tc::smem_desc(sbase + kOffV, kHalfTile, 1024);
+            const uint64_t dq0 = tc::smem_desc(sbase + kOffQ, 16, 1024);   // Q (TMA instance)
             int last_bar = -1;                      // barrier and phase of this thread's last commit
             uint32_t last_par = 0;
             if constexpr (C::kSplitIssue) {
@@ -646,7 +665,10 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                             const int kk = ks % (kPD / 16);
                             const uint32_t off = (kk >> 2) * kHalfTile + (kk & 3) * 32;
                             const uint64_t bd = tc::desc_add(dk0, (KLO ? (ks / (kPD / 16)) : b) * kTileBytes + off);
-                            tc::mma_f16_ts(d_s, tmem + static_cast<uint32_t>(kQCol + kk * 8), bd, kIdescS, ks > 0);
+                            if constexpr (P2)
+                                tc::mma_f16_ss(d_s, tc::desc_add(dq0, off), bd, kIdescS, ks > 0);
+                            else
+                                tc::mma_f16_ts(d_s, tmem + static_cast<uint32_t>(kQCol + kk * 8), bd, kIdescS, ks > 0);
                         }
                         tc::mma_commit(bar(B_SFULL + sb));
                         tc::mma_commit(bar(B_KEMPTY + kb));
@@ -656,14 +678,15 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                 } else {
                     for (int j = 0; j < n_tiles; ++j) {
                         const int b = j & 1;
-                        if (!wait(B_PFULL, j & 1)) break;
+                        const int pb = P2 ? (j & 1) : 0;             // P buffer of tile j
+                        if (!wait(B_PFULL + pb, (P2 ? (j >> 1) : j) & 1)) break;
                         if (!wait(B_VFULL + b, (j >> 1) & 1)) break;
                         tc::tc_fence_after();
                         const uint32_t d_o = tmem + kOCol;
 #pragma unroll
                         for (int kk = 0; kk < kPN / 16; ++kk) {
                             // P of keys 16kk .. 16kk+15: fp16 pairs in columns kPCol + 8kk ..
-                            const uint32_t a_t = tmem + static_cast<uint32_t>(kPCol + kk * 8);
+                            const uint32_t a_t = tmem + static_cast<uint32_t>(kPCol + pb * (kPN / 2) + kk * 8);
                             // V tile as B in MN-major layout: 16 keys = 2048 bytes per k-step;
                             // the second 64-wide d block is kHalfTile away (leading offset),
                             // 8-key row groups are 1024 bytes apart (stride offset).
@@ -671,9 +694,9 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                             tc::mma_f16_ts(d_o, a_t, bd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
                         }
                         tc::mma_commit(bar(B_VEMPTY + b));
-                        tc::mma_commit(bar(B_PFREE));
-                        last_bar = B_PFREE;
-                        last_par = j & 1;
+                        tc::mma_commit(bar(B_PFREE + pb));
+                        last_bar = B_PFREE + pb;
+                        last_par = (P2 ? (j >> 1) : j) & 1;
                     }
                 }
             } else {
@@ -694,7 +717,10 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                             const int kk = ks % (kPD / 16);
                             const uint32_t off = (kk >> 2) * kHalfTile + (kk & 3) * 32;
                             const uint64_t bd = tc::desc_add(dk0, (KLO ? (ks / (kPD / 16)) : b) * kTileBytes + off);
-                            tc::mma_f16_ts(d_s, tmem + static_cast<uint32_t>(kQCol + kk * 8), bd, kIdescS, ks > 0);
+                            if constexpr (P2)
+                                tc::mma_f16_ss(d_s, tc::desc_add(dq0, off), bd, kIdescS, ks > 0);
+                            else
+                                tc::mma_f16_ts(d_s, tmem + static_cast<uint32_t>(kQCol + kk * 8), bd, kIdescS, ks > 0);
                         }
                         tc::mma_commit(bar(B_SFULL + sb));
                         tc::mma_commit(bar(B_KEMPTY + kb));
@@ -704,14 +730,15 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                     if (jj >= 1) {
                         const int j = jj - 1;
                         const int b = j & 1;
-                        if (!wait(B_PFULL, j & 1)) break;
+                        const int pb = P2 ? (j & 1) : 0;             // P buffer of tile j
+                        if (!wait(B_PFULL + pb, (P2 ? (j >> 1) : j) & 1)) break;
                         if (!wait(B_VFULL + b, (j >> 1) & 1)) break;
                         tc::tc_fence_after();
                         const uint32_t d_o = tmem + kOCol;
 #pragma unroll
                         for (int kk = 0; kk < kPN / 16; ++kk) {
                             // P of keys 16kk .. 16kk+15: fp16 pairs in columns kPCol + 8kk ..
-                            const uint32_t a_t = tmem + static_cast<uint32_t>(kPCol + kk * 8);
+                            const uint32_t a_t = tmem + static_cast<uint32_t>(kPCol + pb * (kPN / 2) + kk * 8);
                             // V tile as B in MN-major layout: 16 keys = 2048 bytes per k-step;
                             // the second 64-wide d block is kHalfTile away (leading offset),
                             // 8-key row groups are 1024 bytes apart (stride offset).
@@ -719,9 +746,9 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                             tc::mma_f16_ts(d_o, a_t, bd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
                         }
                         tc::mma_commit(bar(B_VEMPTY + b));
-                        tc::mma_commit(bar(B_PFREE));
-                        last_bar = B_PFREE;
-                        last_par = j & 1;
+                        tc::mma_commit(bar(B_PFREE + pb));
+                        last_bar = B_PFREE + pb;
+                        last_par = (P2 ? (j >> 1) : j) & 1;
                     }
                 }
             }
@@ -731,8 +758,9 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
     } else {
         // ---------------- softmax warps (two threads per query row) -----------
         const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-        // Q: this thread's half of its row (dims hf*64 ..) -> tensor memory
-        // columns kQCol + hf*32 .., two fp16 per column.
+        // Q: this thread's half of its row (dims hf*64 ..) -> shared memory in
+        // the swizzled K-major layout of a K tile (TMA instance), or tensor
+        // memory columns kQCol + hf*32 .., two fp16 per column.
         {
             const __half *qp = a.q + ((static_cast<int64_t>(s) * a.nq + (row_ok ? t_row : 0)) * a.H + kh * a.G +
                                       (m % a.G)) * kPD + hf * 64;
@@ -740,14 +768,22 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
 #pragma unroll
             for (int cc = 0; cc < 8; ++cc) {
                 const uint4 v = row_ok ? *reinterpret_cast<const uint4 *>(qp + cc * 8) : make_uint4(0, 0, 0, 0);
-                qw[4 * cc] = v.x;
-                qw[4 * cc + 1] = v.y;
-                qw[4 * cc + 2] = v.z;
-                qw[4 * cc + 3] = v.w;
+                if constexpr (P2) {
+                    *reinterpret_cast<uint4 *>(sm + kOffQ + tile_off(m, hf * 8 + cc)) = v;
+                } else {
+                    qw[4 * cc] = v.x;
+                    qw[4 * cc + 1] = v.y;
+                    qw[4 * cc + 2] = v.z;
+                    qw[4 * cc + 3] = v.w;
+                }
             }
-            tc::tmem_st32u(lane_base + kQCol + hf * 32, qw);
-            tc::tmem_wait_st();
-            tc::tc_fence_before();
+            if constexpr (P2) {
+                tc::fence_proxy_async_smem();
+            } else {
+                tc::tmem_st32u(lane_base + kQCol + hf * 32, qw);
+                tc::tmem_wait_st();
+                tc::tc_fence_before();
+            }
             tc::mbar_arrive(bar(B_QFULL));
         }
         constexpr int NC = kPN / 2;                 // columns per thread
@@ -828,14 +864,21 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
             }
             l_run = l_run * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));   // this half's columns
             m_ref = ref;
-            // P and O are free once PV of the previous tile is done (long
-            // done by now: it was issued when that tile's P was ready).  O is
-            // rescaled only when the reference maximum moved (rarely).
-            if (j > 0) {
-                __all_sync(0xffffffffu, wait(B_PFREE, (j - 1) & 1));
+            // P's buffer is free once PV of the tile before last (two P
+            // buffers) or of the previous tile (one) is done.  O is rescaled
+            // only when the reference maximum moved (rarely), once PV of the
+            // previous tile is done.
+            const int pb = P2 ? (j & 1) : 0;
+            if (j >= (P2 ? 2 : 1)) {
+                __all_sync(0xffffffffu, wait(B_PFREE + pb, (P2 ? (j >> 1) - 1 : j - 1) & 1));
                 tc::tc_fence_after();
             }
-            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+            const bool resc_o = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
+            if (P2 && resc_o) {
+                __all_sync(0xffffffffu, wait(B_PFREE + ((j - 1) & 1), ((j - 1) >> 1) & 1));
+                tc::tc_fence_after();
+            }
+            if (resc_o) {
 #pragma unroll
                 for (int c = 0; c < NC / 32; ++c) {
                     uint32_t rr[32];
@@ -847,16 +890,19 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                     tc::tmem_st32(lane_base + kOCol + hf * NC + c * 32, v);
                 }
             }
-            // P (fp16 pairs): keys hf*64 + 2c, +1 in column kPCol + hf*32 + c
-            tc::tmem_st32u(lane_base + kPCol + hf * (NC / 2), ph);
+            // P (fp16 pairs): keys hf*64 + 2c, +1 in column kPCol + 64 pb + hf*32 + c
+            tc::tmem_st32u(lane_base + kPCol + pb * (kPN / 2) + hf * (NC / 2), ph);
             tc::tmem_wait_st();
             tc::tc_fence_before();
-            tc::mbar_arrive(bar(B_PFULL));
+            tc::mbar_arrive(bar(B_PFULL + pb));
         }
         // ---------------- epilogue: O / l, lse -------------------------------
         float ov[NC];
         bool have = n_tiles > 0 && !*reinterpret_cast<volatile int *>(&s_abort);
-        if (have) have = wait(B_PFREE, (n_tiles - 1) & 1);   // the last PV
+        if (have) {                                            // the last PV
+            const int jl = n_tiles - 1;
+            have = wait(B_PFREE + (P2 ? (jl & 1) : 0), (P2 ? (jl >> 1) : jl) & 1);
+        }
         have = __all_sync(0xffffffffu, have);
         if (have) {
             tc::tc_fence_after();
@@ -966,10 +1012,10 @@ int launch_prefill_t(skv_handle *h, const CUtensorMap &mk, const CUtensorMap &mv
                      cudaStream_t st)
 {
     cudaError_t e = kernel_smem_optin(prefill_attr_cache<MODE, KT, VT>(), reinterpret_cast<const void *>(splitkv_prefill_kernel<MODE, KT, VT>),
-                                      smem_bytes<KT, VT>(), Cfg<MODE>::kThreads, nullptr);
+                                      smem_bytes<MODE, KT, VT>(), Cfg<MODE>::kThreads, nullptr);
     if (e != cudaSuccess) return cuda_fail(h, e, "cudaFuncSetAttribute(prefill)");
     if (h->prof_before) cudaEventRecord(h->prof_before, st);
-    splitkv_prefill_kernel<MODE, KT, VT><<<grid, Cfg<MODE>::kThreads, smem_bytes<KT, VT>(), st>>>(mk, mv, a);
+    splitkv_prefill_kernel<MODE, KT, VT><<<grid, Cfg<MODE>::kThreads, smem_bytes<MODE, KT, VT>(), st>>>(mk, mv, a);
     if (h->prof_after) cudaEventRecord(h->prof_after, st);
     return cuda_fail(h, cudaGetLastError(), "prefill kernel launch");
 }
