@@ -29,6 +29,10 @@ __global__ void __launch_bounds__(kCombineThreads) splitkv_combine_kernel(int n_
     __shared__ float red[kCombineThreads / 32];
     __shared__ float4 acc_s[kCombineThreads / 32][32];
     static_assert(kCombineThreads % 32 == 0 && kCombineThreads <= 1024, "threads per row");
+    // Launched as a programmatic dependent of the kernel that wrote the
+    // parts: wait until that grid has completed and its writes are visible
+    // (at once when there is no such grid).
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
     const int64_t row = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float M = -INFINITY;
@@ -120,13 +124,27 @@ int launch_combine(int n_parts, const float *o_parts, const float *lse_parts, in
 {
     if (rows <= 0) return SKV_OK;
     if (rows > 0x7fffffff || n_parts > kCombineMaxParts || D > 128 || D % 4) return SKV_EUNSUPPORTED;
-    if (n_parts >= 64 && rows <= 512)
-        splitkv_combine_kernel<1024><<<static_cast<unsigned>(rows), 1024, 0, st>>>(n_parts, o_parts, lse_parts, rows, D,
-                                                                                    o, lse);
-    else
-        splitkv_combine_kernel<256><<<static_cast<unsigned>(rows), 256, 0, st>>>(n_parts, o_parts, lse_parts, rows, D,
-                                                                                  o, lse);
-    return cudaGetLastError() == cudaSuccess ? SKV_OK : SKV_ECUDA;
+    // Programmatic dependent launch: the combine's CTAs may be scheduled
+    // while the kernel before it on the stream finishes (that kernel lets its
+    // dependents launch once its CTAs are past their main loop); each waits
+    // for the whole of it before reading a part.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(rows));
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    if (n_parts >= 64 && rows <= 512) {
+        cfg.blockDim = dim3(1024);
+        e = cudaLaunchKernelEx(&cfg, splitkv_combine_kernel<1024>, n_parts, o_parts, lse_parts, rows, D, o, lse);
+    } else {
+        cfg.blockDim = dim3(256);
+        e = cudaLaunchKernelEx(&cfg, splitkv_combine_kernel<256>, n_parts, o_parts, lse_parts, rows, D, o, lse);
+    }
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? SKV_OK : SKV_ECUDA;
 }
 
 }  // namespace skv

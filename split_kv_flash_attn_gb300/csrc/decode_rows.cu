@@ -381,6 +381,10 @@ __global__ void __launch_bounds__(256) splitkv_decode_rows_kernel(const DecodeAr
             tc::mbar_wait(bar(j % kRStages), (j / kRStages) & 1, nullptr, 100000000ull);
     }
 
+    // The combine that merges the splits may be scheduled from here on (it
+    // waits for this whole grid before reading).
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+
     // ---- normalised partial O (this warp's head, 8 columns) and lse ----
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
