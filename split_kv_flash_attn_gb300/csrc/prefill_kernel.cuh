@@ -814,32 +814,36 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                 vm1 = s_vmask[j & 3][hf * 2 + 1];
             }
             tc::tc_fence_after();
-            uint32_t sr[NC / 32][32];
-#pragma unroll
-            for (int c = 0; c < NC / 32; ++c) tc::tmem_ld32(lane_base + sb * kPN + hf * NC + c * 32, sr[c]);
-#pragma unroll
-            for (int c = 0; c < NC / 32; ++c) tc::tmem_wait_ld(sr[c]);
-            tc::tc_fence_before();
-            tc::mbar_arrive(bar(B_SFREE + sb));           // the S buffer may take the next tile's S
-            float x[NC];
-#pragma unroll
-            for (int c = 0; c < NC / 32; ++c)
-#pragma unroll
-                for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(sr[c][i]);
-
             const int64_t pos0 = a.key_pos0 + a.logical0 + key0;
             const int64_t lim_pos = static_cast<int64_t>(pos_row) - pos0;   // columns > lim_pos are masked
             const int64_t lim_end = j_hi - key0;                            // columns >= lim_end are outside the split
-            // Masking only where a tile reaches past a row's position or the
-            // split's end, or holds padding (warp-uniform test; most tiles
-            // skip it).
-            if (__any_sync(0xffffffffu, lim_pos < NC - 1 || lim_end < NC || (vm0 & vm1) != 0xffffffffu)) {
+            // This half's scores, masked only where a tile reaches past a
+            // row's position or the split's end, or holds padding
+            // (warp-uniform test; most tiles skip it).
+            float x[NC];
+            auto load_scores = [&](bool release) {
+                uint32_t sr[NC / 32][32];
 #pragma unroll
-                for (int i = 0; i < NC; ++i) {
-                    const bool present = ((i < 32 ? vm0 : vm1) >> (i & 31)) & 1u;
-                    if (i > lim_pos || i >= lim_end || !present) x[i] = -INFINITY;
+                for (int c = 0; c < NC / 32; ++c) tc::tmem_ld32(lane_base + sb * kPN + hf * NC + c * 32, sr[c]);
+#pragma unroll
+                for (int c = 0; c < NC / 32; ++c) tc::tmem_wait_ld(sr[c]);
+                if (release) {
+                    tc::tc_fence_before();
+                    tc::mbar_arrive(bar(B_SFREE + sb));   // the S buffer may take the next tile's S
                 }
-            }
+#pragma unroll
+                for (int c = 0; c < NC / 32; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(sr[c][i]);
+                if (__any_sync(0xffffffffu, lim_pos < NC - 1 || lim_end < NC || (vm0 & vm1) != 0xffffffffu)) {
+#pragma unroll
+                    for (int i = 0; i < NC; ++i) {
+                        const bool present = ((i < 32 ? vm0 : vm1) >> (i & 31)) & 1u;
+                        if (i > lim_pos || i >= lim_end || !present) x[i] = -INFINITY;
+                    }
+                }
+            };
+            load_scores(!P2);
             // Row maximum on the raw scores (the scale is positive): this
             // half's four chains, then the partner half's value.
             float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -852,22 +856,44 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
             }
             const float mh = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
             s_pair[b][hf][m] = mh;
+            // p = 2^(s * scale_log2 - ref): one FMA and one exp2 per score.
+            float ls[4];
+            uint32_t ph[NC / 2];
+            auto exps = [&](float nref) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) ls[q] = 0.f;
+#pragma unroll
+                for (int i = 0; i < NC; i += 2) {
+                    const float p0 = fast_exp2(fmaf(x[i], a.scale_log2, nref));
+                    const float p1 = fast_exp2(fmaf(x[i + 1], a.scale_log2, nref));
+                    ls[(i >> 1) & 3] += p0 + p1;
+                    ph[i / 2] = pack_half2(p0, p1);
+                }
+            };
+            // TMA instance: the exponentials are first taken against the
+            // current reference, which stays unless the row maximum grew by
+            // more than 2^8 (rare after a row's first tile), while the partner
+            // half is still on its way to the exchange; a warp with a row
+            // whose reference moves loads its scores again and takes them over,
+            // and the S buffer is released once that is settled (the S MMAs
+            // run ahead).  The software-producer instances, at 128 registers,
+            // exchange first and keep no second pass.
+            if constexpr (P2) exps(m_ref == -INFINITY ? 0.f : -m_ref);
             pair_sync();
             const float mx = fmaxf(mh, s_pair[b][hf ^ 1][m]) * a.scale_log2;
             const float m_new = fmaxf(m_ref, mx);
             const bool resc = m_new > m_ref + kRescaleLog2;   // true on the first finite maximum
             const float ref = resc ? m_new : m_ref;
             const float alpha = resc ? fast_exp2(m_ref - ref) : 1.f;
-            const float neg_ref = ref == -INFINITY ? 0.f : -ref;
-            // p = 2^(s * scale_log2 - ref): one FMA and one exp2 per score.
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
-            uint32_t ph[NC / 2];
-#pragma unroll
-            for (int i = 0; i < NC; i += 2) {
-                const float p0 = fast_exp2(fmaf(x[i], a.scale_log2, neg_ref));
-                const float p1 = fast_exp2(fmaf(x[i + 1], a.scale_log2, neg_ref));
-                ls[(i >> 1) & 3] += p0 + p1;
-                ph[i / 2] = pack_half2(p0, p1);
+            if constexpr (P2) {
+                if (__any_sync(0xffffffffu, resc)) {
+                    load_scores(false);
+                    exps(ref == -INFINITY ? 0.f : -ref);
+                }
+                tc::tc_fence_before();
+                tc::mbar_arrive(bar(B_SFREE + sb));       // the S buffer may take the next tile's S
+            } else {
+                exps(ref == -INFINITY ? 0.f : -ref);
             }
             l_run = l_run * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));   // this half's columns
             m_ref = ref;
