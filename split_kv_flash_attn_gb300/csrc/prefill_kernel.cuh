@@ -844,6 +844,13 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                 }
             };
             load_scores(!P2);
+            if (P2 && j > 0) {
+                // the previous tile's P store has landed by now: publish it
+                // (its PV is not urgent with two P buffers)
+                tc::tmem_wait_st();
+                tc::tc_fence_before();
+                tc::mbar_arrive(bar(B_PFULL + ((j - 1) & 1)));
+            }
             // Row maximum on the raw scores (the scale is positive): this
             // half's four chains, then the partner half's value.
             float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -923,11 +930,20 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
                     tc::tmem_st32(lane_base + kOCol + hf * NC + c * 32, v);
                 }
             }
-            // P (fp16 pairs): keys hf*64 + 2c, +1 in column kPCol + 64 pb + hf*32 + c
+            // P (fp16 pairs): keys hf*64 + 2c, +1 in column kPCol + 64 pb + hf*32 + c;
+            // the TMA instance publishes it after the next tile's scores are
+            // loaded, so that the store lands under that load
             tc::tmem_st32u(lane_base + kPCol + pb * (kPN / 2) + hf * (NC / 2), ph);
+            if constexpr (!P2) {
+                tc::tmem_wait_st();
+                tc::tc_fence_before();
+                tc::mbar_arrive(bar(B_PFULL + pb));
+            }
+        }
+        if (P2 && n_tiles > 0) {
             tc::tmem_wait_st();
             tc::tc_fence_before();
-            tc::mbar_arrive(bar(B_PFULL + pb));
+            tc::mbar_arrive(bar(B_PFULL + ((n_tiles - 1) & 1)));
         }
         // ---------------- epilogue: O / l, lse -------------------------------
         float ov[NC];
