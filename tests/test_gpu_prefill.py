@@ -73,6 +73,33 @@ def test_prefill_causal_subrange(skv, h, oracle_mod):
     assert h.status() == 0
 
 
+@pytest.mark.parametrize("rows_list", [False, True])
+def test_prefill_reference_moves_on_a_later_tile(skv, h, oracle_mod, rows_list):
+    """Keys of later 128-key tiles scaled up (x4 in tile 3, x12 in tile 6,
+    x40 on four keys of tile 9) so that row maxima grow by far more than 2^8
+    after the first tile: the kernel's lazy reference moves mid-walk, O is
+    rescaled in tensor memory and the tile's exponentials are taken again
+    against the new reference (the dense range runs the TMA kernel, the
+    identity row list the copy-warp kernel)."""
+    S, nq, H, Hk, n = 1, 64, 32, 8, 1400
+    rng, q, K, V = _case(812, S, nq, H, Hk, n)
+    Kf = K.view(np.float16).reshape(n, Hk * 128).astype(np.float32)
+    Kf[3 * 128:4 * 128] *= 4.0
+    Kf[6 * 128:7 * 128] *= 12.0
+    Kf[9 * 128 + 5:9 * 128 + 9] *= 40.0
+    K = Kf.astype(np.float16).view(np.uint8).reshape(n, Hk * 256)
+    kw = {"kv_rows": dev(np.arange(n, dtype=np.int32).reshape(1, n))} if rows_list else {}
+    o, l = skv.attn_partial(h, dev(q), dev(K), dev(V), Hk=Hk, **kw)
+    want_o, want_l = oracle_mod.attention(q, D=128, H=H, Hk=Hk, scale=1 / math.sqrt(128), k0=K, v0=V, n_rows0=n,
+                                          k_row_bytes0=K.shape[1], v_row_bytes0=V.shape[1], n_keys=n)
+    # the maxima did move by more than 2^8 (log2 units) after the first tile
+    first = oracle_mod.attention(q, D=128, H=H, Hk=Hk, scale=1 / math.sqrt(128), k0=K[:128], v0=V[:128],
+                                 n_rows0=128, k_row_bytes0=K.shape[1], v_row_bytes0=V.shape[1], n_keys=128)[1]
+    assert float(np.max(want_l - first)) / math.log(2) > 8
+    check_attention(o, l, want_o, want_l, vmax_of(oracle_mod, wl.F16, V, 128), "reference moves")
+    assert h.status() == 0
+
+
 @pytest.mark.parametrize("tile_rows", [384, 1024])
 def test_prefill_window_tail_reduced(skv, h, oracle_mod, tile_rows):
     w = wl.prefill_chunk(n_kv=4096, wc=2048, nq=64, H=32, Hk=8, D=128, tile_rows=tile_rows)
