@@ -36,16 +36,23 @@
 //   softmax (0-7) : two threads per query row (TMEM lane), 64 key columns
 //                   each: tcgen05.ld S_j, causal / padding mask, online
 //                   softmax in log2 units, P_j (fp16) into tensor memory,
-//                   where the PV MMA reads it as its A operand.  An S buffer
-//                   is released as soon as the softmax warps have loaded it,
-//                   so S_{j+1} and S_{j+2} are computed while P_j is.  MODE 0
-//                   keeps two P buffers (the tensor-memory columns Q would
-//                   take), so P_j is written once PV_{j-2} has read P_{j-2};
-//                   MODE 1 and 2 one, written once PV_{j-1} is done.  O is
+//                   where the PV MMA reads it as its A operand.  O is
 //                   rescaled in TMEM only when a row maximum grows by more than
 //                   2^8 (the stale maximum stays the reference otherwise,
 //                   exactly as in the plain online softmax with another shift),
 //                   so the softmax waits for the previous PV only then.
+//                   MODE 1 and 2: an S buffer is released as soon as the
+//                   softmax warps have loaded it (S_{j+1} and S_{j+2} are
+//                   computed while P_j is), the row maximum is exchanged
+//                   between a row's two warps before the exponentials, and
+//                   P_j is written once PV_{j-1} is done.  MODE 0: two P
+//                   buffers (the tensor-memory columns Q would take), so P_j
+//                   is written once PV_{j-2} has read P_{j-2} and published
+//                   after the next tile's scores are loaded; the exponentials
+//                   are taken against the current reference while the
+//                   maximum exchange completes, and taken again (the scores
+//                   reloaded, the S buffer released only then) by a warp whose
+//                   row's reference moves.
 //
 // The per-split result (O normalised, lse) is merged across splits by the
 // last CTA of each (sequence, KV head, query tile), as in the decode kernel.
