@@ -21,7 +21,7 @@ from . import _lib
 from ._lib import F16, Q4_0, Q8_0, SkvShape
 
 __all__ = ["Handle", "SplitKVError", "F16", "Q8_0", "Q4_0", "attn_partial", "attn_combine", "attn_window_tail",
-           "attn_paged", "BlockCache", "kv_dequant_q8_0", "kv_dequant_q4_0", "gather_rows", "kv_append", "plan_splits",
+           "attn_paged", "BlockCache", "kv_dequant_q8_0", "kv_dequant_q4_0", "gather_rows", "kv_append", "plan_splits", "plan_prefill_splits",
            "segment_bytes"]
 
 
@@ -111,6 +111,17 @@ class Handle:
             self.close()
         except Exception:
             pass
+
+
+def plan_prefill_splits(n_keys, n_units, sm_count, k_type=F16):
+    """The tensor-core prefill path's split plan (no GPU needed): returns
+    (split_len, n_splits)."""
+    sl, ns = ctypes.c_int64(), ctypes.c_int32()
+    rc = _lib.lib().skv_plan_prefill_splits(int(n_keys), int(n_units), int(sm_count), int(k_type), ctypes.byref(sl),
+                                            ctypes.byref(ns))
+    if rc != 0:
+        raise SplitKVError(rc, "skv_plan_prefill_splits rejected its arguments")
+    return sl.value, ns.value
 
 
 def plan_splits(n_keys, n_units, sm_count, ctas_per_sm, tile=64, max_split=0):

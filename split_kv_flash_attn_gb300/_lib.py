@@ -20,7 +20,7 @@ F16, Q8_0, Q4_0 = 0, 1, 2
 # Every entry point that include/splitkv.h declares.
 EXPORTS = [
     "skv_create", "skv_destroy", "skv_last_error", "skv_status_string", "skv_reserve", "skv_scratch_info",
-    "skv_sm_count", "skv_status", "skv_set_profile_events", "skv_plan_splits", "skv_attn_partial", "skv_attn_combine", "skv_attn_window_tail",
+    "skv_sm_count", "skv_status", "skv_set_profile_events", "skv_plan_splits", "skv_plan_prefill_splits", "skv_attn_partial", "skv_attn_combine", "skv_attn_window_tail",
     "skv_kv_dequant_q8_0", "skv_kv_dequant_q4_0", "skv_gather_rows", "skv_kv_append",
     "skv_attn_paged", "skv_bcache_create", "skv_bcache_destroy", "skv_bcache_reset", "skv_bcache_resolve",
     "skv_bcache_append", "skv_bcache_attn", "skv_bcache_stats", "skv_bcache_check", "skv_bcache_pool",
@@ -55,6 +55,7 @@ def _declare(lib):
         "skv_set_profile_events": ([P, P, P], ctypes.c_int),
         "skv_status": ([P, ctypes.POINTER(I32)], ctypes.c_int),
         "skv_plan_splits": ([I64, I64, I32, I32, I32, I64, ctypes.POINTER(I64), ctypes.POINTER(I32)], ctypes.c_int),
+        "skv_plan_prefill_splits": ([I64, I64, I32, I32, ctypes.POINTER(I64), ctypes.POINTER(I32)], ctypes.c_int),
         "skv_attn_partial": ([P, SH, P, P, P, P, I64, P, I64, P, I64, I32, I64, I64, P, P, P], ctypes.c_int),
         "skv_attn_combine": ([P, I32, P, P, I64, I32, P, P, P], ctypes.c_int),
         "skv_attn_window_tail": ([P, SH, P, P, P, I64, P, P, I64, I64, P, I64, P, P, P, P], ctypes.c_int),

@@ -134,7 +134,7 @@ int64_t segment_bytes(int type, int D)
 // The split count minimising waves x (tiles per split + overhead) wins; ties
 // go to fewer splits.
 int plan_splits_cost(int64_t n_keys, int64_t n_units, int sm_count, int ctas_per_sm, int tile, int64_t max_split,
-                     int overhead_tiles, int64_t *split_len, int32_t *n_splits)
+                     int overhead_tiles, int64_t *split_len, int32_t *n_splits, bool head_tail)
 {
     const int64_t tiles = (n_keys + tile - 1) / tile;
     const int64_t wave = static_cast<int64_t>(sm_count) * ctas_per_sm;
@@ -152,6 +152,27 @@ int plan_splits_cost(int64_t n_keys, int64_t n_units, int sm_count, int ctas_per
         if (best_tps < 0 || cost < best_cost - 1e-9) {
             best_cost = cost;
             best_tps = tps;
+        }
+    }
+    // Head and tail: with fewer units than CTA slots, each unit takes a long
+    // head split on the slots the units fill and a short tail split; the
+    // launch dispatches every head before any tail (the split index is the
+    // slowest grid dimension), so the slots the heads leave free run
+    // k = ceil(units / free) tails each while the heads run.  Cost: the
+    // longer of a head and k tails, plus the merge of the two partials.
+    if (head_tail && best_tps >= 0 && tiles >= 2 && n_units < wave) {
+        const int64_t free_slots = wave - n_units;
+        const int64_t k = (n_units + free_slots - 1) / free_slots;
+        const int64_t c = overhead_tiles;
+        const int64_t b0 = (tiles - (k - 1) * c) / (k + 1);
+        for (int64_t b = b0 - 1; b <= b0 + 2; ++b) {
+            const int64_t head = tiles - b;
+            if (b < 1 || head < b || head > max_tps) continue;
+            const double cost = static_cast<double>(std::max(head + c, k * (b + c)) + kMergeTiles);
+            if (cost < best_cost - 1e-9) {
+                best_cost = cost;
+                best_tps = head;
+            }
         }
     }
     if (best_tps < 0) best_tps = std::max<int64_t>(1, max_tps);
@@ -378,6 +399,24 @@ int skv_plan_splits(int64_t n_keys, int64_t n_units, int32_t sm_count, int32_t c
     return skv::plan_splits_cost(n_keys, n_units, sm_count, ctas_per_sm, tile, max_split, 1, split_len, n_splits);
 }
 
+int skv_plan_prefill_splits(int64_t n_keys, int64_t n_units, int32_t sm_count, int32_t k_type, int64_t *split_len,
+                            int32_t *n_splits)
+{
+    if (!split_len || !n_splits || n_keys < 0 || n_units <= 0 || sm_count <= 0 ||
+        (k_type != SKV_F16 && k_type != SKV_Q8_0 && k_type != SKV_Q4_0))
+        return SKV_EINVAL;
+    if (n_keys == 0) {
+        *split_len = skv::kPrefillTile;
+        *n_splits = 0;
+        return SKV_OK;
+    }
+    skv_shape sh;
+    memset(&sh, 0, sizeof(sh));
+    sh.k_type = k_type;
+    return skv::plan_splits_cost(n_keys, n_units, sm_count, 1, skv::kPrefillTile, 0, skv::prefill_overhead_tiles(&sh),
+                                 split_len, n_splits, true);
+}
+
 int skv_attn_combine(skv_handle *h, int32_t n_parts, const float *o_parts, const float *lse_parts, int64_t rows,
                      int32_t D, float *o, float *lse, void *stream)
 {
@@ -422,7 +461,7 @@ int skv_attn_partial(skv_handle *h, const skv_shape *shape, const void *q, const
         int64_t split_len = 0;
         int32_t n_splits = 0;
         if ((rc = plan_splits_cost(n_local, units_p, h->sm_count, 1, kPrefillTile, 0, prefill_overhead_tiles(shape),
-                                   &split_len, &n_splits)))
+                                   &split_len, &n_splits, true)))
             return fail(h, rc, "split planning failed");
         if (units_p > kMaxUnits) return fail(h, SKV_EUNSUPPORTED, "too many query tiles");
         PrefillLaunch L;
@@ -566,10 +605,11 @@ int skv_attn_window_tail(skv_handle *h, const skv_shape *shape, const void *q, c
     int64_t w_len = 0, t_len = 0;
     int32_t w_splits = 0, t_splits = 0;
     const int overhead = use_tc ? prefill_overhead_tiles(shape) : 1;
-    if ((rc = plan_splits_cost(n_win, units, h->sm_count, ctas, tile, 0, overhead, &w_len, &w_splits)))
+    if ((rc = plan_splits_cost(n_win, units, h->sm_count, ctas, tile, 0, overhead, &w_len, &w_splits, use_tc)))
         return fail(h, rc, "split planning failed");
     const int64_t n_tt = n_tail > 0 ? (n_tail + tile_rows - 1) / tile_rows : 0;
-    if (n_tt > 0 && (rc = plan_splits_cost(tile_rows, units, h->sm_count, ctas, tile, 0, overhead, &t_len, &t_splits)))
+    if (n_tt > 0 &&
+        (rc = plan_splits_cost(tile_rows, units, h->sm_count, ctas, tile, 0, overhead, &t_len, &t_splits, use_tc)))
         return fail(h, rc, "split planning failed");
     // One merged part per launch (window, then each tail tile); each launch's
     // splits merge inside the decode kernel.

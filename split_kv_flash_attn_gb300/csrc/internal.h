@@ -185,8 +185,11 @@ constexpr int kPrefillTile = 128;
 // lists) and seven beat one over q8_0 / q4_0 rows (667 against 710 us).
 inline int prefill_overhead_tiles(const skv_shape *sh) { return sh->k_type == SKV_F16 ? 10 : 4; }
 
+// Merge of a unit's split partials by its last CTA, in tiles, charged to a
+// head-and-tail plan (which replaces a single split's direct write).
+constexpr int kMergeTiles = 2;
 int plan_splits_cost(int64_t n_keys, int64_t n_units, int sm_count, int ctas_per_sm, int tile, int64_t max_split,
-                     int overhead_tiles, int64_t *split_len, int32_t *n_splits);
+                     int overhead_tiles, int64_t *split_len, int32_t *n_splits, bool head_tail = false);
 
 // Paged attention over local keys [key_lo, key_hi) of page lists of
 // pages_per_list pages (skv_attn_paged is the whole range).

@@ -101,8 +101,10 @@ int launch_prefill(skv_handle *h, const PrefillLaunch &L, cudaStream_t st)
     if (a.split_len % kPN) return fail(h, SKV_EINVAL, "prefill split length must be a multiple of %d", kPN);
     if (sh->Hk * a.m_tiles > 65535 || a.n_splits > 65535 || sh->S > 65535)
         return fail(h, SKV_EUNSUPPORTED, "prefill grid too large");
-    dim3 grid(static_cast<unsigned>(sh->Hk * a.m_tiles), static_cast<unsigned>(a.n_splits),
-              static_cast<unsigned>(sh->S));
+    // split index slowest: every CTA of split 0 is dispatched before any of
+    // split 1 (head-and-tail plans rely on it)
+    dim3 grid(static_cast<unsigned>(sh->Hk * a.m_tiles), static_cast<unsigned>(sh->S),
+              static_cast<unsigned>(a.n_splits));
     if ((reinterpret_cast<uintptr_t>(L.k) | reinterpret_cast<uintptr_t>(L.v)) % (f16 ? 16 : 8))
         return fail(h, SKV_EUNSUPPORTED, "K/V bases must be %d-byte aligned for the prefill kernel", f16 ? 16 : 8);
     if (!f16 || L.rows) return launch_prefill_sw(h, a, sh->k_type, sh->v_type, grid, st);

@@ -56,6 +56,9 @@
 //
 // The per-split result (O normalised, lse) is merged across splits by the
 // last CTA of each (sequence, KV head, query tile), as in the decode kernel.
+// Grid: x = (KV head, query tile), y = sequence, z = split, so that every CTA
+// of a split is dispatched before any CTA of the next (a long head split on
+// the SMs the query tiles fill, short tail splits on the SMs they leave).
 // Every mbarrier wait is bounded; a wait that gives up sets the handle's
 // device status word and the CTA stops issuing work, drains what it issued
 // and frees its TMEM.
@@ -330,8 +333,8 @@ __global__ void __launch_bounds__(Cfg<MODE>::kThreads, 1)
     const int lane = tid & 31;
     const int mt = blockIdx.x % a.m_tiles;
     const int kh = blockIdx.x / a.m_tiles;
-    const int split = blockIdx.y;
-    const int s = blockIdx.z;
+    const int split = blockIdx.z;
+    const int s = blockIdx.y;
     const int unit = (s * a.Hk + kh) * a.m_tiles + mt;
     const int tpt = kPM / a.G;                       // tokens per query tile
     const int64_t list = a.rows_per_head ? static_cast<int64_t>(s) * a.Hk + kh : s;

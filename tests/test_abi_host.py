@@ -93,6 +93,47 @@ def test_planner_empty_and_bad_args():
         plan_splits(10, 1, 152, 2, tile=64, max_split=32)
 
 
+def test_prefill_plan_head_and_tail():
+    # 128 query tiles (16 per KV head x 8 KV heads) over 32768 keys on 152
+    # SMs: one split leaves 24 SMs idle.  A head of 227 tiles per query tile
+    # and a tail of 29 let the 24 free SMs run six tails each (6 x (29 + 10)
+    # = 234 tile-times) within one head (227 + 10 = 237), against 256 + 10
+    # for one split; q8_0 keys (4 tiles of fixed cost): 223 + 33, against
+    # seven even splits of 37 tiles in six waves (6 x 41 = 246).
+    from split_kv_flash_attn_gb300 import F16, Q8_0, plan_prefill_splits
+    assert plan_prefill_splits(32768, 128, 152, F16) == (227 * 128, 2)
+    assert plan_prefill_splits(32768, 128, 152, Q8_0) == (223 * 128, 2)
+
+
+@pytest.mark.parametrize("n_keys,units", [
+    (32768, 128), (32768, 152), (32768, 304), (65536, 64), (1000, 8), (128, 128), (129, 100), (5 * 128, 151),
+    (1 << 20, 120), (32768, 1)])
+@pytest.mark.parametrize("k_type", [0, 1, 2])
+def test_prefill_plan_properties(n_keys, units, k_type):
+    from split_kv_flash_attn_gb300 import plan_prefill_splits
+    sl, ns = plan_prefill_splits(n_keys, units, 152, k_type)
+    tiles = -(-n_keys // 128)
+    assert sl % 128 == 0 and sl > 0
+    assert ns * sl >= n_keys and (ns - 1) * sl < n_keys     # covers, no empty split
+    if units >= 152:
+        assert ns == 1 or 2 * sl <= n_keys + 128 * (ns - 1)   # no head-and-tail pair once the SMs are full
+    if ns == 2 and 2 * sl > n_keys and units < 152:
+        # a head and a shorter tail: the free SMs' tails fit beside the heads
+        c = 10 if k_type == 0 else 4
+        head, tail = sl // 128, tiles - sl // 128
+        k = -(-units // (152 - units))
+        assert tail <= head
+        assert k * (tail + c) <= head + c + k + 1
+
+
+def test_prefill_plan_bad_args():
+    from split_kv_flash_attn_gb300 import SplitKVError, plan_prefill_splits
+    assert plan_prefill_splits(0, 4, 152)[1] == 0
+    for args in ((10, 0, 152, 0), (10, 1, 0, 0), (-1, 1, 152, 0), (10, 1, 152, 7)):
+        with pytest.raises(SplitKVError):
+            plan_prefill_splits(*args)
+
+
 def test_product_path_fails_loudly_without_library(tmp_path):
     from split_kv_flash_attn_gb300 import _lib
     with pytest.raises(ImportError):
