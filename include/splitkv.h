@@ -148,18 +148,22 @@ int skv_set_profile_events(skv_handle *h, void *before, void *after);
 int skv_plan_splits(int64_t n_keys, int64_t n_units, int32_t sm_count, int32_t ctas_per_sm,
                     int32_t tile, int64_t max_split, int64_t *split_len, int32_t *n_splits);
 
-/* The split plan of the tensor-core prefill path (many query rows per KV
- * head: skv_attn_partial and skv_attn_window_tail's window and tail tiles):
- * 128-key tiles, one CTA per SM, and a fixed cost per CTA of 10 tiles for
- * fp16 rows, 4 for q8_0 / q4_0 rows (k_type).  Besides the even splits of
- * skv_plan_splits it weighs a head and a tail per unit when the n_units
- * query tiles leave some of the sm_count SMs free: a long head split for
- * every unit, then a short tail split for every unit that the free SMs run
+/* The split plan a call of this shape over n_keys keys gets on the
+ * tensor-core prefill path (many query rows per KV head: skv_attn_partial
+ * and skv_attn_window_tail's window and tail tiles) on sm_count SMs; rows
+ * != 0: the keys come through row lists.  One CTA takes a 128-row query tile
+ * of a KV head (dense q8_0 / q4_0 keys with q4_0 values: a pair of query
+ * tiles) and one split of 128-key tiles, one CTA per SM, at a fixed cost per
+ * CTA of 10 tiles (fp16 rows, query-tile pairs) or 4 (other quantised
+ * rows).  Besides the even splits of skv_plan_splits the plan weighs a head
+ * and a tail split per unit when the units leave some SMs free: a long head
+ * for every unit, then a short tail for every unit that the free SMs run
  * while the heads do (n_splits = 2, split_len = the head's keys).
- * n_keys = 0 gives *n_splits = 0.  SKV_EINVAL on a NULL output, a negative
- * n_keys, n_units or sm_count below 1, or an unknown k_type. */
-int skv_plan_prefill_splits(int64_t n_keys, int64_t n_units, int32_t sm_count, int32_t k_type,
-                            int64_t *split_len, int32_t *n_splits);
+ * *n_ctas = units x n_splits.  n_keys = 0 gives *n_splits = 0.  SKV_EINVAL
+ * on a NULL pointer, negative n_keys, sm_count below 1 or an invalid shape;
+ * SKV_EUNSUPPORTED when the shape does not take the tensor-core path. */
+int skv_plan_prefill_splits(const skv_shape *shape, int64_t n_keys, int32_t sm_count, int32_t rows,
+                            int64_t *split_len, int32_t *n_splits, int64_t *n_ctas);
 
 /* Resident window size ("Rolling KV" page, position-axis residency sizing).
  * budget = min(free_bytes, target_bytes if > 0) - reserve_bytes (floored at

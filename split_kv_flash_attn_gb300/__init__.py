@@ -113,15 +113,17 @@ class Handle:
             pass
 
 
-def plan_prefill_splits(n_keys, n_units, sm_count, k_type=F16):
-    """The tensor-core prefill path's split plan (no GPU needed): returns
-    (split_len, n_splits)."""
-    sl, ns = ctypes.c_int64(), ctypes.c_int32()
-    rc = _lib.lib().skv_plan_prefill_splits(int(n_keys), int(n_units), int(sm_count), int(k_type), ctypes.byref(sl),
-                                            ctypes.byref(ns))
+def plan_prefill_splits(S, nq, H, Hk, n_keys, sm_count, *, k_type=F16, v_type=F16, D=128, rows=False):
+    """The split plan a prefill call of this shape gets on the tensor-core
+    path (no GPU needed): returns (split_len, n_splits, n_ctas)."""
+    sh = SkvShape(int(S), int(nq), int(H), int(Hk), int(D), 1.0 / math.sqrt(D), int(k_type), int(v_type),
+                  int(Hk) * segment_bytes(k_type, D), int(Hk) * segment_bytes(v_type, D))
+    sl, ns, nc = ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int64()
+    rc = _lib.lib().skv_plan_prefill_splits(ctypes.byref(sh), int(n_keys), int(sm_count), int(bool(rows)),
+                                            ctypes.byref(sl), ctypes.byref(ns), ctypes.byref(nc))
     if rc != 0:
         raise SplitKVError(rc, "skv_plan_prefill_splits rejected its arguments")
-    return sl.value, ns.value
+    return sl.value, ns.value, nc.value
 
 
 def plan_splits(n_keys, n_units, sm_count, ctas_per_sm, tile=64, max_split=0):

@@ -55,7 +55,8 @@ def _declare(lib):
         "skv_set_profile_events": ([P, P, P], ctypes.c_int),
         "skv_status": ([P, ctypes.POINTER(I32)], ctypes.c_int),
         "skv_plan_splits": ([I64, I64, I32, I32, I32, I64, ctypes.POINTER(I64), ctypes.POINTER(I32)], ctypes.c_int),
-        "skv_plan_prefill_splits": ([I64, I64, I32, I32, ctypes.POINTER(I64), ctypes.POINTER(I32)], ctypes.c_int),
+        "skv_plan_prefill_splits": ([SH, I64, I32, I32, ctypes.POINTER(I64), ctypes.POINTER(I32), ctypes.POINTER(I64)],
+                                    ctypes.c_int),
         "skv_attn_partial": ([P, SH, P, P, P, P, I64, P, I64, P, I64, I32, I64, I64, P, P, P], ctypes.c_int),
         "skv_attn_combine": ([P, I32, P, P, I64, I32, P, P, P], ctypes.c_int),
         "skv_attn_window_tail": ([P, SH, P, P, P, I64, P, P, I64, I64, P, I64, P, P, P, P], ctypes.c_int),

@@ -399,22 +399,24 @@ int skv_plan_splits(int64_t n_keys, int64_t n_units, int32_t sm_count, int32_t c
     return skv::plan_splits_cost(n_keys, n_units, sm_count, ctas_per_sm, tile, max_split, 1, split_len, n_splits);
 }
 
-int skv_plan_prefill_splits(int64_t n_keys, int64_t n_units, int32_t sm_count, int32_t k_type, int64_t *split_len,
-                            int32_t *n_splits)
+int skv_plan_prefill_splits(const skv_shape *shape, int64_t n_keys, int32_t sm_count, int32_t rows,
+                            int64_t *split_len, int32_t *n_splits, int64_t *n_ctas)
 {
-    if (!split_len || !n_splits || n_keys < 0 || n_units <= 0 || sm_count <= 0 ||
-        (k_type != SKV_F16 && k_type != SKV_Q8_0 && k_type != SKV_Q4_0))
+    if (!shape || !split_len || !n_splits || !n_ctas || n_keys < 0 || sm_count <= 0 || shape->S < 1 ||
+        shape->nq < 1 || shape->Hk < 1 || shape->H < shape->Hk || shape->H % shape->Hk)
         return SKV_EINVAL;
+    if (!skv::prefill_eligible(shape, nullptr)) return SKV_EUNSUPPORTED;
+    const int64_t units = static_cast<int64_t>(shape->S) * skv::prefill_units(shape, rows != 0);
     if (n_keys == 0) {
         *split_len = skv::kPrefillTile;
         *n_splits = 0;
+        *n_ctas = 0;
         return SKV_OK;
     }
-    skv_shape sh;
-    memset(&sh, 0, sizeof(sh));
-    sh.k_type = k_type;
-    return skv::plan_splits_cost(n_keys, n_units, sm_count, 1, skv::kPrefillTile, 0, skv::prefill_overhead_tiles(&sh),
-                                 split_len, n_splits, true);
+    const int rc = skv::plan_splits_cost(n_keys, units, sm_count, 1, skv::kPrefillTile, 0,
+                                         skv::prefill_overhead_tiles(shape, rows != 0), split_len, n_splits, true);
+    if (rc == SKV_OK) *n_ctas = units * *n_splits;
+    return rc;
 }
 
 int skv_attn_combine(skv_handle *h, int32_t n_parts, const float *o_parts, const float *lse_parts, int64_t rows,
@@ -457,11 +459,11 @@ int skv_attn_partial(skv_handle *h, const skv_shape *shape, const void *q, const
     if (prefill_eligible(shape, mask)) {
         // Many query rows per KV head: the tensor-core path (dense fp16 ranges
         // by TMA; row lists and quantised rows by its software producers).
-        const int64_t units_p = static_cast<int64_t>(shape->S) * prefill_units(shape);
+        const int64_t units_p = static_cast<int64_t>(shape->S) * prefill_units(shape, kv_rows != nullptr);
         int64_t split_len = 0;
         int32_t n_splits = 0;
-        if ((rc = plan_splits_cost(n_local, units_p, h->sm_count, 1, kPrefillTile, 0, prefill_overhead_tiles(shape),
-                                   &split_len, &n_splits, true)))
+        if ((rc = plan_splits_cost(n_local, units_p, h->sm_count, 1, kPrefillTile, 0,
+                                   prefill_overhead_tiles(shape, kv_rows != nullptr), &split_len, &n_splits, true)))
             return fail(h, rc, "split planning failed");
         if (units_p > kMaxUnits) return fail(h, SKV_EUNSUPPORTED, "too many query tiles");
         PrefillLaunch L;
@@ -597,14 +599,14 @@ int skv_attn_window_tail(skv_handle *h, const skv_shape *shape, const void *q, c
                      : use_rows ? decode_rows_ctas_per_sm(shape)
                                 : decode_ctas_per_sm(h, shape->k_type, shape->v_type, D);
     if (ctas <= 0) return fail(h, SKV_EUNSUPPORTED, "no decode kernel for this type pairing / head dim");
-    const int64_t units = use_tc ? static_cast<int64_t>(shape->S) * prefill_units(shape)
+    const int64_t units = use_tc ? static_cast<int64_t>(shape->S) * prefill_units(shape, false)
                           : use_rows ? static_cast<int64_t>(shape->S) * n_cg
                                      : static_cast<int64_t>(shape->S) * shape->Hk * n_cg;
     const int tile = use_tc ? kPrefillTile : use_rows ? kRowsTile : kDecodeTile;
 
     int64_t w_len = 0, t_len = 0;
     int32_t w_splits = 0, t_splits = 0;
-    const int overhead = use_tc ? prefill_overhead_tiles(shape) : 1;
+    const int overhead = use_tc ? prefill_overhead_tiles(shape, false) : 1;
     if ((rc = plan_splits_cost(n_win, units, h->sm_count, ctas, tile, 0, overhead, &w_len, &w_splits, use_tc)))
         return fail(h, rc, "split planning failed");
     const int64_t n_tt = n_tail > 0 ? (n_tail + tile_rows - 1) / tile_rows : 0;

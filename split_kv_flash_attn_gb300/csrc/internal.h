@@ -173,7 +173,14 @@ struct PrefillLaunch {
     int rows_per_head;
 };
 bool prefill_eligible(const skv_shape *sh, const void *mask);
-int prefill_units(const skv_shape *sh);    // (KV head, 128-row query tile) pairs per sequence
+// Whether the two-query-tile instance serves a call: dense q8_0 / q4_0 keys
+// with q4_0 values over at least two query tiles (`rows`: the keys come
+// through row lists).
+bool prefill_pairs(const skv_shape *sh, bool rows);
+// CTA units per sequence: (KV head, 128-row query tile), or (KV head, pair of
+// query tiles) where the two-query-tile instance serves (dense q8_0 / q4_0
+// keys with q4_0 values; `rows`: the keys come through row lists)
+int prefill_units(const skv_shape *sh, bool rows);
 int launch_prefill(skv_handle *h, const PrefillLaunch &L, cudaStream_t st);
 constexpr int kPrefillTile = 128;
 // Per-CTA fixed cost of the prefill kernel in 128-key tiles (TMEM allocation,
@@ -183,7 +190,14 @@ constexpr int kPrefillTile = 128;
 // 128 query tiles over 32768 keys on 152 SMs, where one split per tile beat
 // seven (312 against 331 us over fp16 rows, 363 against 397 us over fp16 row
 // lists) and seven beat one over q8_0 / q4_0 rows (667 against 710 us).
-inline int prefill_overhead_tiles(const skv_shape *sh) { return sh->k_type == SKV_F16 ? 10 : 4; }
+// The two-query-tile instance (dense q8_0 / q4_0 keys with q4_0 values)
+// takes ~3.6 us a key tile for both query tiles: one wave of two splits per
+// pair (128 CTAs, 463 us) beat seven splits in three waves (492 us) over the
+// 512-token, 32768-row window, which a fixed cost of 10 tiles picks.
+inline int prefill_overhead_tiles(const skv_shape *sh, bool rows)
+{
+    return (sh->k_type == SKV_F16 || prefill_pairs(sh, rows)) ? 10 : 4;
+}
 
 // Merge of a unit's split partials by its last CTA, in tiles, charged to a
 // head-and-tail plan (which replaces a single split's direct write).

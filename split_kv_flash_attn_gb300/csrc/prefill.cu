@@ -59,7 +59,19 @@ bool prefill_eligible(const skv_shape *sh, const void *mask)
            sh->v_row_bytes % al == 0;
 }
 
-int prefill_units(const skv_shape *sh) { return sh->Hk * ((sh->nq * (sh->H / sh->Hk) + kPM - 1) / kPM); }
+// Dense q8_0 / q4_0 keys with q4_0 values and at least two query tiles: the
+// two-query-tile instance, which decodes each K and V tile once for both.
+bool prefill_pairs(const skv_shape *sh, bool rows)
+{
+    const int m_tiles = (sh->nq * (sh->H / sh->Hk) + kPM - 1) / kPM;
+    return !rows && (sh->k_type == SKV_Q8_0 || sh->k_type == SKV_Q4_0) && sh->v_type == SKV_Q4_0 && m_tiles >= 2;
+}
+
+int prefill_units(const skv_shape *sh, bool rows)
+{
+    const int m_tiles = (sh->nq * (sh->H / sh->Hk) + kPM - 1) / kPM;
+    return sh->Hk * (prefill_pairs(sh, rows) ? (m_tiles + 1) / 2 : m_tiles);
+}
 
 int launch_prefill(skv_handle *h, const PrefillLaunch &L, cudaStream_t st)
 {
@@ -107,6 +119,11 @@ int launch_prefill(skv_handle *h, const PrefillLaunch &L, cudaStream_t st)
               static_cast<unsigned>(a.n_splits));
     if ((reinterpret_cast<uintptr_t>(L.k) | reinterpret_cast<uintptr_t>(L.v)) % (f16 ? 16 : 8))
         return fail(h, SKV_EUNSUPPORTED, "K/V bases must be %d-byte aligned for the prefill kernel", f16 ? 16 : 8);
+    if (prefill_pairs(sh, L.rows != nullptr)) {
+        const int n_pairs = (a.m_tiles + 1) / 2;
+        return launch_prefill_pairq(h, a, sh->k_type,
+                                    dim3(static_cast<unsigned>(sh->Hk * n_pairs), grid.y, grid.z), st);
+    }
     if (!f16 || L.rows) return launch_prefill_sw(h, a, sh->k_type, sh->v_type, grid, st);
     CUtensorMap mk, mv;
     int rc = make_map(h, &mk, L.k, L.n_rows, sh->Hk, sh->k_row_bytes);

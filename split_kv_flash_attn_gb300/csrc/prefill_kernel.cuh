@@ -1081,6 +1081,9 @@ int launch_prefill_t(skv_handle *h, const CUtensorMap &mk, const CUtensorMap &mv
 
 // Software-producer instances (prefill_sw.cu).
 int launch_prefill_sw(skv_handle *h, const PrefillArgs &a, int kt, int vt, dim3 grid, cudaStream_t st);
+// Two query tiles per CTA over dense q8_0 / q4_0 keys and q4_0 values
+// (prefill_pairq.cu); grid x = (KV head, query-tile pair).
+int launch_prefill_pairq(skv_handle *h, const PrefillArgs &a, int kt, dim3 grid, cudaStream_t st);
 
 }  // namespace pf
 }  // namespace skv

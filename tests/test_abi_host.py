@@ -94,32 +94,44 @@ def test_planner_empty_and_bad_args():
 
 
 def test_prefill_plan_head_and_tail():
-    # 128 query tiles (16 per KV head x 8 KV heads) over 32768 keys on 152
-    # SMs: one split leaves 24 SMs idle.  A head of 227 tiles per query tile
-    # and a tail of 29 let the 24 free SMs run six tails each (6 x (29 + 10)
-    # = 234 tile-times) within one head (227 + 10 = 237), against 256 + 10
-    # for one split; q8_0 keys (4 tiles of fixed cost): 223 + 33, against
-    # seven even splits of 37 tiles in six waves (6 x 41 = 246).
-    from split_kv_flash_attn_gb300 import F16, Q8_0, plan_prefill_splits
-    assert plan_prefill_splits(32768, 128, 152, F16) == (227 * 128, 2)
-    assert plan_prefill_splits(32768, 128, 152, Q8_0) == (223 * 128, 2)
+    # 512 tokens x 32 q heads over 8 KV heads make 128 query tiles (16 per KV
+    # head) over 32768 keys on 152 SMs: one split leaves 24 SMs idle.  A head
+    # of 227 tiles per query tile and a tail of 29 let the 24 free SMs run
+    # six tails each (6 x (29 + 10) = 234 tile-times) within one head (227 +
+    # 10 = 237), against 256 + 10 for one split.  Over q8_0 keys and values
+    # (4 tiles of fixed cost): 223 + 33, against seven even splits of 37
+    # tiles in six waves (6 x 41 = 246).  Over q8_0 keys with q4_0 values the
+    # CTAs take query-tile pairs (64 units): two even splits, one wave.
+    # Eight sequences of 64 tokens through row lists: 128 units again.
+    from split_kv_flash_attn_gb300 import F16, Q4_0, Q8_0, plan_prefill_splits
+    assert plan_prefill_splits(1, 512, 32, 8, 32768, 152) == (227 * 128, 2, 256)
+    assert plan_prefill_splits(1, 512, 32, 8, 32768, 152, k_type=Q8_0, v_type=Q8_0) == (223 * 128, 2, 256)
+    assert plan_prefill_splits(1, 512, 32, 8, 32768, 152, k_type=Q8_0, v_type=Q4_0) == (128 * 128, 2, 128)
+    assert plan_prefill_splits(8, 64, 32, 8, 32768, 152, rows=True) == (227 * 128, 2, 256)
+    # row lists of quantised rows stay one query tile a CTA
+    assert plan_prefill_splits(1, 512, 32, 8, 32768, 152, k_type=Q8_0, v_type=Q4_0, rows=True)[2] % 128 == 0
 
 
-@pytest.mark.parametrize("n_keys,units", [
-    (32768, 128), (32768, 152), (32768, 304), (65536, 64), (1000, 8), (128, 128), (129, 100), (5 * 128, 151),
-    (1 << 20, 120), (32768, 1)])
-@pytest.mark.parametrize("k_type", [0, 1, 2])
-def test_prefill_plan_properties(n_keys, units, k_type):
+@pytest.mark.parametrize("S,nq,n_keys", [
+    (1, 512, 32768), (1, 512 * 19 // 16, 32768), (4, 512, 32768), (1, 1024, 65536), (8, 64, 1000), (1, 32, 128),
+    (2, 80, 129), (1, 152 * 8, 5 * 128), (1, 480, 1 << 20), (1, 64, 32768)])
+@pytest.mark.parametrize("kt,vt", [(0, 0), (1, 1), (1, 2), (2, 2), (2, 1)])
+def test_prefill_plan_properties(S, nq, n_keys, kt, vt):
     from split_kv_flash_attn_gb300 import plan_prefill_splits
-    sl, ns = plan_prefill_splits(n_keys, units, 152, k_type)
+    H, Hk = 32, 8
+    sl, ns, nc = plan_prefill_splits(S, nq, H, Hk, n_keys, 152, k_type=kt, v_type=vt)
     tiles = -(-n_keys // 128)
+    q_tiles = Hk * -(-nq * (H // Hk) // 128)
+    pairs = kt != 0 and vt == 2 and q_tiles // Hk >= 2
+    units = S * (Hk * -(-(q_tiles // Hk) // 2) if pairs else q_tiles)
+    assert nc == units * ns
     assert sl % 128 == 0 and sl > 0
     assert ns * sl >= n_keys and (ns - 1) * sl < n_keys     # covers, no empty split
     if units >= 152:
         assert ns == 1 or 2 * sl <= n_keys + 128 * (ns - 1)   # no head-and-tail pair once the SMs are full
-    if ns == 2 and 2 * sl > n_keys and units < 152:
+    if ns == 2 and 2 * sl > n_keys + 128 and units < 152:
         # a head and a shorter tail: the free SMs' tails fit beside the heads
-        c = 10 if k_type == 0 else 4
+        c = 10 if (kt == 0 or pairs) else 4
         head, tail = sl // 128, tiles - sl // 128
         k = -(-units // (152 - units))
         assert tail <= head
@@ -128,10 +140,12 @@ def test_prefill_plan_properties(n_keys, units, k_type):
 
 def test_prefill_plan_bad_args():
     from split_kv_flash_attn_gb300 import SplitKVError, plan_prefill_splits
-    assert plan_prefill_splits(0, 4, 152)[1] == 0
-    for args in ((10, 0, 152, 0), (10, 1, 0, 0), (-1, 1, 152, 0), (10, 1, 152, 7)):
+    assert plan_prefill_splits(1, 512, 32, 8, 0, 152)[1] == 0
+    for args, kw in (((1, 512, 32, 8, -1, 152), {}), ((1, 512, 32, 8, 10, 0), {}), ((0, 512, 32, 8, 10, 152), {}),
+                     ((1, 512, 32, 7, 10, 152), {}), ((1, 512, 32, 8, 10, 152), {"D": 64}),
+                     ((1, 8, 32, 8, 10, 152), {})):
         with pytest.raises(SplitKVError):
-            plan_prefill_splits(*args)
+            plan_prefill_splits(*args, **kw)
 
 
 def test_product_path_fails_loudly_without_library(tmp_path):

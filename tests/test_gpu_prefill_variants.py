@@ -65,6 +65,30 @@ def test_prefill_quant_dense(skv, h, oracle_mod, kt, vt):
     assert h.status() == 0
 
 
+@pytest.mark.parametrize("kt", [wl.Q8_0, wl.Q4_0])
+def test_prefill_quant_query_tile_pairs_ragged(skv, h, oracle_mod, kt):
+    """Dense q8_0 / q4_0 keys with q4_0 values are served two query tiles a
+    CTA: 80 tokens x 4 heads make three 128-row tiles, so the last pair has
+    one tile, itself ragged (64 of its rows past the last token); two
+    sequences, causal positions inside a sub-range whose ends are ragged
+    against the 128-key tiles, and a range long enough to be split."""
+    vt = wl.Q4_0
+    rng = wl.generator(4, salt=330 + kt)
+    S, nq, H, Hk, n = 2, 80, 16, 4, 9000
+    q = wl.normal_f16(rng, (S, nq, H, D))
+    K = wl.cache_rows(rng, kt, n, Hk, D)
+    V = wl.cache_rows(rng, vt, n, Hk, D)
+    b, e, kp0 = 45, 8931, 11
+    q_pos = np.stack([np.sort(rng.integers(e + kp0 - 600, e + kp0 + 5, size=nq)) for _ in range(S)]).astype(np.int32)
+    o, l = skv.attn_partial(h, dev(q), dev(K), dev(V), Hk=Hk, k_type=kt, v_type=vt, kv_begin=b, kv_end=e,
+                            q_pos=dev(q_pos), key_pos0=kp0)
+    rows = np.tile(np.arange(b, e, dtype=np.int32), (S, 1))
+    want_o, want_l = _oracle(oracle_mod, q, H, Hk, kt, vt, K, V, n, n_keys=e - b, kv_rows=rows, q_pos=q_pos,
+                             key_pos0=kp0 + b)
+    check_attention(o, l, want_o, want_l, vmax_of(oracle_mod, vt, V, D), "query-tile pairs")
+    assert h.status() == 0
+
+
 def test_prefill_quant_window_tail(skv, h, oracle_mod):
     """Prefill over a q8_0 / q4_0 window and a pinned quantised tail streamed
     in 768-row tiles (the long-context layout at reduced size)."""
