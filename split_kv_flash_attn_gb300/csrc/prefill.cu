@@ -1,7 +1,9 @@
 // prefill.cu -- host side of the tensor-core prefill kernel
 // (prefill_kernel.cuh): eligibility, tensor maps, split arguments, and the
-// TMA instance over dense fp16 regions.  Row lists and quantised rows use
-// the software-producer instances in prefill_sw.cu.
+// TMA instance over dense fp16 regions.  Dense q8_0 / q4_0 keys with q4_0
+// values over two or more query tiles use the two-query-tile instance
+// (prefill_pairq.cu); other row lists and quantised rows the
+// software-producer instances in prefill_sw.cu.
 #include "prefill_kernel.cuh"
 
 namespace skv {

@@ -1,6 +1,7 @@
 // prefill_sw.cu -- software-producer instances of the tensor-core prefill
-// kernel: fp16 rows through row lists (MODE 2), and q8_0 / q4_0 rows (dense
-// or listed) decoded into the fp16 operand tiles (MODE 1).
+// kernel: fp16 rows through row lists (MODE 2), and q8_0 / q4_0 rows (listed,
+// or dense with q8_0 values or a single query tile) decoded into the fp16
+// operand tiles (MODE 1).
 #include "prefill_kernel.cuh"
 
 namespace skv {
