@@ -155,10 +155,11 @@ int skv_plan_splits(int64_t n_keys, int64_t n_units, int32_t sm_count, int32_t c
  * of a KV head (dense q8_0 / q4_0 keys with q4_0 values: a pair of query
  * tiles) and one split of 128-key tiles, one CTA per SM, at a fixed cost per
  * CTA of 10 tiles (fp16 rows, query-tile pairs) or 4 (other quantised
- * rows).  Besides the even splits of skv_plan_splits the plan weighs a head
- * and a tail split per unit when the units leave some SMs free: a long head
- * for every unit, then a short tail for every unit that the free SMs run
- * while the heads do (n_splits = 2, split_len = the head's keys).
+ * rows).  Besides the even splits of skv_plan_splits the plan weighs m head
+ * splits and a tail split per unit when the units' heads leave some SMs
+ * free: long heads for every unit, then a short tail for every unit that the
+ * free SMs run while the heads do (n_splits = m + 1, split_len = a head's
+ * keys).
  * *n_ctas = units x n_splits.  n_keys = 0 gives *n_splits = 0.  SKV_EINVAL
  * on a NULL pointer, negative n_keys, sm_count below 1 or an invalid shape;
  * SKV_EUNSUPPORTED when the shape does not take the tensor-core path. */

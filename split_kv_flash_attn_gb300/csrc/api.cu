@@ -154,24 +154,30 @@ int plan_splits_cost(int64_t n_keys, int64_t n_units, int sm_count, int ctas_per
             best_tps = tps;
         }
     }
-    // Head and tail: with fewer units than CTA slots, each unit takes a long
-    // head split on the slots the units fill and a short tail split; the
-    // launch dispatches every head before any tail (the split index is the
-    // slowest grid dimension), so the slots the heads leave free run
-    // k = ceil(units / free) tails each while the heads run.  Cost: the
-    // longer of a head and k tails, plus the merge of the two partials.
-    if (head_tail && best_tps >= 0 && tiles >= 2 && n_units < wave) {
-        const int64_t free_slots = wave - n_units;
-        const int64_t k = (n_units + free_slots - 1) / free_slots;
+    // Heads and a tail: with fewer units than CTA slots, each unit takes m
+    // long head splits on the slots the units' heads fill and one short
+    // tail split; the launch dispatches every head before any tail (the
+    // split index is the slowest grid dimension), so the slots the heads
+    // leave free run k = ceil(units / free) tails each while the heads run.
+    // Cost: the longer of a head and k tails, plus the merge of the parts.
+    // With fixed cost c per CTA, head + c = k (tail + c) and m heads + tail
+    // = tiles balance at tail = (tiles - m c (k - 1)) / (1 + m k).
+    if (head_tail && best_tps >= 0 && tiles >= 2) {
         const int64_t c = overhead_tiles;
-        const int64_t b0 = (tiles - (k - 1) * c) / (k + 1);
-        for (int64_t b = b0 - 1; b <= b0 + 2; ++b) {
-            const int64_t head = tiles - b;
-            if (b < 1 || head < b || head > max_tps) continue;
-            const double cost = static_cast<double>(std::max(head + c, k * (b + c)) + kMergeTiles);
-            if (cost < best_cost - 1e-9) {
-                best_cost = cost;
-                best_tps = head;
+        for (int64_t m = 1; n_units * m < wave && m < tiles; ++m) {
+            const int64_t free_slots = wave - n_units * m;
+            const int64_t k = (n_units + free_slots - 1) / free_slots;
+            const int64_t b0 = (tiles - m * c * (k - 1)) / (1 + m * k);
+            for (int64_t b = b0 - 1; b <= b0 + 2; ++b) {
+                if (b < 1 || b >= tiles) continue;
+                const int64_t head = (tiles - b + m - 1) / m;
+                if (head < b || head > max_tps || (tiles + head - 1) / head != m + 1) continue;
+                const int64_t tail = tiles - m * head;
+                const double cost = static_cast<double>(std::max(head + c, k * (tail + c)) + kMergeTiles);
+                if (cost < best_cost - 1e-9) {
+                    best_cost = cost;
+                    best_tps = head;
+                }
             }
         }
     }

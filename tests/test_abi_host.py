@@ -101,12 +101,15 @@ def test_prefill_plan_head_and_tail():
     # 10 = 237), against 256 + 10 for one split.  Over q8_0 keys and values
     # (4 tiles of fixed cost): 223 + 33, against seven even splits of 37
     # tiles in six waves (6 x 41 = 246).  Over q8_0 keys with q4_0 values the
-    # CTAs take query-tile pairs (64 units): two even splits, one wave.
-    # Eight sequences of 64 tokens through row lists: 128 units again.
+    # CTAs take query-tile pairs (64 units, 10 tiles of fixed cost): two heads
+    # of 113 tiles per pair fill 128 SMs and the 24 others run the 64 tails of
+    # 30, three each (3 x 40 = 120 <= 113 + 10), against 128 + 10 for two
+    # even splits.  Eight sequences of 64 tokens through row lists: 128 units
+    # again.
     from split_kv_flash_attn_gb300 import F16, Q4_0, Q8_0, plan_prefill_splits
     assert plan_prefill_splits(1, 512, 32, 8, 32768, 152) == (227 * 128, 2, 256)
     assert plan_prefill_splits(1, 512, 32, 8, 32768, 152, k_type=Q8_0, v_type=Q8_0) == (223 * 128, 2, 256)
-    assert plan_prefill_splits(1, 512, 32, 8, 32768, 152, k_type=Q8_0, v_type=Q4_0) == (128 * 128, 2, 128)
+    assert plan_prefill_splits(1, 512, 32, 8, 32768, 152, k_type=Q8_0, v_type=Q4_0) == (113 * 128, 3, 192)
     assert plan_prefill_splits(8, 64, 32, 8, 32768, 152, rows=True) == (227 * 128, 2, 256)
     # row lists of quantised rows stay one query tile a CTA
     assert plan_prefill_splits(1, 512, 32, 8, 32768, 152, k_type=Q8_0, v_type=Q4_0, rows=True)[2] % 128 == 0
@@ -128,14 +131,13 @@ def test_prefill_plan_properties(S, nq, n_keys, kt, vt):
     assert sl % 128 == 0 and sl > 0
     assert ns * sl >= n_keys and (ns - 1) * sl < n_keys     # covers, no empty split
     if units >= 152:
-        assert ns == 1 or 2 * sl <= n_keys + 128 * (ns - 1)   # no head-and-tail pair once the SMs are full
-    if ns == 2 and 2 * sl > n_keys + 128 and units < 152:
-        # a head and a shorter tail: the free SMs' tails fit beside the heads
+        assert ns == 1 or 2 * sl <= n_keys + 128 * (ns - 1)   # no heads-and-tail plan once the SMs are full
+    head, tail = sl // 128, tiles - (ns - 1) * (sl // 128)
+    if ns >= 2 and units * (ns - 1) < 152 and 2 * tail < head:
+        # heads and a much shorter tail: the free SMs' tails fit beside the heads
         c = 10 if (kt == 0 or pairs) else 4
-        head, tail = sl // 128, tiles - sl // 128
-        k = -(-units // (152 - units))
-        assert tail <= head
-        assert k * (tail + c) <= head + c + k + 1
+        k = -(-units // (152 - units * (ns - 1)))
+        assert k * (tail + c) <= head + c + k * (ns - 1) + 1
 
 
 def test_prefill_plan_bad_args():
