@@ -191,9 +191,10 @@ constexpr int kPrefillTile = 128;
 // seven (312 against 331 us over fp16 rows, 363 against 397 us over fp16 row
 // lists) and seven beat one over q8_0 / q4_0 rows (667 against 710 us).
 // The two-query-tile instance (dense q8_0 / q4_0 keys with q4_0 values)
-// takes ~3.6 us a key tile for both query tiles: one wave of two splits per
-// pair (128 CTAs, 463 us) beat seven splits in three waves (492 us) over the
-// 512-token, 32768-row window, which a fixed cost of 10 tiles picks.
+// takes ~3.6 us a key tile for both query tiles: over the 512-token,
+// 32768-row window one wave of two even splits per pair (128 CTAs, 463 us)
+// beat seven splits in three waves (492 us), and two heads and a tail per
+// pair (192 CTAs, 417 us) beat both; a fixed cost of 10 tiles picks that.
 inline int prefill_overhead_tiles(const skv_shape *sh, bool rows)
 {
     return (sh->k_type == SKV_F16 || prefill_pairs(sh, rows)) ? 10 : 4;
